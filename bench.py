@@ -1,0 +1,454 @@
+"""Benchmark: GQA split-KV decode on GB300.
+
+One step = one decode call over the workload (contiguous: ``gqa_decode``, the
+split-KV partial pass with the in-kernel merge; paged: ``gqa_decode_paged``),
+inputs resident in HBM.  The headline workload is the long-context single
+sequence (S_kv = 2^20, h_q = 32, h_kv = 8, d_head = 128, ~4 GiB of f16 K+V).
+
+Printed (rank 0, one JSON line): KV-cache read GB/s over the whole job
+(bytes = K + V + Q + O per step, plus block tables and lengths when paged),
+microseconds per step, the roofline of the kernel against the measured HBM
+copy bandwidth, the same metric end to end from pinned host buffers, and the
+CPU float64 oracle timed on the host cores as a reported baseline.
+
+``--impl reference`` times the oracle instead (host cores, bounded samples of
+the same workload, same metric).  Multi-GPU runs (torchrun) are independent
+replicas: every rank runs the whole workload on its own GPU, nothing is
+exchanged; ``value`` sums the ranks' bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gqa_inputs as gi  # noqa: E402
+
+METRIC = "KV-cache read GB/s (fraction of GB300 HBM peak); µs per decode step"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(gi.WORKLOADS), default="long")
+    ap.add_argument("--n-splits", type=int, default=0)
+    ap.add_argument("--merge-mode", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "decode_attention_03_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        time.sleep(0.15)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        inside = [p for (t, p) in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        use = inside if inside else [p for (_, p) in self.samples]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(p[1]) for p in use if p[1].replace(".", "").isdigit()]
+        mx = [float(p[2]) for p in use if p[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for p in use:
+            for i, n in enumerate(names):
+                if p[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(use), "in_window": bool(inside)}
+
+
+# ---------------------------------------------------------------------------------------------
+def load_inputs(name: str):
+    w = gi.WORKLOADS[name]
+    x = gi.make(w)
+    return w, x
+
+
+def to_device(x: dict, dev):
+    keys = ("q", "k", "v") if "k" in x else ("q", "k_pool", "v_pool", "block_tables", "seq_lens")
+    return {k: torch.from_numpy(np.ascontiguousarray(x[k])).to(dev) for k in keys}
+
+
+def make_step(pkg, w, x, d, out, ws, args):
+    if w.kind == "contiguous":
+        def step():
+            pkg.gqa_decode(d["q"], d["k"], d["v"], w.h_q, w.h_kv, w.scale, out=out, workspace_tensor=ws,
+                           n_splits=args.n_splits, merge_mode=args.merge_mode)
+    else:
+        q2 = d["q"].reshape(w.batch, -1)
+
+        def step():
+            pkg.gqa_decode_paged(q2, d["k_pool"], d["v_pool"], d["block_tables"], d["seq_lens"], w.h_q, w.h_kv,
+                                 w.scale, max_seq_len=x["max_seq_len"], partition_size=w.partition_size,
+                                 out=out, workspace_tensor=ws)
+    return step
+
+
+def oracle_sample(x, w, target_s: float):
+    """Time the CPU oracle on a bounded sample of the workload; returns (bytes/s, desc, threads)."""
+    import oracle
+    threads = os.cpu_count() or 1
+    torch.set_num_threads(threads)
+    if w.kind == "contiguous":
+        S = x["k"].shape[1]
+        s_len = min(S, 4096)
+        units = [(0, 0)]
+
+        def run(n):
+            oracle.decode(x["q"][:1], x["k"][:1, :n], x["v"][:1, :n], w.h_q, w.h_kv, w.d_head, w.scale,
+                          units=units)
+
+        def nbytes(n):
+            return 2 * n * w.d_head * 2 + 2 * w.T_q * w.G * w.d_head * 2
+        # grow the sample until one pass takes ~target_s / 4
+        t = 0.0
+        while True:
+            t0 = time.perf_counter()
+            run(s_len)
+            t = time.perf_counter() - t0
+            if t > target_s / 4 or s_len >= S:
+                break
+            s_len = min(S, s_len * 4)
+        reps, t_tot = 0, 0.0
+        while t_tot < target_s or reps == 0:
+            t0 = time.perf_counter()
+            run(s_len)
+            t_tot += time.perf_counter() - t0
+            reps += 1
+        desc = f"sequence 0, KV head 0 ({w.G * w.T_q} query rows) over the first {s_len} keys, {reps} passes"
+        return reps * nbytes(s_len) / t_tot, desc, threads
+    else:
+        lens = x["seq_lens"]
+        seqs = []
+        total, t_tot, reps = 0, 0.0, 0
+        row = w.h_kv * w.d_head * 2
+        order = list(range(len(lens)))
+        i = 0
+        while t_tot < target_s or reps == 0:
+            b = order[i % len(order)]
+            t0 = time.perf_counter()
+            oracle.decode_paged_seq(x["q"], x["k_pool"], x["v_pool"], x["block_tables"], lens, b, w.h_q, w.h_kv,
+                                    w.d_head, w.scale, w.block_size)
+            t_tot += time.perf_counter() - t0
+            total += 2 * int(lens[b]) * row + 2 * w.h_q * w.d_head * 2
+            reps += 1
+            i += 1
+            seqs.append(b)
+        desc = f"{reps} whole sequences of the paged workload ({sorted(set(seqs))[:8]}...)"
+        return total / t_tot, desc, threads
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: host cores, bounded samples, the same metric."""
+    if rank != 0:
+        return 0
+    w, x = load_inputs(args.workload)
+    steps = args.steps if args.steps is not None else 5
+    warm = args.warmup if args.warmup is not None else 1
+    per_step = max(0.2, min(10.0, 150.0 / max(1, steps + warm)))
+    for _ in range(warm):
+        oracle_sample(x, w, per_step * 0.25)
+    vals, descs, t_total = [], [], 0.0
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        bps, desc, threads = oracle_sample(x, w, per_step)
+        t_total += time.perf_counter() - t0
+        vals.append(bps)
+        descs.append(desc)
+    gbs = statistics.median(vals) / 1e9
+    bytes_step = gi.kv_bytes(x)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": steps, "warmup": warm, "ms_per_step": round(bytes_step / (gbs * 1e9) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, x, None, note="CPU float64 oracle on bounded samples of this workload"),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": descs[0]},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, x, n_splits, note=None):
+    c = {"workload": w.name, "kind": w.kind, "batch": w.batch, "T_q": w.T_q, "h_q": w.h_q, "h_kv": w.h_kv,
+         "d_head": w.d_head, "scale": w.scale, "parallelism": "replicas (no exchange)"}
+    if w.kind == "contiguous":
+        c["S_kv"] = w.S_kv
+    else:
+        c.update(block_size=w.block_size, partition_size=w.partition_size,
+                 tokens=int(np.asarray(x["seq_lens"], dtype=np.int64).sum()), max_seq_len=int(x["max_seq_len"]))
+    if n_splits is not None:
+        c["n_splits"] = n_splits
+    c["bytes_per_step"] = gi.kv_bytes(x)
+    if note:
+        c["note"] = note
+    return c
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from decode_attention_03_gb300 import build as _b
+    _b.build()
+    import decode_attention_03_gb300 as pkg
+
+    w, x = load_inputs(args.workload)
+    d = to_device(x, dev)
+    bytes_step = gi.kv_bytes(x)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    big = bytes_step > 2 * l2
+    stream = torch.cuda.Stream(dev)
+    out = torch.empty(w.batch * w.T_q * w.h_q * w.d_head, dtype=torch.float16, device=dev)
+    out = out.reshape(w.batch, w.T_q, -1) if w.kind == "contiguous" else out.reshape(w.batch, -1)
+    if w.kind == "contiguous":
+        nbytes = pkg.gqa_decode_workspace_size(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head, args.n_splits)
+        n_splits = args.n_splits or pkg.gqa_decode_num_splits(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head)
+    else:
+        nbytes = pkg.gqa_paged_workspace_size(w.batch, w.h_q, w.h_kv, w.d_head, x["max_seq_len"], w.partition_size)
+        n_splits = None
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    step = make_step(pkg, w, x, d, out, ws, args)
+    flush = None if big else torch.empty(int(2 * l2), dtype=torch.uint8, device=dev)
+
+    # default step counts: about two seconds of timed work
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            step()
+    torch.cuda.synchronize()
+    est = (time.perf_counter() - t0) / 5
+    steps = args.steps if args.steps is not None else int(min(5000, max(20, 2.0 / max(est, 1e-6))))
+    warm = args.warmup if args.warmup is not None else 10
+
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            if flush is not None:
+                flush.zero_()
+            step()
+    torch.cuda.synchronize()
+    if pkg.gqa_workspace_check(ws, stream) != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)] \
+        if flush is not None else None
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    with torch.cuda.stream(stream):
+        if flush is None:
+            e0.record(stream)
+            for _ in range(steps):
+                step()
+            e1.record(stream)
+        else:
+            for i in range(steps):
+                flush.zero_()
+                ev[i][0].record(stream)
+                step()
+                ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks.stop()
+    if flush is None:
+        t_ms = e0.elapsed_time(e1)
+    else:
+        t_ms = sum(a.elapsed_time(b) for a, b in ev)
+    status = pkg.gqa_workspace_check(ws, stream)
+    if status != 0:
+        raise RuntimeError(f"device status word set in the timed region: {status}")
+    t_max = t_ms
+    if world > 1:
+        tt = torch.tensor([t_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_max = float(tt.item())
+    ms_step = t_max / steps
+    value = bytes_step * steps * world / (t_max * 1e-3) / 1e9
+    per_launch_gbs = bytes_step / (ms_step * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    traffic = recorded_traffic(w.name)
+
+    # ---- end to end: pinned host inputs -> device, decode, output -> host, every step
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(pkg, w, x, d, out, ws, stream, args, steps_hint=steps)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        bps, desc, threads = oracle_sample(x, w, 10.0)
+        cpu = {"value": round(bps / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        launches_per_step = 1 if (w.kind == "paged" or args.merge_mode == 0 or (n_splits or 1) <= 1) else 2
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
+            "warmup": warm, "ms_per_step": round(ms_step, 6), "us_per_step": round(ms_step * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic",
+            "config": dict(config_of(w, x, n_splits), accum="f32",
+                           l2=("inputs larger than L2, no flush" if flush is None
+                               else f"L2 flushed ({2 * l2 >> 20} MiB write) before every timed step, outside events")),
+            "roofline": {"bound": "hbm", "achieved": round(per_launch_gbs, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(per_launch_gbs / peak, 4), "traffic": traffic,
+                         "peak_source": peak_src, "kernel": "gqa_split_kernel",
+                         "frac_of_nominal_7900": round(per_launch_gbs / NOMINAL_HBM_GBS, 4)},
+            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": steps * launches_per_step,
+            "clocks": clocks.summary(wall0, wall1),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def end_to_end(pkg, w, x, d, out, ws, stream, args, steps_hint):
+    keys = list(d.keys())
+    host = {k: torch.from_numpy(np.ascontiguousarray(x[k])).pin_memory() for k in keys}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = host_out.numel() * host_out.element_size()
+    step = make_step(pkg, w, x, d, out, ws, args)
+
+    def one():
+        for k in keys:
+            d[k].copy_(host[k], non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        one()
+    torch.cuda.synchronize()
+    est = time.perf_counter() - t0
+    n = int(min(max(3, 2.0 / max(est, 1e-6)), max(3, steps_hint)))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n):
+            one()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    return {"value": round(gi.kv_bytes(x) / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "steps": n}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,515 @@
+// Host side of the C ABI (include/gqa_decode.h): argument validation, the
+// split-count heuristic, workspace layout, TMA descriptor encoding and launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gqa_decode.h"
+#include "gqa_instances.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kVersion = 10000;            // 1.0.0
+constexpr size_t kHeaderBytes = 256;        // status word (+ reserved)
+constexpr int kMinTilesPerSplit = 4;        // a split streams at least 4 x 64 keys
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;
+constexpr int kMaxDevices = 64;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int d_index(int d) { return d == 64 ? 0 : (d == 128 ? 1 : -1); }
+
+int row_class(int rows) {
+  if (rows <= 8) return 0;
+  if (rows <= 16) return 1;
+  if (rows <= 32) return 2;
+  if (rows <= 64) return 3;
+  return -1;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- per-device state
+struct DevState {
+  bool ready = false;
+  int sms = 0;
+  int occ[2][4][2] = {};       // [d index][row class][paged] resident CTAs per SM, 0 = not prepared
+};
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+cudaError_t prepare_unit(int di, int cls, bool paged, int* occ) {
+  if (!paged) return di == 0 ? contig_d64_prepare(cls, occ) : contig_d128_prepare(cls, occ);
+  return di == 0 ? paged_d64_prepare(cls, occ) : paged_d128_prepare(cls, occ);
+}
+
+cudaError_t launch_unit(int di, int cls, bool paged, dim3 grid, cudaStream_t st, const CUtensorMap& tk,
+                        const CUtensorMap& tv, const DecodeArgs& a) {
+  if (!paged) return di == 0 ? contig_d64_launch(cls, grid, st, tk, tv, a) : contig_d128_launch(cls, grid, st, tk, tv, a);
+  return di == 0 ? paged_d64_launch(cls, grid, st, tk, tv, a) : paged_d128_launch(cls, grid, st, tk, tv, a);
+}
+
+// SM count and resident CTAs per SM of one kernel configuration on the current device
+gqa_status device_info(int di, int cls, bool paged, int* sms, int* occ) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState& st = g_dev[dev];
+  if (!st.ready) {
+    if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return GQA_ERR_CUDA;
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return GQA_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    st.ready = true;
+  }
+  int& o = st.occ[di][cls][paged ? 1 : 0];
+  if (o == 0) {
+    int v = 0;
+    if (prepare_unit(di, cls, paged, &v) != cudaSuccess || v <= 0) return GQA_ERR_CUDA;
+    o = v;
+  }
+  *sms = st.sms;
+  *occ = o;
+  return GQA_OK;
+}
+
+// 2-D map over a (rows, cols) f16 matrix, boxes of 64 columns x box_rows rows, 128-byte swizzle
+gqa_status encode_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows > 0 ? rows : 1};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GQA_OK : GQA_ERR_CUDA;
+}
+
+// Split count: enough (b, g, split) CTAs to fill every resident slot of the GPU once
+// (one wave, all CTAs co-resident), each split at least kMinTilesPerSplit tiles long.
+// Prior art: page "muh_cc_dispatch.py", grid_even_share (grid = min(tiles, SMs x
+// subscription), even shares of tiles).
+int heuristic_splits(int64_t units, int64_t tiles, int sms, int occ) {
+  const int64_t slots = (int64_t)sms * occ;
+  if (tiles <= 0) return 1;
+  if (units >= slots) return 1;
+  int64_t n = slots / units;
+  const int64_t cap = tiles / kMinTilesPerSplit;
+  if (n > cap) n = cap;
+  if (n < 1) n = 1;
+  if (n > 65535) n = 65535;
+  return (int)n;
+}
+
+struct Layout {
+  size_t counters, m, l, o, total;
+};
+
+Layout ws_layout(int64_t units, int64_t n_parts, int64_t R, int D) {
+  Layout L;
+  L.counters = kHeaderBytes;
+  size_t off = L.counters + align256((size_t)units * 4);
+  if (n_parts <= 1) {
+    L.m = L.l = L.o = 0;
+    L.total = off;
+    return L;
+  }
+  L.m = off;
+  off += align256((size_t)(n_parts * R) * 4);
+  L.l = off;
+  off += align256((size_t)(n_parts * R) * 4);
+  L.o = off;
+  off += align256((size_t)(n_parts * R * D) * 4);
+  L.total = off;
+  return L;
+}
+
+gqa_options defaults() {
+  gqa_options o;
+  o.n_splits = 0;
+  o.merge_mode = 0;
+  o.timeout_us = 0;
+  o.test_stall_cta = -1;
+  return o;
+}
+
+struct ContigPlan {
+  int di, cls, rows, n_splits;
+  int64_t units, tiles, R;
+  Layout lay;
+};
+
+// validation shared by the size query and the calls
+gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_len, int h_q, int h_kv, int D,
+                       int forced_splits, bool need_device, ContigPlan* p) {
+  if (B < 0 || T_q < 1 || h_q < 1 || h_kv < 1 || S_kv < 0 || s_begin < 0 || s_len < 0) return GQA_ERR_INVALID_ARG;
+  if (s_begin + s_len > S_kv) return GQA_ERR_INVALID_ARG;
+  if (h_q % h_kv != 0 || forced_splits < 0) return GQA_ERR_INVALID_ARG;
+  if (B > 65535 || h_kv > 65535) return GQA_ERR_INVALID_ARG;
+  if ((int64_t)B * S_kv >= (int64_t(1) << 31)) return GQA_ERR_INVALID_ARG;
+  p->di = d_index(D);
+  p->rows = (h_q / h_kv) * T_q;
+  if (p->di < 0) return GQA_ERR_UNSUPPORTED;
+  if ((int64_t)(h_q / h_kv) * T_q > 64) return GQA_ERR_UNSUPPORTED;
+  p->cls = row_class(p->rows);
+  p->units = (int64_t)B * h_kv;
+  p->tiles = (s_len + kTile - 1) / kTile;
+  p->R = (int64_t)B * T_q * h_q;
+  if (forced_splits > 0) {
+    int64_t n = forced_splits;
+    if (n > p->tiles) n = p->tiles > 0 ? p->tiles : 1;
+    if (n > 65535) n = 65535;
+    p->n_splits = (int)n;
+  } else if (need_device) {
+    int sms = 0, occ = 0;
+    gqa_status s = device_info(p->di, p->cls, false, &sms, &occ);
+    if (s != GQA_OK) return s;
+    p->n_splits = heuristic_splits(p->units, p->tiles, sms, occ);
+  } else {
+    p->n_splits = 1;
+  }
+  p->lay = ws_layout(p->units, p->n_splits, p->R, D);
+  return GQA_OK;
+}
+
+gqa_status merge_launch(const float* m, const float* l, const float* op, int n_parts, int64_t rows, int D,
+                        __half* o, float* mo, float* lo, float* oo, cudaStream_t st) {
+  if (rows == 0) return GQA_OK;
+  const int warps = 8;
+  const int64_t blocks = (rows + warps - 1) / warps;
+  if (blocks > 2147483647LL) return GQA_ERR_INVALID_ARG;
+  if (D == 64)
+    gqa_merge_kernel<64><<<(unsigned)blocks, warps * 32, 0, st>>>(m, l, op, n_parts, rows, o, mo, lo, oo);
+  else
+    gqa_merge_kernel<128><<<(unsigned)blocks, warps * 32, 0, st>>>(m, l, op, n_parts, rows, o, mo, lo, oo);
+  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* m_out,
+                       float* l_out, float* op_out, int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_len,
+                       int h_q, int h_kv, int D, float scale, void* ws, size_t ws_bytes, void* stream,
+                       const gqa_options* opt_in, bool partial) {
+  const gqa_options opt = opt_in ? *opt_in : defaults();
+  if (opt.merge_mode < 0 || opt.merge_mode > 1) return GQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  if (!partial && S_kv < 1) return GQA_ERR_INVALID_ARG;
+  ContigPlan p;
+  // shape checks first: they need no device
+  gqa_status s = plan_contig(B, T_q, S_kv, s_begin, s_len, h_q, h_kv, D, 1, false, &p);
+  if (s != GQA_OK) return s;
+  if (B == 0) return GQA_OK;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(ws)) return GQA_ERR_INVALID_ARG;
+  if (partial) {
+    if (!aligned16(m_out) || !aligned16(l_out) || !aligned16(op_out)) return GQA_ERR_INVALID_ARG;
+  } else if (!aligned16(o)) {
+    return GQA_ERR_INVALID_ARG;
+  }
+  s = plan_contig(B, T_q, S_kv, s_begin, s_len, h_q, h_kv, D, opt.n_splits, true, &p);
+  if (s != GQA_OK) return s;
+  if (ws_bytes < p.lay.total) return GQA_ERR_WORKSPACE;
+  int sms = 0, occ = 0;
+  s = device_info(p.di, p.cls, false, &sms, &occ);
+  if (s != GQA_OK) return s;
+
+  CUtensorMap tk, tv;
+  const uint64_t cols = (uint64_t)h_kv * D, nrows = (uint64_t)B * (uint64_t)S_kv;
+  if ((s = encode_map(&tk, k, cols, nrows, kTile)) != GQA_OK) return s;
+  if ((s = encode_map(&tv, v, cols, nrows, kTile)) != GQA_OK) return s;
+
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  DecodeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = reinterpret_cast<const __half*>(q);
+  a.o = partial ? nullptr : reinterpret_cast<__half*>(o);
+  a.m_out = partial ? m_out : nullptr;
+  a.l_out = partial ? l_out : nullptr;
+  a.o_part_out = partial ? op_out : nullptr;
+  a.status = reinterpret_cast<uint32_t*>(wsb);
+  a.counters = reinterpret_cast<uint32_t*>(wsb + p.lay.counters);
+  if (p.n_splits > 1) {
+    a.ws_m = reinterpret_cast<float*>(wsb + p.lay.m);
+    a.ws_l = reinterpret_cast<float*>(wsb + p.lay.l);
+    a.ws_o = reinterpret_cast<float*>(wsb + p.lay.o);
+  }
+  a.B = B;
+  a.T_q = T_q;
+  a.h_q = h_q;
+  a.h_kv = h_kv;
+  a.G = h_q / h_kv;
+  a.rows = p.rows;
+  a.R = p.R;
+  a.S_kv = S_kv;
+  a.s_begin = s_begin;
+  a.s_len = s_len;
+  a.n_splits = p.n_splits;
+  a.merge_in_kernel = opt.merge_mode == 0 ? 1 : 0;
+  a.scale_log2 = scale * kLog2e;
+  a.timeout_ns = opt.timeout_us ? (uint64_t)opt.timeout_us * 1000ull : kDefaultTimeoutNs;
+  a.stall_cta = opt.test_stall_cta;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  dim3 grid((unsigned)h_kv, (unsigned)p.n_splits, (unsigned)B);
+  if (launch_unit(p.di, p.cls, false, grid, st, tk, tv, a) != cudaSuccess) return GQA_ERR_CUDA;
+  if (p.n_splits > 1 && !a.merge_in_kernel) {
+    return merge_launch(a.ws_m, a.ws_l, a.ws_o, p.n_splits, p.R, D, a.o, a.m_out, a.l_out, a.o_part_out, st);
+  }
+  return GQA_OK;
+}
+
+struct PagedPlan {
+  int di, cls, rows, max_parts;
+  int64_t units, R;
+  Layout lay;
+};
+
+gqa_status plan_paged(int N, int h_q, int h_kv, int D, int max_seq_len, int partition_size, PagedPlan* p) {
+  if (N < 0 || h_q < 1 || h_kv < 1 || max_seq_len < 0 || partition_size <= 0) return GQA_ERR_INVALID_ARG;
+  if (h_q % h_kv != 0 || N > 65535 || h_kv > 65535) return GQA_ERR_INVALID_ARG;
+  if (partition_size % kTile != 0) return GQA_ERR_INVALID_ARG;
+  p->di = d_index(D);
+  if (p->di < 0) return GQA_ERR_UNSUPPORTED;
+  p->rows = h_q / h_kv;
+  if (p->rows > 64) return GQA_ERR_UNSUPPORTED;
+  p->cls = row_class(p->rows);
+  const int64_t parts = ((int64_t)max_seq_len + partition_size - 1) / partition_size;
+  if (parts > 65535) return GQA_ERR_INVALID_ARG;
+  p->max_parts = parts > 0 ? (int)parts : 1;
+  p->units = (int64_t)N * h_kv;
+  p->R = (int64_t)N * h_q;
+  p->lay = ws_layout(p->units, p->max_parts, p->R, D);
+  return GQA_OK;
+}
+
+gqa_status paged_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool, const int32_t* tables,
+                      const int32_t* lens, uint16_t* o, int N, int max_blocks, int num_blocks, int block_size,
+                      int partition_size, int h_q, int h_kv, int D, float scale, int max_seq_len, void* ws,
+                      size_t ws_bytes, void* stream, const gqa_options* opt_in) {
+  const gqa_options opt = opt_in ? *opt_in : defaults();
+  if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  PagedPlan p;
+  gqa_status s = plan_paged(N, h_q, h_kv, D, max_seq_len, partition_size, &p);
+  if (s != GQA_OK) return s;
+  if (!(block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64)) return GQA_ERR_INVALID_ARG;
+  if (partition_size / block_size > kMaxPagedBlocksPerPart) return GQA_ERR_INVALID_ARG;
+  if (max_blocks < 1 || num_blocks < 0) return GQA_ERR_INVALID_ARG;
+  if ((int64_t)num_blocks * block_size >= (int64_t(1) << 31)) return GQA_ERR_INVALID_ARG;
+  if (N == 0) return GQA_OK;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o) || !aligned16(ws) ||
+      tables == nullptr || lens == nullptr || (reinterpret_cast<uintptr_t>(tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lens) & 3u))
+    return GQA_ERR_INVALID_ARG;
+  if (ws_bytes < p.lay.total) return GQA_ERR_WORKSPACE;
+  int sms = 0, occ = 0;
+  s = device_info(p.di, p.cls, true, &sms, &occ);
+  if (s != GQA_OK) return s;
+
+  CUtensorMap tk, tv;
+  const uint64_t cols = (uint64_t)h_kv * D, nrows = (uint64_t)num_blocks * block_size;
+  if ((s = encode_map(&tk, k_pool, cols, nrows, (uint32_t)block_size)) != GQA_OK) return s;
+  if ((s = encode_map(&tv, v_pool, cols, nrows, (uint32_t)block_size)) != GQA_OK) return s;
+
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  DecodeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = reinterpret_cast<const __half*>(q);
+  a.o = reinterpret_cast<__half*>(o);
+  a.status = reinterpret_cast<uint32_t*>(wsb);
+  a.counters = reinterpret_cast<uint32_t*>(wsb + p.lay.counters);
+  if (p.max_parts > 1) {
+    a.ws_m = reinterpret_cast<float*>(wsb + p.lay.m);
+    a.ws_l = reinterpret_cast<float*>(wsb + p.lay.l);
+    a.ws_o = reinterpret_cast<float*>(wsb + p.lay.o);
+  }
+  a.block_tables = tables;
+  a.seq_lens = lens;
+  a.max_blocks_per_seq = max_blocks;
+  a.num_blocks = num_blocks;
+  a.block_size = block_size;
+  a.partition_size = partition_size;
+  a.B = N;
+  a.T_q = 1;
+  a.h_q = h_q;
+  a.h_kv = h_kv;
+  a.G = h_q / h_kv;
+  a.rows = p.rows;
+  a.R = p.R;
+  a.n_splits = p.max_parts;
+  a.merge_in_kernel = 1;
+  a.scale_log2 = scale * kLog2e;
+  a.timeout_ns = opt.timeout_us ? (uint64_t)opt.timeout_us * 1000ull : kDefaultTimeoutNs;
+  a.stall_cta = opt.test_stall_cta;
+
+  dim3 grid((unsigned)h_kv, (unsigned)p.max_parts, (unsigned)N);
+  if (launch_unit(p.di, p.cls, true, grid, reinterpret_cast<cudaStream_t>(stream), tk, tv, a) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
+}  // namespace
+}  // namespace gqa
+
+using namespace gqa;
+
+extern "C" {
+
+gqa_options gqa_default_options(void) { return defaults(); }
+
+const char* gqa_status_string(int status) {
+  switch (status) {
+    case GQA_OK: return "ok";
+    case GQA_ERR_INVALID_ARG: return "invalid argument";
+    case GQA_ERR_UNSUPPORTED: return "unsupported shape (d_head must be 64 or 128, G*T_q <= 64)";
+    case GQA_ERR_WORKSPACE: return "workspace too small";
+    case GQA_ERR_CUDA: return "CUDA error";
+    case GQA_ERR_TIMEOUT: return "a device wait timed out";
+  }
+  return "unknown status";
+}
+
+int gqa_version(void) { return kVersion; }
+
+int gqa_decode_num_splits(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head) {
+  try {
+    ContigPlan p;
+    if (S_kv < 1 || batch < 1) return -1;
+    if (plan_contig(batch, T_q, S_kv, 0, S_kv, h_q, h_kv, d_head, 0, true, &p) != GQA_OK) return -1;
+    return p.n_splits;
+  } catch (...) {
+    return -1;
+  }
+}
+
+size_t gqa_decode_workspace_size(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head, int n_splits) {
+  try {
+    ContigPlan p;
+    if (plan_contig(batch, T_q, S_kv, 0, S_kv, h_q, h_kv, d_head, n_splits, true, &p) != GQA_OK) return 0;
+    return p.lay.total;
+  } catch (...) {
+    return 0;
+  }
+}
+
+size_t gqa_paged_workspace_size(int num_seqs, int h_q, int h_kv, int d_head, int max_seq_len, int partition_size) {
+  PagedPlan p;
+  if (plan_paged(num_seqs, h_q, h_kv, d_head, max_seq_len, partition_size, &p) != GQA_OK) return 0;
+  return p.lay.total;
+}
+
+gqa_status gqa_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+  if (workspace == nullptr || ws_bytes < kHeaderBytes) return GQA_ERR_INVALID_ARG;
+  return cudaMemsetAsync(workspace, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GQA_OK
+             : GQA_ERR_CUDA;
+}
+
+gqa_status gqa_workspace_check(void* workspace, void* stream) {
+  if (workspace == nullptr) return GQA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GQA_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return GQA_ERR_CUDA;
+  if (word != 0 && cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return GQA_ERR_CUDA;
+  if (word & kDevTimeout) return GQA_ERR_TIMEOUT;
+  if (word & kDevBadInput) return GQA_ERR_INVALID_ARG;
+  return GQA_OK;
+}
+
+gqa_status gqa_decode_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, int batch, int T_q,
+                         int64_t S_kv, int h_q, int h_kv, int d_head, float scale, void* workspace, size_t ws_bytes,
+                         void* stream, const gqa_options* opt) {
+  try {
+    return decode_impl(q, k, v, o, nullptr, nullptr, nullptr, batch, T_q, S_kv, 0, S_kv, h_q, h_kv, d_head, scale,
+                       workspace, ws_bytes, stream, opt, false);
+  } catch (...) {
+    return GQA_ERR_CUDA;
+  }
+}
+
+gqa_status gqa_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, int batch, int T_q,
+                      int64_t S_kv, int h_q, int h_kv, int d_head, float scale, void* workspace, size_t ws_bytes,
+                      void* stream) {
+  return gqa_decode_ex(q, k, v, o, batch, T_q, S_kv, h_q, h_kv, d_head, scale, workspace, ws_bytes, stream, nullptr);
+}
+
+gqa_status gqa_decode_partial_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* m, float* l,
+                                 float* o_part, int batch, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_len,
+                                 int h_q, int h_kv, int d_head, float scale, void* workspace, size_t ws_bytes,
+                                 void* stream, const gqa_options* opt) {
+  try {
+    return decode_impl(q, k, v, nullptr, m, l, o_part, batch, T_q, S_kv, s_begin, s_len, h_q, h_kv, d_head, scale,
+                       workspace, ws_bytes, stream, opt, true);
+  } catch (...) {
+    return GQA_ERR_CUDA;
+  }
+}
+
+gqa_status gqa_decode_partial(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* m, float* l,
+                              float* o_part, int batch, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_len, int h_q,
+                              int h_kv, int d_head, float scale, void* workspace, size_t ws_bytes, void* stream) {
+  return gqa_decode_partial_ex(q, k, v, m, l, o_part, batch, T_q, S_kv, s_begin, s_len, h_q, h_kv, d_head, scale,
+                               workspace, ws_bytes, stream, nullptr);
+}
+
+gqa_status gqa_merge(const float* m, const float* l, const float* o_part, int n_parts, int64_t rows, int d_head,
+                     uint16_t* o, void* stream) {
+  if (n_parts < 1 || rows < 0) return GQA_ERR_INVALID_ARG;
+  if (d_index(d_head) < 0) return GQA_ERR_UNSUPPORTED;
+  if (rows == 0) return GQA_OK;
+  if (!aligned16(m) || !aligned16(l) || !aligned16(o_part) || !aligned16(o)) return GQA_ERR_INVALID_ARG;
+  return merge_launch(m, l, o_part, n_parts, rows, d_head, reinterpret_cast<__half*>(o), nullptr, nullptr, nullptr,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+gqa_status gqa_merge_partial(const float* m, const float* l, const float* o_part, int n_parts, int64_t rows,
+                             int d_head, float* m_out, float* l_out, float* o_out, void* stream) {
+  if (n_parts < 1 || rows < 0) return GQA_ERR_INVALID_ARG;
+  if (d_index(d_head) < 0) return GQA_ERR_UNSUPPORTED;
+  if (rows == 0) return GQA_OK;
+  if (!aligned16(m) || !aligned16(l) || !aligned16(o_part) || !aligned16(m_out) || !aligned16(l_out) ||
+      !aligned16(o_out))
+    return GQA_ERR_INVALID_ARG;
+  return merge_launch(m, l, o_part, n_parts, rows, d_head, nullptr, m_out, l_out, o_out,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+gqa_status gqa_decode_paged_ex(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                               const int32_t* block_tables, const int32_t* seq_lens, uint16_t* o, int num_seqs,
+                               int max_blocks_per_seq, int num_blocks, int block_size, int partition_size, int h_q,
+                               int h_kv, int d_head, float scale, int max_seq_len, void* workspace, size_t ws_bytes,
+                               void* stream, const gqa_options* opt) {
+  try {
+    return paged_impl(q, k_pool, v_pool, block_tables, seq_lens, o, num_seqs, max_blocks_per_seq, num_blocks,
+                      block_size, partition_size, h_q, h_kv, d_head, scale, max_seq_len, workspace, ws_bytes, stream,
+                      opt);
+  } catch (...) {
+    return GQA_ERR_CUDA;
+  }
+}
+
+gqa_status gqa_decode_paged(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                            const int32_t* block_tables, const int32_t* seq_lens, uint16_t* o, int num_seqs,
+                            int max_blocks_per_seq, int num_blocks, int block_size, int partition_size, int h_q,
+                            int h_kv, int d_head, float scale, int max_seq_len, void* workspace, size_t ws_bytes,
+                            void* stream) {
+  return gqa_decode_paged_ex(q, k_pool, v_pool, block_tables, seq_lens, o, num_seqs, max_blocks_per_seq, num_blocks,
+                             block_size, partition_size, h_q, h_kv, d_head, scale, max_seq_len, workspace, ws_bytes,
+                             stream, nullptr);
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// Compile-time configurations of the split-KV kernel and their launchers.
+// A configuration is (d_head, query-row class, paged); the row class picks how
+// many 8-row MMA n-tiles a consumer warp carries (NT) and how many warp
+// columns share a tile (WN).
+#pragma once
+#include <cuda_runtime.h>
+
+#include "gqa_kernels.cuh"
+
+namespace gqa {
+
+// row class -> (NT, WN): <=8 rows (1,1), <=16 (2,1), <=32 (2,2), <=64 (2,4)
+constexpr int cls_nt(int cls) { return cls == 0 ? 1 : 2; }
+constexpr int cls_wn(int cls) { return cls <= 1 ? 1 : (cls == 2 ? 2 : 4); }
+
+// pipeline depth: ~96 KB of K/V stages when two CTAs fit on an SM; ~192 KB when
+// one CTA per SM is all that fits anyway (merge scratch above 96 KB, or more than
+// half of the register file: d_head 128 with two warp columns)
+template <int D, int NT, int WN>
+constexpr int stages_for() {
+  constexpr int stage = 2 * (D / 64) * kTile * 128;
+  constexpr int scratch = kWK * WN * 8 * NT * (D + 6) * 4;
+  constexpr bool one_per_sm = scratch > 96 * 1024 || (D == 128 && WN >= 2);
+  return one_per_sm ? (192 * 1024) / stage : (96 * 1024) / stage;
+}
+
+template <int D, int CLS, bool PAGED>
+struct Inst {
+  static constexpr int NT = cls_nt(CLS);
+  static constexpr int WN = cls_wn(CLS);
+  static constexpr int STAGES = stages_for<D, NT, WN>();
+  using C = Cfg<D, NT, WN, STAGES>;
+  static_assert(C::SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+  static cudaError_t prepare(int* occupancy) {
+    auto fn = gqa_split_kernel<D, NT, WN, STAGES, PAGED>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, fn, C::THREADS, C::SMEM_BYTES);
+  }
+  static cudaError_t launch(dim3 grid, cudaStream_t st, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const DecodeArgs& a) {
+    gqa_split_kernel<D, NT, WN, STAGES, PAGED><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tk, tv, a);
+    return cudaGetLastError();
+  }
+};
+
+// One of these per (d_head, paged) translation unit; cls in [0, 4).
+#define GQA_DECLARE_UNIT(NAME)                                                                   \
+  cudaError_t NAME##_prepare(int cls, int* occupancy);                                           \
+  cudaError_t NAME##_launch(int cls, dim3 grid, cudaStream_t st, const CUtensorMap& tk,          \
+                            const CUtensorMap& tv, const DecodeArgs& a);
+
+#define GQA_DEFINE_UNIT(NAME, D, PAGED)                                                          \
+  cudaError_t NAME##_prepare(int cls, int* occupancy) {                                          \
+    switch (cls) {                                                                               \
+      case 0: return Inst<D, 0, PAGED>::prepare(occupancy);                                      \
+      case 1: return Inst<D, 1, PAGED>::prepare(occupancy);                                      \
+      case 2: return Inst<D, 2, PAGED>::prepare(occupancy);                                      \
+      case 3: return Inst<D, 3, PAGED>::prepare(occupancy);                                      \
+    }                                                                                            \
+    return cudaErrorInvalidValue;                                                                \
+  }                                                                                              \
+  cudaError_t NAME##_launch(int cls, dim3 grid, cudaStream_t st, const CUtensorMap& tk,          \
+                            const CUtensorMap& tv, const DecodeArgs& a) {                        \
+    switch (cls) {                                                                               \
+      case 0: return Inst<D, 0, PAGED>::launch(grid, st, tk, tv, a);                             \
+      case 1: return Inst<D, 1, PAGED>::launch(grid, st, tk, tv, a);                             \
+      case 2: return Inst<D, 2, PAGED>::launch(grid, st, tk, tv, a);                             \
+      case 3: return Inst<D, 3, PAGED>::launch(grid, st, tk, tv, a);                             \
+    }                                                                                            \
+    return cudaErrorInvalidValue;                                                                \
+  }
+
+GQA_DECLARE_UNIT(contig_d64)
+GQA_DECLARE_UNIT(contig_d128)
+GQA_DECLARE_UNIT(paged_d64)
+GQA_DECLARE_UNIT(paged_d128)
+
+}  // namespace gqa

@@ -1,0 +1,174 @@
+/*
+ * gqa_decode.h -- C ABI of the GB300 (sm_103a) GQA split-KV decode attention library
+ * (libgqa_decode.so).
+ *
+ * The operation (page "kernbench2 ... _gqa_attention_decode_long.py", "GQA
+ * fused-attention decode kernel -- long context": kernel docstring "Tensor
+ * layout", the local tile math and "Final normalise + store"): for every
+ * sequence b, query token t < T_q and query head h < h_q, with G = h_q / h_kv
+ * query heads sharing KV head g = h / G,
+ *
+ *     O[b,t,h,:] = softmax_j( scale * Q[b,t,h,:] . K[b,j,g,:] ) . V[b,j,g,:]
+ *
+ * The key axis is swept in tiles and splits; every split yields a partial
+ * (m, l, O) -- m the row max of the scaled logits (natural-log units), l the sum
+ * of exp(logit - m), O the unnormalised sum of exp(logit - m) * V -- and partials
+ * are folded with the page's online-softmax merge (_merge_running):
+ * m = max(m_a, m_b), each side rescaled by exp(m_side - m), l and O summed.
+ * The paged variant is page "muh_kernel_map.py", VLLM_KERNEL_MAP
+ * 'paged_attention_v2': a per-partition pass plus a cross-partition merge.
+ *
+ * Conventions for every call
+ *  - f16 buffers hold IEEE binary16 values (passed as uint16_t); float buffers are fp32.
+ *  - All tensors are dense row-major, in device memory of the CURRENT CUDA
+ *    device, 16-byte aligned.  The caller owns every buffer; the library never
+ *    allocates device memory and never synchronises (except gqa_workspace_check).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *    asynchronous; arguments are validated on the host before any launch and
+ *    a failed validation returns an error code without touching the GPU.
+ *  - Launch failures return GQA_ERR_CUDA.  Faults detected on the device (a
+ *    bounded wait that gave up, a block id outside the pool) are recorded in
+ *    the workspace's status word; gqa_workspace_check reads it.
+ *  - Supported: h_q % h_kv == 0, G * T_q <= 64, d_head in {64, 128}
+ *    (GQA_ERR_UNSUPPORTED otherwise); no C++ exception crosses this ABI.
+ *  - Scores, softmax statistics, partials and accumulation are fp32; the output
+ *    O is rounded to f16 (nearest even).
+ */
+#ifndef GQA_DECODE_H_
+#define GQA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GQA_OK = 0,
+  GQA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or range, bad block id (device) */
+  GQA_ERR_UNSUPPORTED = 2, /* d_head or G*T_q outside the supported set */
+  GQA_ERR_WORKSPACE = 3,   /* workspace smaller than the size query asks for */
+  GQA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a launch failed */
+  GQA_ERR_TIMEOUT = 5      /* a bounded device wait gave up (reported by gqa_workspace_check) */
+} gqa_status;
+
+/* Optional knobs for tests and benchmarks (NULL = defaults everywhere). */
+typedef struct {
+  int n_splits;          /* contiguous calls: splits per (sequence, KV head); 0 = heuristic */
+  int merge_mode;        /* 0 = last-arriving CTA merges in the same kernel; 1 = separate merge kernel */
+  uint32_t timeout_us;   /* limit of every device wait; 0 = 1,000,000 us */
+  int test_stall_cta;    /* test hook, -1 = off: linear id (x + X*(y + Y*z)) of one CTA whose
+                            producer never loads its second tile, so that the waits on it run out.
+                            Use with a small timeout_us; the call then reports GQA_ERR_TIMEOUT
+                            through gqa_workspace_check and the workspace must be re-initialised. */
+} gqa_options;
+
+/* Default options: n_splits 0, merge_mode 0, timeout_us 0, test_stall_cta -1. */
+gqa_options gqa_default_options(void);
+
+/* Static text for a status code. */
+const char* gqa_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int gqa_version(void);
+
+/* Splits per (sequence, KV head) the heuristic picks on the current device for a contiguous
+ * call sweeping S_kv keys; <= 0 on invalid arguments or when no device is usable. */
+int gqa_decode_num_splits(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head);
+
+/* Workspace bytes for gqa_decode / gqa_decode_partial on the current device, sweeping S_kv
+ * keys (for a partial call pass s_len).  n_splits = 0 sizes for the heuristic; a positive
+ * value sizes for that forced split count.  Returns 0 on invalid arguments.  The workspace
+ * holds a status word, one arrival counter per (sequence, KV head) and the split partials. */
+size_t gqa_decode_workspace_size(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head,
+                                 int n_splits);
+
+/* Workspace bytes for gqa_decode_paged (T_q = 1).  Returns 0 on invalid arguments. */
+size_t gqa_paged_workspace_size(int num_seqs, int h_q, int h_kv, int d_head, int max_seq_len,
+                                int partition_size);
+
+/* Zero-fill a workspace (asynchronous memset on `stream`).  A workspace must be zero before
+ * its first use; every call that completes without a device fault leaves it so again. */
+gqa_status gqa_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream`, read and clear the workspace's device status word.  Returns GQA_OK,
+ * GQA_ERR_TIMEOUT (a bounded wait gave up; outputs of that call are invalid and the
+ * workspace must be re-initialised) or GQA_ERR_INVALID_ARG (a block id or sequence length
+ * outside the pool / table was seen; affected outputs are invalid). */
+gqa_status gqa_workspace_check(void* workspace, void* stream);
+
+/* Full decode step (contiguous KV).
+ *   q  (batch, T_q, h_q*d_head) f16      k, v (batch, S_kv, h_kv*d_head) f16
+ *   o  (batch, T_q, h_q*d_head) f16, written
+ * Every query token attends to all S_kv >= 1 keys of its sequence (no causal mask).
+ * `scale` multiplies q.k (e.g. 1/sqrt(d_head)).  batch = 0 is a no-op.
+ * batch * S_kv must be < 2^31. */
+gqa_status gqa_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
+                      int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head, float scale,
+                      void* workspace, size_t ws_bytes, void* stream);
+
+gqa_status gqa_decode_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
+                         int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head, float scale,
+                         void* workspace, size_t ws_bytes, void* stream, const gqa_options* opt);
+
+/* Partial over keys [s_begin, s_begin + s_len) of every sequence (0 <= s_begin,
+ * s_begin + s_len <= S_kv; s_len = 0 gives the empty partial m = -inf, l = 0, O = 0).
+ * Outputs, rows ordered like Q's (b, t, h): m, l (batch*T_q*h_q) fp32 and the
+ * unnormalised o_part (batch*T_q*h_q, d_head) fp32.  This is the (m, l, O) a rank of the
+ * page's kernel sends toward the root; gqa_merge folds several of them. */
+gqa_status gqa_decode_partial(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                              float* m, float* l, float* o_part,
+                              int batch, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_len,
+                              int h_q, int h_kv, int d_head, float scale,
+                              void* workspace, size_t ws_bytes, void* stream);
+
+gqa_status gqa_decode_partial_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                 float* m, float* l, float* o_part,
+                                 int batch, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_len,
+                                 int h_q, int h_kv, int d_head, float scale,
+                                 void* workspace, size_t ws_bytes, void* stream,
+                                 const gqa_options* opt);
+
+/* Merge n_parts >= 1 partials laid out m, l: [n_parts][rows], o_part: [n_parts][rows][d_head]
+ * (page: _merge_running folded over the parts, then O / l), writing
+ * o (rows, d_head) f16.  Rows whose partials are all empty (m = -inf) give 0. */
+gqa_status gqa_merge(const float* m, const float* l, const float* o_part, int n_parts,
+                     int64_t rows, int d_head, uint16_t* o, void* stream);
+
+/* As gqa_merge but keeps the merged partial (one hop of the page's chain reduce):
+ * m_out, l_out (rows) and o_out (rows, d_head), fp32. */
+gqa_status gqa_merge_partial(const float* m, const float* l, const float* o_part, int n_parts,
+                             int64_t rows, int d_head, float* m_out, float* l_out, float* o_out,
+                             void* stream);
+
+/* Paged decode (page "muh_kernel_map.py", paged_attention_v2 shape; T_q = 1).
+ *   q             (num_seqs, h_q*d_head) f16
+ *   k_pool/v_pool (num_blocks, block_size, h_kv*d_head) f16: token j of sequence b is row
+ *                 j % block_size of block block_tables[b, j / block_size]
+ *   block_tables  (num_seqs, max_blocks_per_seq) int32; entries past a sequence's last block
+ *                 are never read
+ *   seq_lens      (num_seqs) int32 in [0, min(max_seq_len, max_blocks_per_seq*block_size)];
+ *                 a length-0 sequence gets O = 0
+ *   o             (num_seqs, h_q*d_head) f16, written
+ * block_size in {8, 16, 32, 64}; partition_size a multiple of 64 with
+ * partition_size / block_size <= 512; max_seq_len (host-known bound on seq_lens) sizes the grid.
+ * Block ids outside [0, num_blocks) are not loaded and are reported by gqa_workspace_check. */
+gqa_status gqa_decode_paged(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                            const int32_t* block_tables, const int32_t* seq_lens, uint16_t* o,
+                            int num_seqs, int max_blocks_per_seq, int num_blocks, int block_size,
+                            int partition_size, int h_q, int h_kv, int d_head, float scale,
+                            int max_seq_len, void* workspace, size_t ws_bytes, void* stream);
+
+gqa_status gqa_decode_paged_ex(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                               const int32_t* block_tables, const int32_t* seq_lens, uint16_t* o,
+                               int num_seqs, int max_blocks_per_seq, int num_blocks, int block_size,
+                               int partition_size, int h_q, int h_kv, int d_head, float scale,
+                               int max_seq_len, void* workspace, size_t ws_bytes, void* stream,
+                               const gqa_options* opt);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_DECODE_H_ */
