@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(gi.WORKLOADS), default="long")
+    ap.add_argument("--s-kv", type=int, default=0,
+                    help="contiguous workloads: override S_kv (smaller cases for profiler captures)")
     ap.add_argument("--n-splits", type=int, default=0)
     ap.add_argument("--merge-mode", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -155,8 +157,11 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------------------------
-def load_inputs(name: str):
+def load_inputs(name: str, s_kv: int = 0):
     w = gi.WORKLOADS[name]
+    if s_kv and w.kind == "contiguous" and s_kv != w.S_kv:
+        import dataclasses
+        w = dataclasses.replace(w, name=f"{w.name}[S_kv={s_kv}]", S_kv=int(s_kv))
     x = gi.make(w)
     return w, x
 
@@ -239,7 +244,7 @@ def run_reference(args, rank, world):
     """The oracle as the reference arm: host cores, bounded samples, the same metric."""
     if rank != 0:
         return 0
-    w, x = load_inputs(args.workload)
+    w, x = load_inputs(args.workload, args.s_kv)
     steps = args.steps if args.steps is not None else 5
     warm = args.warmup if args.warmup is not None else 1
     per_step = max(0.2, min(10.0, 150.0 / max(1, steps + warm)))
@@ -298,7 +303,7 @@ def main():
     _b.build()
     import decode_attention_03_gb300 as pkg
 
-    w, x = load_inputs(args.workload)
+    w, x = load_inputs(args.workload, args.s_kv)
     d = to_device(x, dev)
     bytes_step = gi.kv_bytes(x)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
