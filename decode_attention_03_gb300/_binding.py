@@ -70,6 +70,7 @@ _SIGS = {
     "gqa_decode_paged": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p], _i),
     "gqa_decode_paged_ex": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p, _opt],
                             _i),
+    "gqa_decode_noalloc": ([_p, _p, _p, _p, _i, _i, _i64, _i, _i, _i, _f, _p], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -269,4 +270,25 @@ def gqa_decode_paged(q, k_pool, v_pool, block_tables, seq_lens, h_q: int, h_kv: 
                                  h_q, h_kv, D, scale, int(max_seq_len), _ptr(ws), ws.numel(), _stream(stream),
                                  ctypes.byref(opt))
     _check(st, "gqa_decode_paged")
+    return out
+
+
+GQA_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
+
+
+def gqa_decode_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, h_q: int, h_kv: int,
+                       scale: Optional[float] = None, *, out: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+    """gqa_decode without a caller workspace: the library's own per-GPU device array is used.
+
+    For callers that cannot allocate device memory.  Calls on one device share that array,
+    so they must not overlap on the GPU; shapes needing more than 8 MiB of workspace raise."""
+    B, T_q, S, D = _shape_qkv(q, k, v, h_q, h_kv)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    _f16(out, "out")
+    st = lib.gqa_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T_q, S, h_q, h_kv, D, scale,
+                                _stream(stream))
+    _check(st, "gqa_decode_noalloc")
     return out

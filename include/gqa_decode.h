@@ -167,6 +167,28 @@ gqa_status gqa_decode_paged_ex(const uint16_t* q, const uint16_t* k_pool, const 
                                int max_seq_len, void* workspace, size_t ws_bytes, void* stream,
                                const gqa_options* opt);
 
+/* Size of the per-GPU device array used by gqa_decode_noalloc: 8 MiB. */
+#define GQA_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/* gqa_decode for callers that cannot allocate device memory -- e.g. a plugin whose device
+ * memory is budgeted by its host framework, a latency-critical loop that cannot afford
+ * cudaMalloc's implicit synchronisation, or a C / FFI caller with no device allocator.
+ * No counterpart on the pages: it is the same decode step with the workspace replaced by a
+ * library-owned device array of GQA_NOALLOC_SCRATCH_BYTES on every GPU that loads the
+ * library (held until the process exits).  The caller still passes q, k, v and o as for
+ * gqa_decode.  The call allocates nothing.
+ *  - Shapes whose workspace (gqa_decode_workspace_size with n_splits = 0) exceeds
+ *    GQA_NOALLOC_SCRATCH_BYTES are rejected with GQA_ERR_WORKSPACE; use gqa_decode then.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array: calls that overlap on the GPU (other
+ *    streams, other host threads) race and corrupt each other's results.  Each call
+ *    clears the array's status word and counters on `stream` before its kernel. */
+gqa_status gqa_decode_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
+                              int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head, float scale,
+                              void* stream);
+
 #ifdef __cplusplus
 }
 #endif
