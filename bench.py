@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--workload", choices=sorted(gi.WORKLOADS), default="long")
     ap.add_argument("--s-kv", type=int, default=0,
                     help="contiguous workloads: override S_kv (smaller cases for profiler captures)")
+    ap.add_argument("--block-size", type=int, default=0,
+                    help="paged workload: override the KV block size")
     ap.add_argument("--n-splits", type=int, default=0)
     ap.add_argument("--merge-mode", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -64,6 +66,22 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def max_over_ranks(x: float) -> float:
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_step: int, steps: int, world: int, t_max_ms: float) -> float:
+    """Whole-job GB/s: every rank processed steps x bytes_per_step; the slowest rank's time counts."""
+    return bytes_per_step * steps * world / (t_max_ms * 1e-3) / 1e9
 
 
 def measured_peak():
@@ -157,11 +175,13 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------------------------
-def load_inputs(name: str, s_kv: int = 0):
+def load_inputs(name: str, s_kv: int = 0, block_size: int = 0):
+    import dataclasses
     w = gi.WORKLOADS[name]
     if s_kv and w.kind == "contiguous" and s_kv != w.S_kv:
-        import dataclasses
         w = dataclasses.replace(w, name=f"{w.name}[S_kv={s_kv}]", S_kv=int(s_kv))
+    if block_size and w.kind == "paged" and block_size != w.block_size:
+        w = dataclasses.replace(w, name=f"{w.name}[block={block_size}]", block_size=int(block_size))
     x = gi.make(w)
     return w, x
 
@@ -244,7 +264,7 @@ def run_reference(args, rank, world):
     """The oracle as the reference arm: host cores, bounded samples, the same metric."""
     if rank != 0:
         return 0
-    w, x = load_inputs(args.workload, args.s_kv)
+    w, x = load_inputs(args.workload, args.s_kv, args.block_size)
     steps = args.steps if args.steps is not None else 5
     warm = args.warmup if args.warmup is not None else 1
     per_step = max(0.2, min(10.0, 150.0 / max(1, steps + warm)))
@@ -303,7 +323,7 @@ def main():
     _b.build()
     import decode_attention_03_gb300 as pkg
 
-    w, x = load_inputs(args.workload, args.s_kv)
+    w, x = load_inputs(args.workload, args.s_kv, args.block_size)
     d = to_device(x, dev)
     bytes_step = gi.kv_bytes(x)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -376,13 +396,21 @@ def main():
     status = pkg.gqa_workspace_check(ws, stream)
     if status != 0:
         raise RuntimeError(f"device status word set in the timed region: {status}")
-    t_max = t_ms
-    if world > 1:
-        tt = torch.tensor([t_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_max = float(tt.item())
+    l2_hot = None
+    if flush is not None:
+        # small workloads also report back-to-back steps with the inputs resident in L2
+        h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            h0.record(stream)
+            for _ in range(steps):
+                step()
+            h1.record(stream)
+        torch.cuda.synchronize()
+        hot_ms = h0.elapsed_time(h1) / steps
+        l2_hot = {"us_per_step": round(hot_ms * 1e3, 3), "GB/s": round(bytes_step / (hot_ms * 1e-3) / 1e9, 2)}
+    t_max = max_over_ranks(t_ms)
     ms_step = t_max / steps
-    value = bytes_step * steps * world / (t_max * 1e-3) / 1e9
+    value = job_throughput(bytes_step, steps, world, t_max)
     per_launch_gbs = bytes_step / (ms_step * 1e-3) / 1e9
     peak, peak_src = measured_peak()
     traffic = recorded_traffic(w.name)
@@ -398,7 +426,10 @@ def main():
         cpu = {"value": round(bps / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc}
 
     if rank == 0:
-        launches_per_step = 1 if (w.kind == "paged" or args.merge_mode == 0 or (n_splits or 1) <= 1) else 2
+        if w.kind == "paged":   # partition pass, plus the merge pass when a sequence spans partitions
+            launches_per_step = 2 if int(x["max_seq_len"]) > w.partition_size else 1
+        else:
+            launches_per_step = 1 if (args.merge_mode == 0 or (n_splits or 1) <= 1) else 2
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
             "warmup": warm, "ms_per_step": round(ms_step, 6), "us_per_step": round(ms_step * 1e3, 3),
@@ -411,7 +442,7 @@ def main():
                          "frac": round(per_launch_gbs / peak, 4), "traffic": traffic,
                          "peak_source": peak_src, "kernel": "gqa_split_kernel",
                          "frac_of_nominal_7900": round(per_launch_gbs / NOMINAL_HBM_GBS, 4)},
-            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": steps * launches_per_step,
+            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": steps * launches_per_step, "l2_hot": l2_hot,
             "clocks": clocks.summary(wall0, wall1),
         }
         print(json.dumps(line), flush=True)

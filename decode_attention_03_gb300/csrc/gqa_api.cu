@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/gqa_decode.h"
@@ -89,27 +90,34 @@ gqa_status device_info(int di, int cls, bool paged, int* sms, int* occ) {
   return GQA_OK;
 }
 
-// 2-D map over a (rows, cols) f16 matrix, boxes of 64 columns x box_rows rows, 128-byte swizzle
-gqa_status encode_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
-  cuuint64_t dims[2] = {cols, rows > 0 ? rows : 1};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+// 3-D map over a (rows, cols) f16 matrix seen as (64-column planes, rows, 64 columns):
+// dims {64, rows, cols / 64} with strides {cols * 2 bytes, 128 bytes}.  A box of
+// {64, box_rows, planes} lands in shared memory as `planes` consecutive [box_rows][64]
+// arrays, rows 128 bytes with the 128-byte swizzle.
+gqa_status encode_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows,
+                      uint32_t planes) {
+  cuuint64_t dims[3] = {64, rows > 0 ? rows : 1, cols / 64};
+  cuuint64_t strides[2] = {cols * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, planes};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GQA_OK : GQA_ERR_CUDA;
 }
 
-// Split count: enough (b, g, split) CTAs to fill every resident slot of the GPU once
-// (one wave, all CTAs co-resident), each split at least kMinTilesPerSplit tiles long.
-// Prior art: page "muh_cc_dispatch.py", grid_even_share (grid = min(tiles, SMs x
-// subscription), even shares of tiles).
+// Split count: about one (b, g, split) CTA per SM -- ceil(SMs / units) splits per unit --
+// with every CTA co-resident (at most the resident slots of the GPU) and each split at
+// least kMinTilesPerSplit tiles long.  Measured on GB300: one CTA per SM streaming a
+// long split beats two shorter ones (long context: 591 vs 608 us; 8 x 32768 keys: 153
+// vs 156 us).  Prior art: page "muh_cc_dispatch.py", grid_even_share (grid = min(tiles,
+// SMs x subscription), even shares of tiles).
 int heuristic_splits(int64_t units, int64_t tiles, int sms, int occ) {
   const int64_t slots = (int64_t)sms * occ;
   if (tiles <= 0) return 1;
-  if (units >= slots) return 1;
-  int64_t n = slots / units;
+  if (units >= sms) return 1;
+  int64_t n = (sms + units - 1) / units;
+  if (n > slots / units) n = slots / units;
   const int64_t cap = tiles / kMinTilesPerSplit;
   if (n > cap) n = cap;
   if (n < 1) n = 1;
@@ -229,8 +237,8 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
 
   CUtensorMap tk, tv;
   const uint64_t cols = (uint64_t)h_kv * D, nrows = (uint64_t)B * (uint64_t)S_kv;
-  if ((s = encode_map(&tk, k, cols, nrows, kTile)) != GQA_OK) return s;
-  if ((s = encode_map(&tv, v, cols, nrows, kTile)) != GQA_OK) return s;
+  if ((s = encode_map(&tk, k, cols, nrows, kTile, (uint32_t)D / 64)) != GQA_OK) return s;
+  if ((s = encode_map(&tv, v, cols, nrows, kTile, (uint32_t)D / 64)) != GQA_OK) return s;
 
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   DecodeArgs a;
@@ -290,8 +298,10 @@ gqa_status plan_paged(int N, int h_q, int h_kv, int D, int max_seq_len, int part
   const int64_t parts = ((int64_t)max_seq_len + partition_size - 1) / partition_size;
   if (parts > 65535) return GQA_ERR_INVALID_ARG;
   p->max_parts = parts > 0 ? (int)parts : 1;
-  p->units = (int64_t)N * h_kv;
-  p->R = (int64_t)N * h_q;
+  // the kernel runs on at most kPagedSeqs sequences per launch; the workspace serves one launch
+  const int64_t n_launch = std::min<int64_t>(N, kPagedSeqs);
+  p->units = n_launch * h_kv;
+  p->R = n_launch * h_q;
   p->lay = ws_layout(p->units, p->max_parts, p->R, D);
   return GQA_OK;
 }
@@ -308,6 +318,7 @@ gqa_status paged_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t*
   if (!(block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64)) return GQA_ERR_INVALID_ARG;
   if (partition_size / block_size > kMaxPagedBlocksPerPart) return GQA_ERR_INVALID_ARG;
   if (max_blocks < 1 || num_blocks < 0) return GQA_ERR_INVALID_ARG;
+  if ((int64_t)max_blocks * block_size >= (int64_t(1) << 31)) return GQA_ERR_INVALID_ARG;
   if ((int64_t)num_blocks * block_size >= (int64_t(1) << 31)) return GQA_ERR_INVALID_ARG;
   if (N == 0) return GQA_OK;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o) || !aligned16(ws) ||
@@ -321,43 +332,61 @@ gqa_status paged_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t*
 
   CUtensorMap tk, tv;
   const uint64_t cols = (uint64_t)h_kv * D, nrows = (uint64_t)num_blocks * block_size;
-  if ((s = encode_map(&tk, k_pool, cols, nrows, (uint32_t)block_size)) != GQA_OK) return s;
-  if ((s = encode_map(&tv, v_pool, cols, nrows, (uint32_t)block_size)) != GQA_OK) return s;
+  if ((s = encode_map(&tk, k_pool, cols, nrows, (uint32_t)block_size, (uint32_t)D / 64)) != GQA_OK) return s;
+  if ((s = encode_map(&tv, v_pool, cols, nrows, (uint32_t)block_size, (uint32_t)D / 64)) != GQA_OK) return s;
 
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   DecodeArgs a;
   std::memset(&a, 0, sizeof(a));
-  a.q = reinterpret_cast<const __half*>(q);
-  a.o = reinterpret_cast<__half*>(o);
   a.status = reinterpret_cast<uint32_t*>(wsb);
+  a.queue = reinterpret_cast<uint32_t*>(wsb) + 1;
+  a.done = reinterpret_cast<uint32_t*>(wsb) + 2;
   a.counters = reinterpret_cast<uint32_t*>(wsb + p.lay.counters);
   if (p.max_parts > 1) {
     a.ws_m = reinterpret_cast<float*>(wsb + p.lay.m);
     a.ws_l = reinterpret_cast<float*>(wsb + p.lay.l);
     a.ws_o = reinterpret_cast<float*>(wsb + p.lay.o);
   }
-  a.block_tables = tables;
-  a.seq_lens = lens;
   a.max_blocks_per_seq = max_blocks;
   a.num_blocks = num_blocks;
   a.block_size = block_size;
   a.partition_size = partition_size;
-  a.B = N;
   a.T_q = 1;
   a.h_q = h_q;
   a.h_kv = h_kv;
   a.G = h_q / h_kv;
   a.rows = p.rows;
-  a.R = p.R;
   a.n_splits = p.max_parts;
   a.merge_in_kernel = 1;
   a.scale_log2 = scale * kLog2e;
   a.timeout_ns = opt.timeout_us ? (uint64_t)opt.timeout_us * 1000ull : kDefaultTimeoutNs;
   a.stall_cta = opt.test_stall_cta;
 
-  dim3 grid((unsigned)h_kv, (unsigned)p.max_parts, (unsigned)N);
-  if (launch_unit(p.di, p.cls, true, grid, reinterpret_cast<cudaStream_t>(stream), tk, tv, a) != cudaSuccess)
-    return GQA_ERR_CUDA;
+  // persistent: one wave of CTAs pulling (sequence, partition, KV head) items from a queue;
+  // batches beyond kPagedSeqs sequences run as consecutive launches on the same stream
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  for (int s0 = 0; s0 < N; s0 += kPagedSeqs) {
+    const int n = std::min(kPagedSeqs, N - s0);
+    a.q = reinterpret_cast<const __half*>(q) + (int64_t)s0 * h_q * D;
+    a.o = reinterpret_cast<__half*>(o) + (int64_t)s0 * h_q * D;
+    a.block_tables = tables + (int64_t)s0 * max_blocks;
+    a.seq_lens = lens + s0;
+    a.B = n;
+    a.R = (int64_t)n * h_q;
+    a.total_items = (int64_t)n * p.max_parts * h_kv;   // upper bound; the kernel counts the real ones
+    const int64_t ctas = std::min<int64_t>((int64_t)sms * occ, a.total_items);
+    if (launch_unit(p.di, p.cls, true, dim3((unsigned)ctas, 1, 1), st, tk, tv, a) != cudaSuccess)
+      return GQA_ERR_CUDA;
+    if (p.max_parts > 1) {
+      // second pass: fold the partitions of every multi-partition sequence
+      const unsigned blocks = (unsigned)((a.R + 7) / 8);
+      if (D == 64)
+        gqa_paged_merge_kernel<64><<<blocks, 256, 0, st>>>(a);
+      else
+        gqa_paged_merge_kernel<128><<<blocks, 256, 0, st>>>(a);
+      if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+    }
+  }
   return GQA_OK;
 }
 

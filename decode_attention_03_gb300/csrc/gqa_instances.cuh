@@ -24,8 +24,21 @@ constexpr int stages_for() {
   return one_per_sm ? (192 * 1024) / stage : (96 * 1024) / stage;
 }
 
+// paged (persistent, one CTA per SM): as many stages as fit next to the merge scratch
+// and the scheduler's tables in the 227 KB a CTA may use, between 2 and 8
+template <int D, int NT, int WN>
+constexpr int paged_stages_for() {
+  using C8 = Cfg<D, NT, WN, 8>;
+  constexpr int fixed = 1024 + C8::EPI_BUFS * C8::PSCRATCH_STRIDE + C8::PCTRL_BYTES;
+  constexpr int n = (227 * 1024 - fixed) / C8::STAGE_BYTES;
+  return n < 2 ? 2 : (n > 8 ? 8 : n);
+}
+
 template <int D, int CLS, bool PAGED>
-struct Inst {
+struct Inst;
+
+template <int D, int CLS>
+struct Inst<D, CLS, false> {
   static constexpr int NT = cls_nt(CLS);
   static constexpr int WN = cls_wn(CLS);
   static constexpr int STAGES = stages_for<D, NT, WN>();
@@ -33,14 +46,35 @@ struct Inst {
   static_assert(C::SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
   static cudaError_t prepare(int* occupancy) {
-    auto fn = gqa_split_kernel<D, NT, WN, STAGES, PAGED>;
+    auto fn = gqa_split_kernel<D, NT, WN, STAGES>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, fn, C::THREADS, C::SMEM_BYTES);
   }
   static cudaError_t launch(dim3 grid, cudaStream_t st, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a) {
-    gqa_split_kernel<D, NT, WN, STAGES, PAGED><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tk, tv, a);
+    gqa_split_kernel<D, NT, WN, STAGES><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tk, tv, a);
+    return cudaGetLastError();
+  }
+};
+
+template <int D, int CLS>
+struct Inst<D, CLS, true> {
+  static constexpr int NT = cls_nt(CLS);
+  static constexpr int WN = cls_wn(CLS);
+  static constexpr int STAGES = paged_stages_for<D, NT, WN>();
+  using C = Cfg<D, NT, WN, STAGES>;
+  static_assert(C::PSMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+  static cudaError_t prepare(int* occupancy) {
+    auto fn = gqa_paged_kernel<D, NT, WN, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::PSMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, fn, C::PTHREADS, C::PSMEM_BYTES);
+  }
+  static cudaError_t launch(dim3 grid, cudaStream_t st, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const DecodeArgs& a) {
+    gqa_paged_kernel<D, NT, WN, STAGES><<<grid, C::PTHREADS, C::PSMEM_BYTES, st>>>(tk, tv, a);
     return cudaGetLastError();
   }
 };

@@ -1,26 +1,34 @@
 // Split-KV GQA decode kernels for sm_103a.
 //
-// One CTA handles one (sequence b, KV head g, split) work unit: the G*T_q query
-// rows that share KV head g, against one contiguous slice of the key axis.
-// Page "kernbench2 ... _gqa_attention_decode_long.py" ("GQA fused-attention
-// decode kernel -- long context") describes the same decomposition for a PE
-// mesh: every rank sweeps its S_kv slice in tiles, keeps a running (m, l, O)
-// and merges partials with _merge_running; here the ranks become CTAs and the
-// reduce-to-root becomes the last-arriving CTA of the unit merging all splits.
-// The paged variant follows page "muh_kernel_map.py", VLLM_KERNEL_MAP
-// 'paged_attention_v2' (per-partition pass, then a cross-partition merge).
+// Work unit: one (sequence b, KV head g) pair -- the G*T_q query rows that share KV
+// head g -- against one contiguous slice of the key axis.  Page "kernbench2 ...
+// _gqa_attention_decode_long.py" ("GQA fused-attention decode kernel -- long
+// context") describes the same decomposition for a PE mesh: every rank sweeps its
+// S_kv slice in tiles, keeps a running (m, l, O) and partials are merged with
+// _merge_running; here the ranks become CTAs and the reduce-to-root becomes the
+// last-arriving CTA of the unit merging all slices.  The paged variant follows page
+// "muh_kernel_map.py", VLLM_KERNEL_MAP 'paged_attention_v2' (a pass per 512-token
+// partition, then a cross-partition merge).
 //
 // CTA layout: kWK*WN consumer warps + 1 producer warp.
-//  * producer (one lane): TMA 2-D tensor loads of each 64-key K and V tile
-//    (128-byte swizzled boxes of 64 f16 columns) into a STAGES-deep ring of
-//    shared-memory buffers, signalled through mbarriers (full/empty).
-//  * consumer warp (ks, nc): keys [16*ks, 16*ks+16) of every tile, query
-//    n-tiles [nc*NT, nc*NT+NT) (8 query rows each).  Scores are computed
-//    transposed, S^T = K Q^T (keys on the MMA's M side, so G*T_q = 4 wastes
-//    only half of an n=8 tile), the softmax runs in the accumulator layout, P
-//    is transposed in registers (movmatrix) into the B operand of
-//    O^T += V^T P^T.  Each warp keeps its own running (m, l, O) over its keys;
-//    the warps' states are merged through shared memory at the end.
+//  * producer: TMA 3-D tensor loads (64 columns x rows x the head's 64-column
+//    planes, 128-byte swizzle) of each 64-key K and V tile into a STAGES-deep ring of
+//    shared-memory buffers, signalled through mbarriers (full / empty).  One box
+//    covers the whole tile (contiguous) or one KV block (paged).
+//  * consumer warp (ks, nc): keys [16*ks, 16*ks+16) of every tile, query n-tiles
+//    [nc*NT, nc*NT+NT) (8 query rows each).  Scores are computed transposed,
+//    S^T = K Q^T (keys on the MMA's M side, so G*T_q = 4 wastes only half of an n=8
+//    tile), the softmax runs in the accumulator layout, P is transposed in registers
+//    (movmatrix) into the B operand of O^T += V^T P^T.  Each warp keeps its own
+//    running (m, l, O) over its keys; the warps' states are merged through shared
+//    memory at the end of the slice.
+//
+// gqa_split_kernel: one CTA per (KV head, split, sequence) of a contiguous K/V.
+// gqa_paged_kernel: persistent, one CTA per SM; a scheduler warp takes
+//   (sequence, partition, KV head) items from an atomic queue and reads the
+//   partition's block ids ahead of time, the producer warp streams the items'
+//   tiles through one ring that runs across items, so a partition's ramp-up
+//   overlaps the previous one's tail.
 #pragma once
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -37,7 +45,9 @@ constexpr uint32_t kDevTimeout = 1u;
 constexpr uint32_t kDevBadInput = 2u;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMaxPagedBlocksPerPart = 512;
+constexpr int kMaxPagedBlocksPerPart = 256;   // paged: block ids of one partition
+constexpr int kItemSlots = 4;      // paged kernel: descriptors in flight between scheduler and workers
+constexpr int kPagedSeqs = 1024;   // paged kernel: sequences per launch (the host splits larger batches)
 
 struct DecodeArgs {
   const __half* q;        // (B, T_q, h_q*D)
@@ -50,6 +60,8 @@ struct DecodeArgs {
   float* ws_o;            // [n_splits][R][D]
   uint32_t* status;       // device error bits
   uint32_t* counters;     // one arrival counter per (b, g) unit
+  uint32_t* queue;        // paged: next work item
+  uint32_t* done;         // paged: CTAs finished (the last one resets queue and done)
   // paged
   const int32_t* block_tables;
   const int32_t* seq_lens;
@@ -57,34 +69,48 @@ struct DecodeArgs {
   int num_blocks;
   int block_size;
   int partition_size;
+  int64_t total_items;    // paged: num_seqs * max_parts * h_kv
   // shape
   int B, T_q, h_q, h_kv, G, rows;  // rows = G*T_q query rows per unit
   int64_t R;                        // B*T_q*h_q rows of the output
   int64_t S_kv;                     // contiguous: keys per sequence
   int64_t s_begin, s_len;           // contiguous: key range swept
-  int n_splits;                     // contiguous: splits per unit; paged: max partitions
+  int n_splits;                     // contiguous: splits per unit; paged: max partitions per sequence
   int merge_in_kernel;              // last CTA of a unit merges the splits
   float scale_log2;                 // scale * log2(e)
   uint64_t timeout_ns;
-  int stall_cta;                    // test hook: CTA whose producer withholds tile 1 (-1 none)
+  int stall_cta;                    // test hook: CTA whose producer withholds a tile (-1 none)
 };
 
 template <int D, int NT, int WN, int STAGES>
 struct Cfg {
   static constexpr int HALVES = D / 64;
-  static constexpr int HALF_BYTES = kTile * 128;         // [kTile][64] f16, 128B-swizzled
-  static constexpr int KV_BYTES = HALVES * HALF_BYTES;   // one K (or V) tile
+  static constexpr int KV_BYTES = HALVES * kTile * 128; // one K (or V) tile: kTile rows x D f16
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;
   static constexpr int CONSUMERS = kWK * WN;
+  static constexpr int CTHREADS = CONSUMERS * 32;
   static constexpr int THREADS = (CONSUMERS + 1) * 32;
   static constexpr int WROWS = 8 * NT;                   // query rows per consumer warp
   static constexpr int OSTRIDE = D + 4;                  // padded row of the merge scratch
   static constexpr int WSCRATCH = WROWS * (OSTRIDE + 2); // floats per warp
   static constexpr int SCRATCH_BYTES = CONSUMERS * WSCRATCH * 4;
   static constexpr int PIPE_BYTES = STAGES * STAGE_BYTES;
+  // split kernel: the merge scratch reuses the drained ring
   static constexpr int DATA_BYTES = PIPE_BYTES > SCRATCH_BYTES ? PIPE_BYTES : SCRATCH_BYTES;
-  static constexpr int CTRL_BYTES = 2 * STAGES * 8 + 16 + kMaxPagedBlocksPerPart * 4;
+  static constexpr int CTRL_BYTES = 2 * STAGES * 8 + 16;
   static constexpr int SMEM_BYTES = 1024 + DATA_BYTES + CTRL_BYTES;
+  // paged kernel: the ring stays busy across items, so the scratch has its own space,
+  // double-buffered between the consumers and the epilogue warp
+  // (a single buffer when two would crowd out the ring: many query rows per KV head)
+  static constexpr int PSCRATCH_STRIDE = (SCRATCH_BYTES + 1023) & ~1023;
+  static constexpr int EPI_BUFS = 2 * PSCRATCH_STRIDE <= 48 * 1024 ? 2 : 1;
+  static constexpr int PSCRATCH_OFF = PIPE_BYTES;
+  static constexpr int PCTRL_OFF = PIPE_BYTES + EPI_BUFS * PSCRATCH_STRIDE;
+  static constexpr int PCTRL_BYTES = (2 * STAGES + 2 * kItemSlots + 2 * EPI_BUFS) * 8 + 16 +
+                                     (kItemSlots + EPI_BUFS) * 48 + kItemSlots * kMaxPagedBlocksPerPart * 4 +
+                                     (2 * kPagedSeqs + 1) * 4;
+  static constexpr int PSMEM_BYTES = 1024 + PCTRL_OFF + PCTRL_BYTES;
+  static constexpr int PTHREADS = (CONSUMERS + 3) * 32;          // + producer, scheduler, epilogue
 };
 
 // Row r of a unit (0 <= r < G*T_q) is query token r / G, head g*G + r % G.
@@ -93,356 +119,219 @@ __device__ __forceinline__ int64_t out_row(const DecodeArgs& a, int b, int g, in
   return ((int64_t)b * a.T_q + tq) * a.h_q + (int64_t)g * a.G + hh;
 }
 
-// Address of 16-byte chunk c (of D/8) of row `row` in a [kTile][D] tile stored
-// as D/64 swizzled [kTile][64] boxes.
-template <int HALF_BYTES>
-__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int c) {
-  return base + (c >> 3) * HALF_BYTES + row * 128 + ((((c & 7) ^ (row & 7))) << 4);
+// Shared-memory tile layout.  A K (or V) tile of kTile rows x D f16 arrives as
+// consecutive TMA boxes of `rb` rows (the whole tile for contiguous K/V, one KV block
+// when paged); a box holds D/64 planes [rb][64] (the 64-column slices of the head),
+// each row of a plane 128 bytes with its 16-byte chunks swizzled (chunk ^ row % 8).
+// Offset of `row` within the tile (before the chunk and plane terms):
+template <int HALVES>
+__device__ __forceinline__ int row_offset(int row, int rb) {
+  return (row / rb) * (rb * 128 * HALVES) + (row % rb) * 128;
 }
 
-// Merge n partials of one output row element; weights exp(m_s - M).
-// Empty partials (m = -inf) contribute nothing; all empty -> (M=-inf, L=0, O=0).
+// address of 16-byte chunk c (of D/8) of `row`, given row_offset(row); planes rb*128 bytes apart
+__device__ __forceinline__ uint32_t chunk_addr(uint32_t base, int row_off, int row, int c, int plane_bytes) {
+  return base + row_off + (c >> 3) * plane_bytes + ((((c & 7) ^ (row & 7))) << 4);
+}
 
-template <int D, int NT, int WN, int STAGES, bool PAGED>
-__global__ void __launch_bounds__(Cfg<D, NT, WN, STAGES>::THREADS)
-gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                 const DecodeArgs a) {
-  using C = Cfg<D, NT, WN, STAGES>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::DATA_BYTES);
-  uint64_t* empty = full + STAGES;
-  volatile int* flags = reinterpret_cast<volatile int*>(empty + STAGES);  // [0] abort, [1] last-CTA
-  int* blk_ids = const_cast<int*>(reinterpret_cast<volatile int*>(flags + 4));
+__device__ __forceinline__ void raise_timeout(const DecodeArgs& a, volatile int* flags) {
+  atomicOr(a.status, kDevTimeout);
+  flags[0] = 1;
+}
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g_kv = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
-  const int unit = b * a.h_kv + g_kv;
+// =====================================================================================
+// consumer warp state and per-tile math
+// =====================================================================================
+template <int D, int NT>
+struct WarpState {
+  static constexpr int KD = D / 16;   // k-steps over d (QK) / m-tiles over d (PV)
+  uint32_t qf[NT][KD][2];             // Q^T fragments (B operand of S^T = K Q^T)
+  float acc[KD][NT][4];               // O^T accumulators (rows d, columns query rows)
+  float m_run[NT][2];                 // running max (log2 domain), query rows 2*tq4, 2*tq4+1
+  float l_run[NT][2];                 // running sum over this lane's keys
+};
 
-  // ---- this CTA's key range [key_begin, key_end) and the number of splits of its unit
-  int64_t key_begin, key_end, y_base = 0;
-  int n_tiles, n_split_unit;
-  if constexpr (!PAGED) {
-    const int64_t tiles_total = (a.s_len + kTile - 1) / kTile;
-    const int64_t t0 = tiles_total * split / a.n_splits;
-    const int64_t t1 = tiles_total * (split + 1) / a.n_splits;
-    key_begin = a.s_begin + t0 * kTile;
-    key_end = min(a.s_begin + t1 * kTile, a.s_begin + a.s_len);
-    n_tiles = (int)(t1 - t0);
-    n_split_unit = a.n_splits;
-    y_base = (int64_t)b * a.S_kv;
-  } else {
-    int len = __ldg(a.seq_lens + b);
-    const int cap = min(a.max_blocks_per_seq * a.block_size, a.n_splits * a.partition_size);
-    if (len < 0 || len > cap) {
-      if (threadIdx.x == 0 && split == 0) atomicOr(a.status, kDevBadInput);
-      len = len < 0 ? 0 : cap;
-    }
-    n_split_unit = (len + a.partition_size - 1) / a.partition_size;
-    if (split >= n_split_unit) {
-      if (split == 0) {  // empty sequence: its output rows are zero
-        for (int i = threadIdx.x; i < a.rows * D; i += blockDim.x) {
-          const int r = i / D, d = i - r * D;
-          a.o[out_row(a, b, g_kv, r) * D + d] = __float2half_rn(0.f);
-        }
-      }
-      return;
-    }
-    key_begin = (int64_t)split * a.partition_size;
-    key_end = min(key_begin + a.partition_size, (int64_t)len);
-    n_tiles = (int)((key_end - key_begin + kTile - 1) / kTile);
-  }
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(ptx::smem_u32(full + s), 1);
-      ptx::mbar_init(ptx::smem_u32(empty + s), C::CONSUMERS);
-    }
-    flags[0] = 0;
-    flags[1] = 0;
-    ptx::fence_mbar_init();
-  }
-  if constexpr (PAGED) {
-    // block ids of this partition, read once (coalesced) by the producer warp
-    if (warp == C::CONSUMERS) {
-      const int nb = (int)((key_end - key_begin + a.block_size - 1) / a.block_size);
-      const int first = (int)(key_begin / a.block_size);
-      const int32_t* row = a.block_tables + (int64_t)b * a.max_blocks_per_seq + first;
-      for (int i = lane; i < nb; i += 32) {
-        int id = __ldg(row + i);
-        if (id < 0 || id >= a.num_blocks) {
-          atomicOr(a.status, kDevBadInput);
-          id = -1;
-        }
-        blk_ids[i] = id;
-      }
-    }
-  }
-  if (warp == C::CONSUMERS && lane == 0) {
-    ptx::prefetch_tensormap(&tmK);
-    ptx::prefetch_tensormap(&tmV);
-  }
-  __syncthreads();
-
-  // =====================================================================
-  // producer warp
-  // =====================================================================
-  if (warp == C::CONSUMERS) {
-    if (lane == 0) {
-      const uint64_t pol = ptx::policy_evict_first();
-      const int stall_tile = (a.stall_cta >= 0 &&
-                              a.stall_cta == (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)))
-                                 ? 1 : -1;
-      int issued = 0;
-      bool gave_up = false;
-      for (int it = 0; it < n_tiles; ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-        if (it >= STAGES) {
-          if (!ptx::mbar_wait_bounded(ptx::smem_u32(empty + s), ph ^ 1u, a.timeout_ns, flags)) {
-            atomicOr(a.status, kDevTimeout);
-            flags[0] = 1;
-            gave_up = true;
-            break;
-          }
-        }
-        issued = it + 1;
-        if (it == stall_tile) continue;  // test hook: this tile is never loaded
-        const uint32_t kdst = ptx::smem_u32(smem + s * C::STAGE_BYTES);
-        const uint32_t vdst = kdst + C::KV_BYTES;
-        const uint32_t fb = ptx::smem_u32(full + s);
-        if constexpr (!PAGED) {
-          ptx::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-          const int y = (int)(y_base + key_begin + (int64_t)it * kTile);
-#pragma unroll
-          for (int h = 0; h < C::HALVES; ++h) {
-            const int x = g_kv * D + h * 64;
-            ptx::tma_load_2d(kdst + h * C::HALF_BYTES, &tmK, fb, x, y, pol);
-            ptx::tma_load_2d(vdst + h * C::HALF_BYTES, &tmV, fb, x, y, pol);
-          }
-        } else {
-          const int bs = a.block_size;
-          const int64_t k0 = key_begin + (int64_t)it * kTile;
-          const int nblk_tile = kTile / bs;
-          const int first = (int)((k0 - key_begin) / bs);
-          int n_load = 0;
-          for (int j = 0; j < nblk_tile; ++j) {
-            if (k0 + (int64_t)j * bs < key_end && blk_ids[first + j] >= 0) ++n_load;
-          }
-          ptx::mbar_arrive_expect_tx(fb, (uint32_t)(n_load * bs * 128 * 2 * C::HALVES));
-          for (int j = 0; j < nblk_tile; ++j) {
-            if (k0 + (int64_t)j * bs >= key_end) break;
-            const int id = blk_ids[first + j];
-            if (id < 0) continue;
-            const int y = id * bs;
-#pragma unroll
-            for (int h = 0; h < C::HALVES; ++h) {
-              const int x = g_kv * D + h * 64;
-              const uint32_t off = h * C::HALF_BYTES + j * bs * 128;
-              ptx::tma_load_2d(kdst + off, &tmK, fb, x, y, pol);
-              ptx::tma_load_2d(vdst + off, &tmV, fb, x, y, pol);
-            }
-          }
-        }
-      }
-      if (gave_up || stall_tile >= 0) {
-        // wait (bounded) for copies still in flight before the CTA can exit
-        for (int it = max(0, issued - STAGES); it < issued; ++it) {
-          if (it == stall_tile) continue;
-          ptx::mbar_wait_bounded(ptx::smem_u32(full + (it % STAGES)), (uint32_t)(it / STAGES) & 1u,
-                                 a.timeout_ns, nullptr);
-        }
-      }
-    }
-    return;
-  }
-
-  // =====================================================================
-  // consumer warps
-  // =====================================================================
-  const int ks = warp % kWK;        // key slice of every tile
-  const int nc = warp / kWK;        // query column (NT n-tiles)
+// Q^T fragments: b0 = Q[row gq][16kk + 2tq4 ..+1], b1 = the same 8 columns further
+template <int D, int NT>
+__device__ __forceinline__ void load_q(WarpState<D, NT>& st, const DecodeArgs& a, int b, int g, int nc, int lane) {
   const int gq = lane >> 2, tq4 = lane & 3;
-  constexpr int KD = D / 16;        // k-steps over d (QK) / m-tiles over d (PV)
-
-  // Q^T fragments (B operand of S^T = K Q^T): b0 = Q[row gq][16kk + 2tq4 ..+1], b1 = +8
-  uint32_t qf[NT][KD][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int r = (nc * NT + nt) * 8 + gq;
     if (r < a.rows) {
-      const uint32_t* qp = reinterpret_cast<const uint32_t*>(a.q + out_row(a, b, g_kv, r) * D);
+      const uint32_t* qp = reinterpret_cast<const uint32_t*>(a.q + out_row(a, b, g, r) * D);
 #pragma unroll
-      for (int kk = 0; kk < KD; ++kk) {
-        qf[nt][kk][0] = __ldg(qp + kk * 8 + tq4);
-        qf[nt][kk][1] = __ldg(qp + kk * 8 + 4 + tq4);
+      for (int kk = 0; kk < WarpState<D, NT>::KD; ++kk) {
+        st.qf[nt][kk][0] = __ldg(qp + kk * 8 + tq4);
+        st.qf[nt][kk][1] = __ldg(qp + kk * 8 + 4 + tq4);
       }
     } else {
 #pragma unroll
-      for (int kk = 0; kk < KD; ++kk) qf[nt][kk][0] = qf[nt][kk][1] = 0u;
+      for (int kk = 0; kk < WarpState<D, NT>::KD; ++kk) st.qf[nt][kk][0] = st.qf[nt][kk][1] = 0u;
     }
   }
+}
 
-  float acc[KD][NT][4];
+template <int D, int NT>
+__device__ __forceinline__ void reset_state(WarpState<D, NT>& st) {
 #pragma unroll
-  for (int i = 0; i < KD; ++i)
+  for (int i = 0; i < WarpState<D, NT>::KD; ++i)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) acc[i][nt][c] = 0.f;
-  float m_run[NT][2], l_run[NT][2];
+      for (int c = 0; c < 4; ++c) st.acc[i][nt][c] = 0.f;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    m_run[nt][0] = m_run[nt][1] = -CUDART_INF_F;
-    l_run[nt][0] = l_run[nt][1] = 0.f;
+    st.m_run[nt][0] = st.m_run[nt][1] = -CUDART_INF_F;
+    st.l_run[nt][0] = st.l_run[nt][1] = 0.f;
   }
+}
 
-  // per-lane ldmatrix row/chunk (K: non-transposed A of S^T; V: transposed A of O^T)
+// Keys of this warp's slice past the range: zero their V rows so that 0 * (stale or
+// NaN) cannot reach O.  The rows were written by TMA; the fence orders these generic
+// writes before the next asynchronous (TMA) write into the same buffer.
+template <int HALVES>
+__device__ __forceinline__ void zero_masked_v(uint8_t* vtile, int ks, int valid, int lane, int rb) {
+  const int per_row = 8 * HALVES;                      // 16-byte chunks of one row
+  for (int i = lane; i < (16 - valid) * per_row; i += 32) {
+    const int row = ks * 16 + valid + i / per_row;
+    const int rem = i % per_row;
+    const int off = row_offset<HALVES>(row, rb) + (rem >> 3) * (rb * 128) + (rem & 7) * 16;
+    *reinterpret_cast<uint4*>(vtile + off) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+}
+
+// One 64-key tile: this warp's 16 keys against its 8*NT query rows.
+template <int D, int NT>
+__device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbase, uint32_t vbase, int valid,
+                                             int ks, int lane, float scale_log2, int rb) {
+  constexpr int KD = WarpState<D, NT>::KD;
+  constexpr int HALVES = D / 64;
+  const int gq = lane >> 2;
   const int k_row = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
   const int k_c0 = lane >> 4;
   const int v_row = ks * 16 + (lane & 7) + ((lane >> 4) & 1) * 8;
   const int v_c0 = (lane >> 3) & 1;
+  const int k_off = row_offset<HALVES>(k_row, rb), v_off = row_offset<HALVES>(v_row, rb);
+  const int plane = rb * 128;
 
-  for (int it = 0; it < n_tiles; ++it) {
-    const int s = it % STAGES;
-    const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-    const bool landed = ptx::mbar_wait_bounded(ptx::smem_u32(full + s), ph, a.timeout_ns, flags);
-    if (!__all_sync(0xffffffffu, landed)) {   // warp-uniform decision
-      if (lane == 0) {
-        atomicOr(a.status, kDevTimeout);
-        flags[0] = 1;
-      }
-      break;
-    }
-    const uint32_t kbase = ptx::smem_u32(smem + s * C::STAGE_BYTES);
-    const uint32_t vbase = kbase + C::KV_BYTES;
-    const int64_t key0 = key_begin + (int64_t)it * kTile + ks * 16;
-    const int valid = (int)max((int64_t)0, min((int64_t)16, key_end - key0));
-
-    if (valid < 16) {
-      // keys past the range: zero their V rows so that 0 * (stale or NaN) cannot reach O
-      uint4* vrow = reinterpret_cast<uint4*>(smem + s * C::STAGE_BYTES + C::KV_BYTES);
-      for (int i = lane; i < (16 - valid) * 8 * C::HALVES; i += 32) {
-        const int h = i / ((16 - valid) * 8);
-        const int rem = i - h * ((16 - valid) * 8);
-        const int row = ks * 16 + valid + rem / 8;
-        vrow[(h * C::HALF_BYTES + row * 128) / 16 + (rem & 7)] = make_uint4(0u, 0u, 0u, 0u);
-      }
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-    }
-
-    if (valid > 0) {
-      // ---- S^T = K Q^T : 16 keys x 8*NT query rows, fp32
-      float sc[NT][4];
+  // ---- S^T = K Q^T : 16 keys x 8*NT query rows, fp32
+  float sc[NT][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+  for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
-      for (int kk = 0; kk < KD; ++kk) {
-        uint32_t af[4];
-        ptx::ldmatrix_x4(af, tile_addr<C::HALF_BYTES>(kbase, k_row, kk * 2 + k_c0));
+  for (int kk = 0; kk < KD; ++kk) {
+    uint32_t af[4];
+    ptx::ldmatrix_x4(af, chunk_addr(kbase, k_off, k_row, kk * 2 + k_c0, plane));
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) ptx::mma_16816(sc[nt], af, qf[nt][kk]);
-      }
-      // ---- scale (log2 domain), mask, online softmax.  sc[nt][c]: key gq (c<2) or gq+8,
-      //      query row 2*tq4 + (c&1) of n-tile nt
-      float alpha[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int key = gq + ((c >> 1) << 3);
-          sc[nt][c] = key < valid ? sc[nt][c] * a.scale_log2 : -CUDART_INF_F;
-        }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          float mx = fmaxf(sc[nt][j], sc[nt][j + 2]);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float m_new = fmaxf(m_run[nt][j], mx);
-          const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
-          alpha[nt][j] = ptx::ex2(m_run[nt][j] - m_use);
-          m_run[nt][j] = m_new;
-          const float p0 = ptx::ex2(sc[nt][j] - m_use);
-          const float p1 = ptx::ex2(sc[nt][j + 2] - m_use);
-          l_run[nt][j] = l_run[nt][j] * alpha[nt][j] + (p0 + p1);
-          sc[nt][j] = p0;
-          sc[nt][j + 2] = p1;
-        }
-      }
-      // ---- rescale O^T (rows d, columns = query rows 2*tq4, 2*tq4+1)
-#pragma unroll
-      for (int i = 0; i < KD; ++i)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          acc[i][nt][0] *= alpha[nt][0];
-          acc[i][nt][1] *= alpha[nt][1];
-          acc[i][nt][2] *= alpha[nt][0];
-          acc[i][nt][3] *= alpha[nt][1];
-        }
-      // ---- P^T as the B operand (keys x query rows): transpose 8x8 f16 blocks in registers
-      uint32_t pf[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        pf[nt][0] = ptx::movmatrix_trans(ptx::pack_half2(sc[nt][0], sc[nt][1]));
-        pf[nt][1] = ptx::movmatrix_trans(ptx::pack_half2(sc[nt][2], sc[nt][3]));
-      }
-      // ---- O^T += V^T P^T
-#pragma unroll
-      for (int i = 0; i < KD; ++i) {
-        uint32_t af[4];
-        ptx::ldmatrix_x4_trans(af, tile_addr<C::HALF_BYTES>(vbase, v_row, i * 2 + v_c0));
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) ptx::mma_16816(acc[i][nt], af, pf[nt]);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(empty + s));
+    for (int nt = 0; nt < NT; ++nt) ptx::mma_16816(sc[nt], af, st.qf[nt][kk]);
   }
+  // ---- scale (log2 domain), mask, online softmax.  sc[nt][c]: key gq (c<2) or gq+8,
+  //      query row 2*tq4 + (c&1) of n-tile nt
+  float alpha[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int key = gq + ((c >> 1) << 3);
+      sc[nt][c] = key < valid ? sc[nt][c] * scale_log2 : -CUDART_INF_F;
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float mx = fmaxf(sc[nt][j], sc[nt][j + 2]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(st.m_run[nt][j], mx);
+      const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
+      alpha[nt][j] = ptx::ex2(st.m_run[nt][j] - m_use);
+      st.m_run[nt][j] = m_new;
+      const float p0 = ptx::ex2(sc[nt][j] - m_use);
+      const float p1 = ptx::ex2(sc[nt][j + 2] - m_use);
+      st.l_run[nt][j] = st.l_run[nt][j] * alpha[nt][j] + (p0 + p1);
+      sc[nt][j] = p0;
+      sc[nt][j + 2] = p1;
+    }
+  }
+  // ---- rescale O^T (rows d, columns = query rows 2*tq4, 2*tq4+1)
+#pragma unroll
+  for (int i = 0; i < KD; ++i)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      st.acc[i][nt][0] *= alpha[nt][0];
+      st.acc[i][nt][1] *= alpha[nt][1];
+      st.acc[i][nt][2] *= alpha[nt][0];
+      st.acc[i][nt][3] *= alpha[nt][1];
+    }
+  // ---- P^T as the B operand (keys x query rows): transpose 8x8 f16 blocks in registers
+  uint32_t pf[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    pf[nt][0] = ptx::movmatrix_trans(ptx::pack_half2(sc[nt][0], sc[nt][1]));
+    pf[nt][1] = ptx::movmatrix_trans(ptx::pack_half2(sc[nt][2], sc[nt][3]));
+  }
+  // ---- O^T += V^T P^T
+#pragma unroll
+  for (int i = 0; i < KD; ++i) {
+    uint32_t af[4];
+    ptx::ldmatrix_x4_trans(af, chunk_addr(vbase, v_off, v_row, i * 2 + v_c0, plane));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) ptx::mma_16816(st.acc[i][nt], af, pf[nt]);
+  }
+}
 
-  // ---- merge the kWK key-slice warps of each query column through shared memory
-  constexpr uint32_t kConsumerThreads = C::CONSUMERS * 32;
-  // all tiles consumed (the ring is free); a wait that gave up anywhere -> leave the output alone
-  if (ptx::named_bar_or(1, kConsumerThreads, flags[0] != 0)) return;
+// =====================================================================================
+// end of a slice: merge the key-slice warps, emit, merge the unit's slices
+// =====================================================================================
 
+// Reduce l over the lanes that share a query row and write this warp's (O, m, l)
+// into its block of the shared-memory scratch.
+template <int D, int NT, int WN, int STAGES>
+__device__ __forceinline__ void stash_warp(WarpState<D, NT>& st, float* scratch, int warp, int lane) {
+  using C = Cfg<D, NT, WN, STAGES>;
+  const int gq = lane >> 2, tq4 = lane & 3;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      float l = l_run[nt][j];
+      float l = st.l_run[nt][j];
       l += __shfl_xor_sync(0xffffffffu, l, 4);
       l += __shfl_xor_sync(0xffffffffu, l, 8);
       l += __shfl_xor_sync(0xffffffffu, l, 16);
-      l_run[nt][j] = l;
+      st.l_run[nt][j] = l;
     }
-  float* scratch = reinterpret_cast<float*>(smem);
-  {
-    float* wsp = scratch + warp * C::WSCRATCH;
-    float* wm = wsp + C::WROWS * C::OSTRIDE;
-    float* wl = wm + C::WROWS;
+  float* wsp = scratch + warp * C::WSCRATCH;
+  float* wm = wsp + C::WROWS * C::OSTRIDE;
+  float* wl = wm + C::WROWS;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int r0 = nt * 8 + 2 * tq4;
+  for (int nt = 0; nt < NT; ++nt) {
+    const int r0 = nt * 8 + 2 * tq4;
 #pragma unroll
-      for (int i = 0; i < KD; ++i) {
-        wsp[r0 * C::OSTRIDE + i * 16 + gq] = acc[i][nt][0];
-        wsp[(r0 + 1) * C::OSTRIDE + i * 16 + gq] = acc[i][nt][1];
-        wsp[r0 * C::OSTRIDE + i * 16 + gq + 8] = acc[i][nt][2];
-        wsp[(r0 + 1) * C::OSTRIDE + i * 16 + gq + 8] = acc[i][nt][3];
-      }
-      if (gq == 0) {
-        wm[r0] = m_run[nt][0];
-        wm[r0 + 1] = m_run[nt][1];
-        wl[r0] = l_run[nt][0];
-        wl[r0 + 1] = l_run[nt][1];
-      }
+    for (int i = 0; i < WarpState<D, NT>::KD; ++i) {
+      wsp[r0 * C::OSTRIDE + i * 16 + gq] = st.acc[i][nt][0];
+      wsp[(r0 + 1) * C::OSTRIDE + i * 16 + gq] = st.acc[i][nt][1];
+      wsp[r0 * C::OSTRIDE + i * 16 + gq + 8] = st.acc[i][nt][2];
+      wsp[(r0 + 1) * C::OSTRIDE + i * 16 + gq + 8] = st.acc[i][nt][3];
+    }
+    if (gq == 0) {
+      wm[r0] = st.m_run[nt][0];
+      wm[r0 + 1] = st.m_run[nt][1];
+      wl[r0] = st.l_run[nt][0];
+      wl[r0 + 1] = st.l_run[nt][1];
     }
   }
-  ptx::named_bar_sync(1, kConsumerThreads);
+}
 
-  const bool single = (n_split_unit == 1);
-  for (int idx = threadIdx.x; idx < a.rows * D; idx += kConsumerThreads) {
+// Combine the kWK key-slice warps of every query row of the unit and emit: the final
+// f16 output (single slice), the caller's partial (single slice, partial mode) or this
+// slice's fp32 partial in the workspace.  Consumer threads only.
+template <int D, int NT, int WN, int STAGES>
+__device__ __forceinline__ void emit_slice(const DecodeArgs& a, const float* scratch, int b, int g, int slice,
+                                           bool single, int tid, int nthreads) {
+  using C = Cfg<D, NT, WN, STAGES>;
+  for (int idx = tid; idx < a.rows * D; idx += nthreads) {
     const int r = idx / D, d = idx - r * D;
     const int col = r / C::WROWS, lr = r - col * C::WROWS;
     float mk[kWK];
@@ -463,7 +352,7 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         O += w * wsp[lr * C::OSTRIDE + d];
       }
     }
-    const int64_t orow = out_row(a, b, g_kv, r);
+    const int64_t orow = out_row(a, b, g, r);
     if (single) {
       if (a.o != nullptr) {
         a.o[orow * D + d] = __float2half_rn(L > 0.f ? O / L : 0.f);
@@ -475,7 +364,7 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         a.o_part_out[orow * D + d] = O;
       }
     } else {
-      const int64_t prow = (int64_t)split * a.R + orow;
+      const int64_t prow = (int64_t)slice * a.R + orow;
       if (d == 0) {
         a.ws_m[prow] = M * kLn2;
         a.ws_l[prow] = L;
@@ -483,44 +372,572 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       a.ws_o[prow * D + d] = O;
     }
   }
-  if (single || !a.merge_in_kernel) return;
+}
 
-  // ---- last CTA of the unit merges all splits (page: _merge_running, then O / l)
+// After this slice's partial is written: take an arrival ticket for the unit; true
+// on the CTA that arrives last (all other slices of the unit are then in memory).
+template <int CTHREADS>
+__device__ __forceinline__ bool last_to_arrive(const DecodeArgs& a, int unit, int n_slices, volatile int* flags) {
   __threadfence();
-  ptx::named_bar_sync(1, kConsumerThreads);
+  ptx::named_bar_sync(1, CTHREADS);
   if (threadIdx.x == 0) {
     const unsigned prev = atomicAdd(a.counters + unit, 1u);
-    flags[1] = (prev == (unsigned)(n_split_unit - 1)) ? 1 : 0;
+    flags[1] = (prev == (unsigned)(n_slices - 1)) ? 1 : 0;
   }
-  ptx::named_bar_sync(1, kConsumerThreads);
-  if (flags[1] == 0) return;
-  __threadfence();
-  for (int idx = threadIdx.x; idx < a.rows * D; idx += kConsumerThreads) {
-    const int r = idx / D, d = idx - r * D;
-    const int64_t orow = out_row(a, b, g_kv, r);
-    float M = -CUDART_INF_F;
-    for (int s2 = 0; s2 < n_split_unit; ++s2) M = fmaxf(M, __ldcg(a.ws_m + (int64_t)s2 * a.R + orow));
-    float L = 0.f, O = 0.f;
-    if (M != -CUDART_INF_F) {
-      const float M2 = M * kLog2e;
-      for (int s2 = 0; s2 < n_split_unit; ++s2) {
-        const int64_t prow = (int64_t)s2 * a.R + orow;
-        const float w = ptx::ex2(__ldcg(a.ws_m + prow) * kLog2e - M2);
-        L += w * __ldcg(a.ws_l + prow);
-        O += w * __ldcg(a.ws_o + prow * D + d);
-      }
+  ptx::named_bar_sync(1, CTHREADS);
+  const bool last = flags[1] != 0;
+  if (last) __threadfence();
+  return last;
+}
+
+// Fold the n partials of unit (b, g) (page: _merge_running applied left to right) and
+// write the output (O / l) or the merged partial; resets the unit's counter.  Each
+// thread folds IPT items (4 consecutive d of one row) at once, so all loads of one
+// partial step are in flight together.
+template <int D, int NT, int WN, int STAGES>
+__device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int g, int unit, int n) {
+  using C = Cfg<D, NT, WN, STAGES>;
+  constexpr int DQ = D / 4;
+  constexpr int IPT = (C::WROWS * WN * DQ + C::CTHREADS - 1) / C::CTHREADS;
+  const int n_items = a.rows * DQ;
+  float M[IPT], L[IPT];
+  float4 O[IPT];
+  int64_t orow_i[IPT];
+  int c4_i[IPT];
+#pragma unroll
+  for (int i = 0; i < IPT; ++i) {
+    const int item = threadIdx.x + i * C::CTHREADS;
+    const int r = item < n_items ? item / DQ : 0;
+    c4_i[i] = item < n_items ? item - r * DQ : 0;
+    orow_i[i] = out_row(a, b, g, r);
+    M[i] = -CUDART_INF_F;
+    L[i] = 0.f;
+    O[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll 2
+  for (int s2 = 0; s2 < n; ++s2) {
+    float ms[IPT], ls[IPT];
+    float4 os[IPT];
+#pragma unroll
+    for (int i = 0; i < IPT; ++i) {
+      const int64_t prow = (int64_t)s2 * a.R + orow_i[i];
+      ms[i] = __ldcg(a.ws_m + prow) * kLog2e;
+      ls[i] = __ldcg(a.ws_l + prow);
+      os[i] = __ldcg(reinterpret_cast<const float4*>(a.ws_o + prow * D) + c4_i[i]);
     }
+#pragma unroll
+    for (int i = 0; i < IPT; ++i) {
+      const float m_new = fmaxf(M[i], ms[i]);
+      const float ref = m_new == -CUDART_INF_F ? 0.f : m_new;   // both sides empty so far
+      const float so = ptx::ex2(M[i] - ref), sn = ptx::ex2(ms[i] - ref);
+      L[i] = L[i] * so + ls[i] * sn;
+      O[i].x = O[i].x * so + os[i].x * sn;
+      O[i].y = O[i].y * so + os[i].y * sn;
+      O[i].z = O[i].z * so + os[i].z * sn;
+      O[i].w = O[i].w * so + os[i].w * sn;
+      M[i] = m_new;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < IPT; ++i) {
+    if (threadIdx.x + i * C::CTHREADS >= n_items) continue;
+    const int64_t orow = orow_i[i];
     if (a.o != nullptr) {
-      a.o[orow * D + d] = __float2half_rn(L > 0.f ? O / L : 0.f);
+      const float inv = L[i] > 0.f ? 1.f / L[i] : 0.f;
+      __half2* dst = reinterpret_cast<__half2*>(a.o + orow * D + c4_i[i] * 4);
+      dst[0] = __floats2half2_rn(O[i].x * inv, O[i].y * inv);
+      dst[1] = __floats2half2_rn(O[i].z * inv, O[i].w * inv);
     } else {
-      if (d == 0) {
-        a.m_out[orow] = M;
-        a.l_out[orow] = L;
+      if (c4_i[i] == 0) {
+        a.m_out[orow] = M[i] * kLn2;
+        a.l_out[orow] = L[i];
       }
-      a.o_part_out[orow * D + d] = O;
+      reinterpret_cast<float4*>(a.o_part_out + orow * D)[c4_i[i]] = O[i];
     }
   }
   if (threadIdx.x == 0) atomicExch(a.counters + unit, 0u);
+}
+
+// =====================================================================================
+// contiguous K/V: one CTA per (KV head, split, sequence)
+// =====================================================================================
+template <int D, int NT, int WN, int STAGES>
+__global__ void __launch_bounds__(Cfg<D, NT, WN, STAGES>::THREADS)
+gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                 const DecodeArgs a) {
+  using C = Cfg<D, NT, WN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::DATA_BYTES);
+  uint64_t* empty = full + STAGES;
+  volatile int* flags = reinterpret_cast<volatile int*>(empty + STAGES);  // [0] abort, [1] last-CTA
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g_kv = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
+  const int unit = b * a.h_kv + g_kv;
+
+  // ---- this CTA's key range [key_begin, key_end)
+  const int64_t tiles_total = (a.s_len + kTile - 1) / kTile;
+  const int64_t t0 = tiles_total * split / a.n_splits;
+  const int64_t t1 = tiles_total * (split + 1) / a.n_splits;
+  const int64_t key_begin = a.s_begin + t0 * kTile;
+  const int64_t key_end = min(a.s_begin + t1 * kTile, a.s_begin + a.s_len);
+  const int n_tiles = (int)(t1 - t0);
+  const int64_t y_base = (int64_t)b * a.S_kv;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(ptx::smem_u32(full + s), 1);
+      ptx::mbar_init(ptx::smem_u32(empty + s), C::CONSUMERS);
+    }
+    flags[0] = 0;
+    flags[1] = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == C::CONSUMERS && lane == 0) {
+    ptx::prefetch_tensormap(&tmK);
+    ptx::prefetch_tensormap(&tmV);
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- producer warp
+  if (warp == C::CONSUMERS) {
+    if (lane == 0) {
+      const uint64_t pol = ptx::policy_evict_first();
+      const int stall_tile = (a.stall_cta >= 0 &&
+                              a.stall_cta == (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)))
+                                 ? 1 : -1;
+      int issued = 0;
+      bool gave_up = false;
+      for (int it = 0; it < n_tiles; ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+        if (it >= STAGES && !ptx::mbar_wait_bounded(ptx::smem_u32(empty + s), ph ^ 1u, a.timeout_ns, flags)) {
+          raise_timeout(a, flags);
+          gave_up = true;
+          break;
+        }
+        issued = it + 1;
+        if (it == stall_tile) continue;  // test hook: this tile is never loaded
+        const uint32_t kdst = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+        const uint32_t vdst = kdst + C::KV_BYTES;
+        const uint32_t fb = ptx::smem_u32(full + s);
+        ptx::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+        const int y = (int)(y_base + key_begin + (int64_t)it * kTile);
+        ptx::tma_load_3d(kdst, &tmK, fb, 0, y, g_kv * C::HALVES, pol);
+        ptx::tma_load_3d(vdst, &tmV, fb, 0, y, g_kv * C::HALVES, pol);
+      }
+      if (gave_up || stall_tile >= 0) {
+        // wait (bounded) for copies still in flight before the CTA can exit
+        for (int it = max(0, issued - STAGES); it < issued; ++it) {
+          if (it == stall_tile) continue;
+          ptx::mbar_wait_bounded(ptx::smem_u32(full + (it % STAGES)), (uint32_t)(it / STAGES) & 1u,
+                                 a.timeout_ns, nullptr);
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- consumer warps
+  const int ks = warp % kWK;        // key slice of every tile
+  const int nc = warp / kWK;        // query column (NT n-tiles)
+  WarpState<D, NT> st;
+  load_q(st, a, b, g_kv, nc, lane);
+  reset_state(st);
+
+  for (int it = 0; it < n_tiles; ++it) {
+    const int s = it % STAGES;
+    const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+    const bool landed = ptx::mbar_wait_bounded(ptx::smem_u32(full + s), ph, a.timeout_ns, flags);
+    if (!__all_sync(0xffffffffu, landed)) {   // warp-uniform decision
+      if (lane == 0) raise_timeout(a, flags);
+      break;
+    }
+    const uint32_t kbase = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+    const uint32_t vbase = kbase + C::KV_BYTES;
+    const int64_t key0 = key_begin + (int64_t)it * kTile + ks * 16;
+    const int valid = (int)max((int64_t)0, min((int64_t)16, key_end - key0));
+    if (valid < 16) zero_masked_v<C::HALVES>(smem + s * C::STAGE_BYTES + C::KV_BYTES, ks, valid, lane, kTile);
+    if (valid > 0) consume_tile<D, NT>(st, kbase, vbase, valid, ks, lane, a.scale_log2, kTile);
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(empty + s));
+  }
+
+  // all tiles consumed (the ring is free); a wait that gave up anywhere -> leave the output alone
+  if (ptx::named_bar_or(1, C::CTHREADS, flags[0] != 0)) return;
+  float* scratch = reinterpret_cast<float*>(smem);
+  stash_warp<D, NT, WN, STAGES>(st, scratch, warp, lane);
+  ptx::named_bar_sync(1, C::CTHREADS);
+  const bool single = (a.n_splits == 1);
+  emit_slice<D, NT, WN, STAGES>(a, scratch, b, g_kv, split, single, threadIdx.x, C::CTHREADS);
+  if (single || !a.merge_in_kernel) return;
+  if (last_to_arrive<C::CTHREADS>(a, unit, a.n_splits, flags))
+    merge_unit<D, NT, WN, STAGES>(a, b, g_kv, unit, a.n_splits);
+}
+
+// =====================================================================================
+// paged K/V: persistent CTAs over (sequence, partition, KV head) items
+// =====================================================================================
+struct ItemDesc {
+  int b, g, p, kind;        // kind: 0 partition, 2 no more items
+  int n_tiles, n_parts, pad0, pad1;
+  int64_t key_begin, key_end;
+};
+static_assert(sizeof(ItemDesc) == 48, "descriptor slot size");
+
+// Warps: consumers 0..CONSUMERS-1, TMA producer CONSUMERS, scheduler CONSUMERS+1,
+// epilogue CONSUMERS+2.
+//  * scheduler: takes item indices from the queue (one at a time), maps an index to
+//    (sequence, partition, KV head) through a prefix sum of the sequences' partition
+//    counts (so no index is empty), reads the partition's block ids and publishes a
+//    descriptor into a kItemSlots-deep ring -- running up to kItemSlots items ahead.
+//  * producer: for each descriptor, TMA-loads the partition's K/V blocks into the ring.
+//  * consumers: for each descriptor, the tile loop; at its end they leave their
+//    (O, m, l) in one of EPI_BUFS scratch buffers and go on with the next item.
+//  * epilogue: combines the consumer warps of a finished item and writes the f16
+//    output (one-partition sequences) or the partition's fp32 partial; the partials
+//    are folded by gqa_paged_merge_kernel (the second pass of paged attention v2).
+template <int D, int NT, int WN, int STAGES>
+__global__ void __launch_bounds__(Cfg<D, NT, WN, STAGES>::PTHREADS)
+gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                 const DecodeArgs a) {
+  using C = Cfg<D, NT, WN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* scratch = reinterpret_cast<float*>(smem + C::PSCRATCH_OFF);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::PCTRL_OFF);
+  uint64_t* empty = full + STAGES;
+  uint64_t* ifull = empty + STAGES;
+  uint64_t* iempty = ifull + kItemSlots;
+  uint64_t* sfull = iempty + kItemSlots;                       // scratch buffer filled by the consumers
+  uint64_t* sfree = sfull + C::EPI_BUFS;                          // scratch buffer emptied by the epilogue warp
+  volatile int* flags = reinterpret_cast<volatile int*>(sfree + C::EPI_BUFS);  // [0] abort
+  ItemDesc* desc = reinterpret_cast<ItemDesc*>(const_cast<int*>(flags + 4));
+  ItemDesc* edesc = desc + kItemSlots;                          // item of each scratch buffer
+  int* ids = reinterpret_cast<int*>(edesc + C::EPI_BUFS);          // [kItemSlots][kMaxPagedBlocksPerPart]
+  int* pre = ids + kItemSlots * kMaxPagedBlocksPerPart;         // [N + 1] partition-count prefix
+  int* lens_s = pre + kPagedSeqs + 1;                           // [N] clamped lengths
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = a.partition_size;
+  const int N = a.B;
+  const int cap = min(a.max_blocks_per_seq * a.block_size, a.n_splits * P);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(ptx::smem_u32(full + s), 1);
+      ptx::mbar_init(ptx::smem_u32(empty + s), C::CONSUMERS);
+    }
+    for (int s = 0; s < kItemSlots; ++s) {
+      ptx::mbar_init(ptx::smem_u32(ifull + s), 1);
+      ptx::mbar_init(ptx::smem_u32(iempty + s), C::CONSUMERS + 1);
+    }
+    for (int s = 0; s < C::EPI_BUFS; ++s) {
+      ptx::mbar_init(ptx::smem_u32(sfull + s), C::CONSUMERS);
+      ptx::mbar_init(ptx::smem_u32(sfree + s), 1);
+    }
+    flags[0] = 0;
+    flags[1] = 0;
+    pre[0] = 0;
+    ptx::fence_mbar_init();
+  }
+  // lengths (clamped to what the table can hold) and partitions per sequence
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    int len = __ldg(a.seq_lens + i);
+    if (len < 0 || len > cap) {
+      if (blockIdx.x == 0) atomicOr(a.status, kDevBadInput);
+      len = len < 0 ? 0 : cap;
+    }
+    lens_s[i] = len;
+    pre[i + 1] = (len + P - 1) / P;
+  }
+  __syncthreads();
+  if (warp == 0) {   // inclusive scan of pre[1..N], 32 entries at a time
+    int carry = 0;
+    for (int base = 0; base < N; base += 32) {
+      const int i = base + lane;
+      int v = i < N ? pre[i + 1] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += t;
+      }
+      if (i < N) pre[i + 1] = v + carry;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  if (warp == C::CONSUMERS && lane == 0) {
+    ptx::prefetch_tensormap(&tmK);
+    ptx::prefetch_tensormap(&tmV);
+  }
+  __syncthreads();
+  const int64_t total = (int64_t)pre[N] * a.h_kv;
+  // sequences without keys get zero output rows (spread over the CTAs)
+  for (int b = blockIdx.x; b < N; b += gridDim.x) {
+    if (lens_s[b] != 0) continue;
+    __half* dst = a.o + (int64_t)b * a.T_q * a.h_q * D;
+    for (int i = threadIdx.x; i < a.T_q * a.h_q * D; i += blockDim.x) dst[i] = __float2half_rn(0.f);
+  }
+
+  // ---------------------------------------------------------------- epilogue warp
+  if (warp == C::CONSUMERS + 2) {
+    for (int ke = 0;; ++ke) {
+      const int buf = ke % C::EPI_BUFS;
+      const bool got = ptx::mbar_wait_bounded(ptx::smem_u32(sfull + buf), (uint32_t)(ke / C::EPI_BUFS) & 1u,
+                                              a.timeout_ns, flags);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) raise_timeout(a, flags);
+        break;
+      }
+      const ItemDesc d = edesc[buf];
+      if (d.kind == 2) break;
+      const float* sb = reinterpret_cast<const float*>(smem + C::PSCRATCH_OFF + buf * C::PSCRATCH_STRIDE);
+      emit_slice<D, NT, WN, STAGES>(a, sb, d.b, d.g, d.p, d.n_parts == 1, lane, 32);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(sfree + buf));
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- scheduler warp
+  if (warp == C::CONSUMERS + 1) {
+    for (int k = 0;; ++k) {
+      uint32_t it = 0;
+      if (lane == 0) it = atomicAdd(a.queue, 1u);
+      it = __shfl_sync(0xffffffffu, it, 0);
+      const int slot = k % kItemSlots;
+      int ok = 1;
+      if (lane == 0 && k >= kItemSlots)
+        ok = ptx::mbar_wait_bounded(ptx::smem_u32(iempty + slot), ((uint32_t)(k / kItemSlots) & 1u) ^ 1u,
+                                    a.timeout_ns, flags) ? 1 : 0;
+      if (__shfl_sync(0xffffffffu, ok, 0) == 0) {
+        if (lane == 0) raise_timeout(a, flags);
+        break;
+      }
+      ItemDesc d;
+      d.kind = 2;
+      d.b = d.g = d.p = d.n_tiles = d.n_parts = d.pad0 = d.pad1 = 0;
+      d.key_begin = d.key_end = 0;
+      if ((int64_t)it < total) {
+        d.g = (int)(it % (uint32_t)a.h_kv);
+        const int j = (int)(it / (uint32_t)a.h_kv);
+        int lo = 0, hi = N;                        // pre[lo] <= j < pre[hi]
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (pre[mid] <= j) lo = mid; else hi = mid;
+        }
+        d.b = lo;
+        d.p = j - pre[lo];
+        d.n_parts = pre[lo + 1] - pre[lo];
+        d.kind = 0;
+        d.key_begin = (int64_t)d.p * P;
+        d.key_end = min(d.key_begin + P, (int64_t)lens_s[lo]);
+        d.n_tiles = (int)((d.key_end - d.key_begin + kTile - 1) / kTile);
+        const int nb = (int)((d.key_end - d.key_begin + a.block_size - 1) / a.block_size);
+        const int32_t* row = a.block_tables + (int64_t)d.b * a.max_blocks_per_seq + d.key_begin / a.block_size;
+        int* dst = ids + slot * kMaxPagedBlocksPerPart;
+        for (int i = lane; i < nb; i += 32) {
+          int id = __ldg(row + i);
+          if (id < 0 || id >= a.num_blocks) {
+            atomicOr(a.status, kDevBadInput);
+            id = -1;
+          }
+          dst[i] = id;
+        }
+      }
+      __threadfence_block();
+      __syncwarp();
+      if (lane == 0) {
+        desc[slot] = d;
+        ptx::mbar_arrive(ptx::smem_u32(ifull + slot));
+      }
+      if (d.kind == 2) break;
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- TMA producer warp
+  if (warp == C::CONSUMERS) {
+    if (lane == 0) {
+      const uint64_t pol = ptx::policy_evict_first();
+      const bool stall = a.stall_cta >= 0 && a.stall_cta == (int)blockIdx.x;
+      const int bs = a.block_size;
+      const int nblk_tile = kTile / bs;
+      int tile_it = 0, stall_tile = -1;
+      bool gave_up = false;
+      for (int k = 0;; ++k) {
+        const int slot = k % kItemSlots;
+        if (!ptx::mbar_wait_bounded(ptx::smem_u32(ifull + slot), (uint32_t)(k / kItemSlots) & 1u, a.timeout_ns,
+                                    flags)) {
+          raise_timeout(a, flags);
+          gave_up = true;
+          break;
+        }
+        const ItemDesc d = desc[slot];
+        if (d.kind == 2) break;
+        if (stall && k == 0) stall_tile = tile_it + 1;     // test hook: this tile is never loaded
+        const int* bid = ids + slot * kMaxPagedBlocksPerPart;
+        for (int t = 0; t < d.n_tiles; ++t, ++tile_it) {
+          const int s = tile_it % STAGES;
+          const uint32_t ph = (uint32_t)(tile_it / STAGES) & 1u;
+          if (tile_it >= STAGES &&
+              !ptx::mbar_wait_bounded(ptx::smem_u32(empty + s), ph ^ 1u, a.timeout_ns, flags)) {
+            raise_timeout(a, flags);
+            gave_up = true;
+            break;
+          }
+          if (tile_it == stall_tile) continue;
+          const uint32_t kdst = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+          const uint32_t vdst = kdst + C::KV_BYTES;
+          const uint32_t fb = ptx::smem_u32(full + s);
+          const int64_t k0 = d.key_begin + (int64_t)t * kTile;
+          const int first = t * nblk_tile;
+          int n_load = 0;
+          for (int j = 0; j < nblk_tile; ++j)
+            if (k0 + (int64_t)j * bs < d.key_end && bid[first + j] >= 0) ++n_load;
+          ptx::mbar_arrive_expect_tx(fb, (uint32_t)(n_load * bs * 128 * 2 * C::HALVES));
+          for (int j = 0; j < nblk_tile; ++j) {
+            if (k0 + (int64_t)j * bs >= d.key_end) break;
+            const int id = bid[first + j];
+            if (id < 0) continue;
+            const uint32_t off = j * bs * 128 * C::HALVES;
+            ptx::tma_load_3d(kdst + off, &tmK, fb, 0, id * bs, d.g * C::HALVES, pol);
+            ptx::tma_load_3d(vdst + off, &tmV, fb, 0, id * bs, d.g * C::HALVES, pol);
+          }
+        }
+        ptx::mbar_arrive(ptx::smem_u32(iempty + slot));
+        if (gave_up) break;
+      }
+      if (gave_up || stall_tile >= 0) {
+        // wait (bounded) for copies still in flight before the CTA can exit
+        for (int it = max(0, tile_it - STAGES); it < tile_it; ++it) {
+          if (it == stall_tile) continue;
+          ptx::mbar_wait_bounded(ptx::smem_u32(full + (it % STAGES)), (uint32_t)(it / STAGES) & 1u,
+                                 a.timeout_ns, nullptr);
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- consumer warps
+  const int ks = warp % kWK;
+  const int nc = warp / kWK;
+  WarpState<D, NT> st;
+  int tile_it = 0, kc = 0;   // tiles consumed, items handed to the epilogue warp
+  for (int k = 0;; ++k) {
+    const int slot = k % kItemSlots;
+    const bool got = ptx::mbar_wait_bounded(ptx::smem_u32(ifull + slot), (uint32_t)(k / kItemSlots) & 1u,
+                                            a.timeout_ns, flags);
+    const bool ok_w = __all_sync(0xffffffffu, got);
+    if (!ok_w && lane == 0) raise_timeout(a, flags);
+    if (ptx::named_bar_or(1, C::CTHREADS, !ok_w)) return;          // every consumer warp leaves together
+    const ItemDesc d = desc[slot];
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(iempty + slot));
+    bool aborted = false;
+    if (d.kind != 2) {
+      load_q(st, a, d.b, d.g, nc, lane);
+      reset_state(st);
+      for (int t = 0; t < d.n_tiles; ++t, ++tile_it) {
+        const int s = tile_it % STAGES;
+        const uint32_t ph = (uint32_t)(tile_it / STAGES) & 1u;
+        const bool landed = ptx::mbar_wait_bounded(ptx::smem_u32(full + s), ph, a.timeout_ns, flags);
+        if (!__all_sync(0xffffffffu, landed)) {
+          if (lane == 0) raise_timeout(a, flags);
+          aborted = true;
+          break;
+        }
+        const uint32_t kbase = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+        const uint32_t vbase = kbase + C::KV_BYTES;
+        const int64_t key0 = d.key_begin + (int64_t)t * kTile + ks * 16;
+        const int valid = (int)max((int64_t)0, min((int64_t)16, d.key_end - key0));
+        if (valid < 16)
+          zero_masked_v<C::HALVES>(smem + s * C::STAGE_BYTES + C::KV_BYTES, ks, valid, lane, a.block_size);
+        if (valid > 0) consume_tile<D, NT>(st, kbase, vbase, valid, ks, lane, a.scale_log2, a.block_size);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(empty + s));
+      }
+    }
+    // hand the item (or the end marker) to the epilogue warp through scratch buffer kc % C::EPI_BUFS
+    const int buf = kc % C::EPI_BUFS;
+    bool free_ok = true;
+    if (!aborted && kc >= C::EPI_BUFS)
+      free_ok = ptx::mbar_wait_bounded(ptx::smem_u32(sfree + buf), ((uint32_t)(kc / C::EPI_BUFS) & 1u) ^ 1u,
+                                       a.timeout_ns, flags);
+    if (!__all_sync(0xffffffffu, free_ok)) {
+      if (lane == 0) raise_timeout(a, flags);
+      aborted = true;
+    }
+    // every consumer warp reaches this barrier once per item, aborted or not
+    if (ptx::named_bar_or(1, C::CTHREADS, aborted || flags[0] != 0)) return;
+    if (d.kind != 2) {
+      float* sb = reinterpret_cast<float*>(smem + C::PSCRATCH_OFF + buf * C::PSCRATCH_STRIDE);
+      stash_warp<D, NT, WN, STAGES>(st, sb, warp, lane);
+    }
+    if (warp == 0 && lane == 0) edesc[buf] = d;
+    __threadfence_block();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(sfull + buf));
+    ++kc;
+    if (d.kind == 2) break;
+  }
+  // the last CTA to finish resets the item queue for the next launch
+  __threadfence();
+  ptx::named_bar_sync(1, C::CTHREADS);
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(a.done, 1u);
+    if (prev == gridDim.x - 1) {
+      atomicExch(a.queue, 0u);
+      atomicExch(a.done, 0u);
+    }
+  }
+}
+
+// Second pass of paged decode: for every output row of a sequence with more than one
+// partition, fold its partitions' partials (page: _merge_running left to right, then
+// O / l) into the f16 output.  One warp per row; rows of one-partition or empty
+// sequences were written by the first pass.
+template <int D>
+__global__ void __launch_bounds__(256)
+gqa_paged_merge_kernel(const DecodeArgs a) {
+  constexpr int PER = D / 32;
+  const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= a.R) return;
+  const int b = (int)(r / (a.T_q * a.h_q));
+  const int cap = min(a.max_blocks_per_seq * a.block_size, a.n_splits * a.partition_size);
+  int len = __ldg(a.seq_lens + b);
+  len = len < 0 ? 0 : (len > cap ? cap : len);
+  const int n = (len + a.partition_size - 1) / a.partition_size;
+  if (n <= 1) return;
+  float M = -CUDART_INF_F;
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, a.ws_m[(int64_t)s * a.R + r]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  float L = 0.f;
+  const float M2 = M * kLog2e;
+#pragma unroll 4
+  for (int s = 0; s < n; ++s) {
+    const int64_t pr = (int64_t)s * a.R + r;
+    const float w = ptx::ex2(a.ws_m[pr] * kLog2e - M2);
+    L += w * a.ws_l[pr];
+    const float* src = a.ws_o + pr * D + lane * PER;
+    if constexpr (PER == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(src);
+      acc[0] += w * v.x; acc[1] += w * v.y;
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) a.o[r * D + lane * PER + i] = __float2half_rn(acc[i] * inv);
 }
 
 // Public merge of n_parts partials laid out [n_parts][rows] and
@@ -543,6 +960,7 @@ gqa_merge_kernel(const float* __restrict__ m, const float* __restrict__ l, const
   float L = 0.f;
   if (M != -CUDART_INF_F) {
     const float M2 = M * kLog2e;
+#pragma unroll 4
     for (int s = 0; s < n_parts; ++s) {
       const int64_t pr = (int64_t)s * rows + r;
       const float w = ptx::ex2(m[pr] * kLog2e - M2);

@@ -152,7 +152,7 @@ gqa_status gqa_merge_partial(const float* m, const float* l, const float* o_part
  *                 a length-0 sequence gets O = 0
  *   o             (num_seqs, h_q*d_head) f16, written
  * block_size in {8, 16, 32, 64}; partition_size a multiple of 64 with
- * partition_size / block_size <= 512; max_seq_len (host-known bound on seq_lens) sizes the grid.
+ * partition_size / block_size <= 256; max_seq_len (host-known bound on seq_lens) sizes the grid.
  * Block ids outside [0, num_blocks) are not loaded and are reported by gqa_workspace_check. */
 gqa_status gqa_decode_paged(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
                             const int32_t* block_tables, const int32_t* seq_lens, uint16_t* o,

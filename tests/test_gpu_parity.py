@@ -97,7 +97,7 @@ def test_workload_ragged(gqa):
 
 
 def run_paged(gqa, p, **kw):
-    o = gqa.gqa_decode_paged(cuda(p["q"]).reshape(p["num_seqs"], -1), cuda(p["k_pool"]), cuda(p["v_pool"]),
+    o = gqa.gqa_decode_paged(cuda(p["q"]).reshape(p["q"].shape[0], -1), cuda(p["k_pool"]), cuda(p["v_pool"]),
                              cuda(p["block_tables"]), cuda(p["seq_lens"]), p["h_q"], p["h_kv"], p["scale"],
                              max_seq_len=p["max_seq_len"], partition_size=p["partition_size"], **kw)
     torch.cuda.synchronize()
@@ -298,3 +298,31 @@ def test_timeout_is_reported_not_hung(gqa):
     o = gqa.gqa_decode(q, k, v, 8, 2, x["scale"], n_splits=4, workspace_tensor=ws)
     assert gqa.gqa_workspace_check(ws) == gqa.GQA_OK
     assert_close(o, ref_contig(x), "after a timeout")
+
+
+def test_paged_repeated_calls_reset_the_queue(gqa):
+    """The persistent paged kernel's item queue is reset by its last CTA: back-to-back
+    calls on one workspace give identical results."""
+    w = gi.custom(16, 1, 5000, 32, 8, 128, 1101, kind="paged", block_size=16, partition_size=512,
+                  len_lo=1, len_hi=5000)
+    p = gi.make_paged(w)
+    ws = torch.zeros(gqa.gqa_paged_workspace_size(16, 32, 8, 128, p["max_seq_len"], 512), dtype=torch.uint8,
+                     device="cuda")
+    outs = [run_paged(gqa, p, workspace_tensor=ws) for _ in range(3)]
+    assert gqa.gqa_workspace_check(ws) == gqa.GQA_OK
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    assert_close(outs[2], ref_paged(p).reshape(16, -1), "paged, third call")
+
+
+def test_paged_timeout_is_reported_not_hung(gqa):
+    w = gi.custom(8, 1, 4000, 16, 4, 128, 1201, kind="paged", block_size=16, partition_size=512,
+                  len_lo=2000, len_hi=4000)
+    p = gi.make_paged(w)
+    ws = torch.zeros(gqa.gqa_paged_workspace_size(8, 16, 4, 128, p["max_seq_len"], 512), dtype=torch.uint8,
+                     device="cuda")
+    run_paged(gqa, p, workspace_tensor=ws, timeout_us=20000, test_stall_cta=0)
+    assert gqa.gqa_workspace_check(ws) == gqa.GQA_ERR_TIMEOUT
+    gqa.gqa_workspace_init(ws)
+    o = run_paged(gqa, p, workspace_tensor=ws)
+    assert gqa.gqa_workspace_check(ws) == gqa.GQA_OK
+    assert_close(o, ref_paged(p).reshape(8, -1), "paged after a timeout")
