@@ -54,6 +54,8 @@ def parse():
                     help="contiguous workloads: override S_kv (smaller cases for profiler captures)")
     ap.add_argument("--block-size", type=int, default=0,
                     help="paged workload: override the KV block size")
+    ap.add_argument("--head-group", type=int, default=0,
+                    help="paged workload: KV heads per work item (1, 2, 4; 0 = library default)")
     ap.add_argument("--n-splits", type=int, default=0)
     ap.add_argument("--merge-mode", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -202,7 +204,7 @@ def make_step(pkg, w, x, d, out, ws, args):
         def step():
             pkg.gqa_decode_paged(q2, d["k_pool"], d["v_pool"], d["block_tables"], d["seq_lens"], w.h_q, w.h_kv,
                                  w.scale, max_seq_len=x["max_seq_len"], partition_size=w.partition_size,
-                                 out=out, workspace_tensor=ws)
+                                 out=out, workspace_tensor=ws, head_group=args.head_group)
     return step
 
 

@@ -36,7 +36,8 @@ class GQAError(RuntimeError):
 
 class gqa_options(ctypes.Structure):
     _fields_ = [("n_splits", ctypes.c_int), ("merge_mode", ctypes.c_int),
-                ("timeout_us", ctypes.c_uint32), ("test_stall_cta", ctypes.c_int)]
+                ("timeout_us", ctypes.c_uint32), ("test_stall_cta", ctypes.c_int),
+                ("paged_head_group", ctypes.c_int)]
 
 
 def _load():
@@ -113,10 +114,11 @@ def _f32(t: torch.Tensor, name: str) -> None:
         raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
 
 
-def _opts(n_splits=0, merge_mode=0, timeout_us=0, test_stall_cta=-1):
+def _opts(n_splits=0, merge_mode=0, timeout_us=0, test_stall_cta=-1, paged_head_group=0):
     o = gqa_options()
     o.n_splits, o.merge_mode, o.timeout_us, o.test_stall_cta = int(n_splits), int(merge_mode), int(timeout_us), \
         int(test_stall_cta)
+    o.paged_head_group = int(paged_head_group)
     return o
 
 
@@ -244,7 +246,8 @@ def gqa_merge_partial(m, l, o_part, *, m_out=None, l_out=None, o_out=None, strea
 
 def gqa_decode_paged(q, k_pool, v_pool, block_tables, seq_lens, h_q: int, h_kv: int, scale: Optional[float] = None,
                      *, max_seq_len: int, partition_size: int = 512, out=None, workspace_tensor=None,
-                     stream=None, timeout_us: int = 0, test_stall_cta: int = -1) -> torch.Tensor:
+                     stream=None, timeout_us: int = 0, test_stall_cta: int = -1,
+                     head_group: int = 0) -> torch.Tensor:
     """Paged decode; q (N, h_q*D), pools (num_blocks, block_size, h_kv*D), tables (N, max_blocks) int32."""
     _f16(q, "q"), _f16(k_pool, "k_pool"), _f16(v_pool, "v_pool")
     if not (block_tables.is_cuda and block_tables.dtype == torch.int32 and block_tables.is_contiguous()):
@@ -264,7 +267,7 @@ def gqa_decode_paged(q, k_pool, v_pool, block_tables, seq_lens, h_q: int, h_kv: 
     if nbytes == 0:
         raise GQAError(GQA_ERR_INVALID_ARG, "gqa_paged_workspace_size")
     ws = workspace(nbytes, q.device, stream) if workspace_tensor is None else workspace_tensor
-    opt = _opts(0, 0, timeout_us, test_stall_cta)
+    opt = _opts(0, 0, timeout_us, test_stall_cta, head_group)
     st = lib.gqa_decode_paged_ex(_ptr(q2), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens),
                                  _ptr(out), N, block_tables.shape[1], num_blocks, block_size, partition_size,
                                  h_q, h_kv, D, scale, int(max_seq_len), _ptr(ws), ws.numel(), _stream(stream),

@@ -39,7 +39,8 @@ bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 struct DevState {
   bool ready = false;
   int sms = 0;
-  int occ[2][4][2] = {};       // [d index][row class][paged] resident CTAs per SM, 0 = not prepared
+  int occ[2][4][4] = {};       // [d index][row class][0 contiguous, 1/2/3 paged with head group 1/2/4]
+                               // resident CTAs per SM, 0 = not prepared
 };
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
@@ -49,19 +50,23 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
-cudaError_t prepare_unit(int di, int cls, bool paged, int* occ) {
-  if (!paged) return di == 0 ? contig_d64_prepare(cls, occ) : contig_d128_prepare(cls, occ);
-  return di == 0 ? paged_d64_prepare(cls, occ) : paged_d128_prepare(cls, occ);
+// hg = 0: contiguous kernel; hg in {1, 2, 4}: paged kernel with that head group
+cudaError_t prepare_unit(int di, int cls, int hg, int* occ) {
+  if (hg == 0) return di == 0 ? contig_d64_prepare(cls, 1, occ) : contig_d128_prepare(cls, 1, occ);
+  return di == 0 ? paged_d64_prepare(cls, hg, occ) : paged_d128_prepare(cls, hg, occ);
 }
 
-cudaError_t launch_unit(int di, int cls, bool paged, dim3 grid, cudaStream_t st, const CUtensorMap& tk,
+cudaError_t launch_unit(int di, int cls, int hg, dim3 grid, cudaStream_t st, const CUtensorMap& tk,
                         const CUtensorMap& tv, const DecodeArgs& a) {
-  if (!paged) return di == 0 ? contig_d64_launch(cls, grid, st, tk, tv, a) : contig_d128_launch(cls, grid, st, tk, tv, a);
-  return di == 0 ? paged_d64_launch(cls, grid, st, tk, tv, a) : paged_d128_launch(cls, grid, st, tk, tv, a);
+  if (hg == 0)
+    return di == 0 ? contig_d64_launch(cls, 1, grid, st, tk, tv, a) : contig_d128_launch(cls, 1, grid, st, tk, tv, a);
+  return di == 0 ? paged_d64_launch(cls, hg, grid, st, tk, tv, a) : paged_d128_launch(cls, hg, grid, st, tk, tv, a);
 }
+
+int hg_slot(int hg) { return hg == 0 ? 0 : (hg == 1 ? 1 : (hg == 2 ? 2 : 3)); }
 
 // SM count and resident CTAs per SM of one kernel configuration on the current device
-gqa_status device_info(int di, int cls, bool paged, int* sms, int* occ) {
+gqa_status device_info(int di, int cls, int hg, int* sms, int* occ) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -79,10 +84,10 @@ gqa_status device_info(int di, int cls, bool paged, int* sms, int* occ) {
     }
     st.ready = true;
   }
-  int& o = st.occ[di][cls][paged ? 1 : 0];
+  int& o = st.occ[di][cls][hg_slot(hg)];
   if (o == 0) {
     int v = 0;
-    if (prepare_unit(di, cls, paged, &v) != cudaSuccess || v <= 0) return GQA_ERR_CUDA;
+    if (prepare_unit(di, cls, hg, &v) != cudaSuccess || v <= 0) return GQA_ERR_CUDA;
     o = v;
   }
   *sms = st.sms;
@@ -154,6 +159,7 @@ gqa_options defaults() {
   o.merge_mode = 0;
   o.timeout_us = 0;
   o.test_stall_cta = -1;
+  o.paged_head_group = 0;
   return o;
 }
 
@@ -186,7 +192,7 @@ gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_
     p->n_splits = (int)n;
   } else if (need_device) {
     int sms = 0, occ = 0;
-    gqa_status s = device_info(p->di, p->cls, false, &sms, &occ);
+    gqa_status s = device_info(p->di, p->cls, 0, &sms, &occ);
     if (s != GQA_OK) return s;
     p->n_splits = heuristic_splits(p->units, p->tiles, sms, occ);
   } else {
@@ -232,7 +238,7 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
   if (s != GQA_OK) return s;
   if (ws_bytes < p.lay.total) return GQA_ERR_WORKSPACE;
   int sms = 0, occ = 0;
-  s = device_info(p.di, p.cls, false, &sms, &occ);
+  s = device_info(p.di, p.cls, 0, &sms, &occ);
   if (s != GQA_OK) return s;
 
   CUtensorMap tk, tv;
@@ -273,7 +279,7 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   dim3 grid((unsigned)h_kv, (unsigned)p.n_splits, (unsigned)B);
-  if (launch_unit(p.di, p.cls, false, grid, st, tk, tv, a) != cudaSuccess) return GQA_ERR_CUDA;
+  if (launch_unit(p.di, p.cls, 0, grid, st, tk, tv, a) != cudaSuccess) return GQA_ERR_CUDA;
   if (p.n_splits > 1 && !a.merge_in_kernel) {
     return merge_launch(a.ws_m, a.ws_l, a.ws_o, p.n_splits, p.R, D, a.o, a.m_out, a.l_out, a.o_part_out, st);
   }
@@ -316,7 +322,8 @@ gqa_status paged_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t*
   gqa_status s = plan_paged(N, h_q, h_kv, D, max_seq_len, partition_size, &p);
   if (s != GQA_OK) return s;
   if (!(block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64)) return GQA_ERR_INVALID_ARG;
-  if (partition_size / block_size > kMaxPagedBlocksPerPart) return GQA_ERR_INVALID_ARG;
+  // at most kMaxBoxesPerPart TMA boxes per partition; a box holds min(block_size, 16..64) rows
+  if (partition_size / std::min(block_size, 16) > kMaxBoxesPerPart) return GQA_ERR_INVALID_ARG;
   if (max_blocks < 1 || num_blocks < 0) return GQA_ERR_INVALID_ARG;
   if ((int64_t)max_blocks * block_size >= (int64_t(1) << 31)) return GQA_ERR_INVALID_ARG;
   if ((int64_t)num_blocks * block_size >= (int64_t(1) << 31)) return GQA_ERR_INVALID_ARG;
@@ -326,14 +333,21 @@ gqa_status paged_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t*
       (reinterpret_cast<uintptr_t>(lens) & 3u))
     return GQA_ERR_INVALID_ARG;
   if (ws_bytes < p.lay.total) return GQA_ERR_WORKSPACE;
+  // head group: one item (and one TMA box) covers hg KV heads; larger boxes move the
+  // small 16-token blocks at full bandwidth.  Needs a single query column (G <= 16).
+  int hg = opt.paged_head_group;
+  if (hg == 0) hg = p.cls <= 1 ? (h_kv % 4 == 0 ? 4 : (h_kv % 2 == 0 ? 2 : 1)) : 1;
+  if (!(hg == 1 || hg == 2 || hg == 4) || h_kv % hg != 0 || (hg > 1 && p.cls > 1)) return GQA_ERR_INVALID_ARG;
   int sms = 0, occ = 0;
-  s = device_info(p.di, p.cls, true, &sms, &occ);
+  s = device_info(p.di, p.cls, hg, &sms, &occ);
   if (s != GQA_OK) return s;
 
   CUtensorMap tk, tv;
   const uint64_t cols = (uint64_t)h_kv * D, nrows = (uint64_t)num_blocks * block_size;
-  if ((s = encode_map(&tk, k_pool, cols, nrows, (uint32_t)block_size, (uint32_t)D / 64)) != GQA_OK) return s;
-  if ((s = encode_map(&tv, v_pool, cols, nrows, (uint32_t)block_size, (uint32_t)D / 64)) != GQA_OK) return s;
+  const uint32_t box_rows = (uint32_t)std::min(block_size, 16 * (4 / hg));   // min(block, keys per tile)
+  const uint32_t planes = (uint32_t)(hg * D / 64);
+  if ((s = encode_map(&tk, k_pool, cols, nrows, box_rows, planes)) != GQA_OK) return s;
+  if ((s = encode_map(&tv, v_pool, cols, nrows, box_rows, planes)) != GQA_OK) return s;
 
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   DecodeArgs a;
@@ -373,9 +387,9 @@ gqa_status paged_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t*
     a.seq_lens = lens + s0;
     a.B = n;
     a.R = (int64_t)n * h_q;
-    a.total_items = (int64_t)n * p.max_parts * h_kv;   // upper bound; the kernel counts the real ones
+    a.total_items = (int64_t)n * p.max_parts * (h_kv / hg);   // upper bound; the kernel counts the real ones
     const int64_t ctas = std::min<int64_t>((int64_t)sms * occ, a.total_items);
-    if (launch_unit(p.di, p.cls, true, dim3((unsigned)ctas, 1, 1), st, tk, tv, a) != cudaSuccess)
+    if (launch_unit(p.di, p.cls, hg, dim3((unsigned)ctas, 1, 1), st, tk, tv, a) != cudaSuccess)
       return GQA_ERR_CUDA;
     if (p.max_parts > 1) {
       // second pass: fold the partitions of every multi-partition sequence

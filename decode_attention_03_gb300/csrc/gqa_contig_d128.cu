@@ -1,6 +1,6 @@
-// Instances of the split-KV decode kernel: d_head = 128, paged = false.
+// Instances of the split-KV decode kernels: contiguous K/V, d_head = 128.
 #include "gqa_instances.cuh"
 
 namespace gqa {
-GQA_DEFINE_UNIT(contig_d128, 128, false)
+GQA_DEFINE_CONTIG_UNIT(contig_d128, 128)
 }  // namespace gqa

@@ -34,11 +34,8 @@ constexpr int paged_stages_for() {
   return n < 2 ? 2 : (n > 8 ? 8 : n);
 }
 
-template <int D, int CLS, bool PAGED>
-struct Inst;
-
 template <int D, int CLS>
-struct Inst<D, CLS, false> {
+struct Inst {
   static constexpr int NT = cls_nt(CLS);
   static constexpr int WN = cls_wn(CLS);
   static constexpr int STAGES = stages_for<D, NT, WN>();
@@ -58,8 +55,8 @@ struct Inst<D, CLS, false> {
   }
 };
 
-template <int D, int CLS>
-struct Inst<D, CLS, true> {
+template <int D, int CLS, int HG>
+struct PagedInst {
   static constexpr int NT = cls_nt(CLS);
   static constexpr int WN = cls_wn(CLS);
   static constexpr int STAGES = paged_stages_for<D, NT, WN>();
@@ -67,43 +64,64 @@ struct Inst<D, CLS, true> {
   static_assert(C::PSMEM_BYTES <= 227 * 1024, "shared memory budget");
 
   static cudaError_t prepare(int* occupancy) {
-    auto fn = gqa_paged_kernel<D, NT, WN, STAGES>;
+    auto fn = gqa_paged_kernel<D, NT, WN, STAGES, HG>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::PSMEM_BYTES);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, fn, C::PTHREADS, C::PSMEM_BYTES);
   }
   static cudaError_t launch(dim3 grid, cudaStream_t st, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a) {
-    gqa_paged_kernel<D, NT, WN, STAGES><<<grid, C::PTHREADS, C::PSMEM_BYTES, st>>>(tk, tv, a);
+    gqa_paged_kernel<D, NT, WN, STAGES, HG><<<grid, C::PTHREADS, C::PSMEM_BYTES, st>>>(tk, tv, a);
     return cudaGetLastError();
   }
 };
 
-// One of these per (d_head, paged) translation unit; cls in [0, 4).
+// Contiguous units: cls in [0, 4).  Paged units: cls in [0, 4) and head group hg in
+// {1, 2, 4} (hg > 1 only for cls 0 and 1).
 #define GQA_DECLARE_UNIT(NAME)                                                                   \
-  cudaError_t NAME##_prepare(int cls, int* occupancy);                                           \
-  cudaError_t NAME##_launch(int cls, dim3 grid, cudaStream_t st, const CUtensorMap& tk,          \
+  cudaError_t NAME##_prepare(int cls, int hg, int* occupancy);                                   \
+  cudaError_t NAME##_launch(int cls, int hg, dim3 grid, cudaStream_t st, const CUtensorMap& tk,  \
                             const CUtensorMap& tv, const DecodeArgs& a);
 
-#define GQA_DEFINE_UNIT(NAME, D, PAGED)                                                          \
-  cudaError_t NAME##_prepare(int cls, int* occupancy) {                                          \
+#define GQA_DEFINE_CONTIG_UNIT(NAME, D)                                                          \
+  cudaError_t NAME##_prepare(int cls, int, int* occupancy) {                                     \
     switch (cls) {                                                                               \
-      case 0: return Inst<D, 0, PAGED>::prepare(occupancy);                                      \
-      case 1: return Inst<D, 1, PAGED>::prepare(occupancy);                                      \
-      case 2: return Inst<D, 2, PAGED>::prepare(occupancy);                                      \
-      case 3: return Inst<D, 3, PAGED>::prepare(occupancy);                                      \
+      case 0: return Inst<D, 0>::prepare(occupancy);                                             \
+      case 1: return Inst<D, 1>::prepare(occupancy);                                             \
+      case 2: return Inst<D, 2>::prepare(occupancy);                                             \
+      case 3: return Inst<D, 3>::prepare(occupancy);                                             \
     }                                                                                            \
     return cudaErrorInvalidValue;                                                                \
   }                                                                                              \
-  cudaError_t NAME##_launch(int cls, dim3 grid, cudaStream_t st, const CUtensorMap& tk,          \
+  cudaError_t NAME##_launch(int cls, int, dim3 grid, cudaStream_t st, const CUtensorMap& tk,     \
                             const CUtensorMap& tv, const DecodeArgs& a) {                        \
     switch (cls) {                                                                               \
-      case 0: return Inst<D, 0, PAGED>::launch(grid, st, tk, tv, a);                             \
-      case 1: return Inst<D, 1, PAGED>::launch(grid, st, tk, tv, a);                             \
-      case 2: return Inst<D, 2, PAGED>::launch(grid, st, tk, tv, a);                             \
-      case 3: return Inst<D, 3, PAGED>::launch(grid, st, tk, tv, a);                             \
+      case 0: return Inst<D, 0>::launch(grid, st, tk, tv, a);                                    \
+      case 1: return Inst<D, 1>::launch(grid, st, tk, tv, a);                                    \
+      case 2: return Inst<D, 2>::launch(grid, st, tk, tv, a);                                    \
+      case 3: return Inst<D, 3>::launch(grid, st, tk, tv, a);                                    \
     }                                                                                            \
     return cudaErrorInvalidValue;                                                                \
+  }
+
+#define GQA_PAGED_CASES(D, CALL)                                                                 \
+  if (cls == 0 && hg == 1) return PagedInst<D, 0, 1>::CALL;                                      \
+  if (cls == 0 && hg == 2) return PagedInst<D, 0, 2>::CALL;                                      \
+  if (cls == 0 && hg == 4) return PagedInst<D, 0, 4>::CALL;                                      \
+  if (cls == 1 && hg == 1) return PagedInst<D, 1, 1>::CALL;                                      \
+  if (cls == 1 && hg == 2) return PagedInst<D, 1, 2>::CALL;                                      \
+  if (cls == 1 && hg == 4) return PagedInst<D, 1, 4>::CALL;                                      \
+  if (cls == 2 && hg == 1) return PagedInst<D, 2, 1>::CALL;                                      \
+  if (cls == 3 && hg == 1) return PagedInst<D, 3, 1>::CALL;                                      \
+  return cudaErrorInvalidValue;
+
+#define GQA_DEFINE_PAGED_UNIT(NAME, D)                                                           \
+  cudaError_t NAME##_prepare(int cls, int hg, int* occupancy) {                                  \
+    GQA_PAGED_CASES(D, prepare(occupancy))                                                       \
+  }                                                                                              \
+  cudaError_t NAME##_launch(int cls, int hg, dim3 grid, cudaStream_t st, const CUtensorMap& tk,  \
+                            const CUtensorMap& tv, const DecodeArgs& a) {                        \
+    GQA_PAGED_CASES(D, launch(grid, st, tk, tv, a))                                              \
   }
 
 GQA_DECLARE_UNIT(contig_d64)

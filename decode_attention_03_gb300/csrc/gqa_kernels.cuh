@@ -45,7 +45,7 @@ constexpr uint32_t kDevTimeout = 1u;
 constexpr uint32_t kDevBadInput = 2u;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMaxPagedBlocksPerPart = 256;   // paged: block ids of one partition
+constexpr int kMaxBoxesPerPart = 256;   // paged: TMA boxes (blocks or block slices) of one partition
 constexpr int kItemSlots = 4;      // paged kernel: descriptors in flight between scheduler and workers
 constexpr int kPagedSeqs = 1024;   // paged kernel: sequences per launch (the host splits larger batches)
 
@@ -107,7 +107,7 @@ struct Cfg {
   static constexpr int PSCRATCH_OFF = PIPE_BYTES;
   static constexpr int PCTRL_OFF = PIPE_BYTES + EPI_BUFS * PSCRATCH_STRIDE;
   static constexpr int PCTRL_BYTES = (2 * STAGES + 2 * kItemSlots + 2 * EPI_BUFS) * 8 + 16 +
-                                     (kItemSlots + EPI_BUFS) * 48 + kItemSlots * kMaxPagedBlocksPerPart * 4 +
+                                     (kItemSlots + EPI_BUFS) * 48 + kItemSlots * kMaxBoxesPerPart * 4 +
                                      (2 * kPagedSeqs + 1) * 4;
   static constexpr int PSMEM_BYTES = 1024 + PCTRL_OFF + PCTRL_BYTES;
   static constexpr int PTHREADS = (CONSUMERS + 3) * 32;          // + producer, scheduler, epilogue
@@ -119,14 +119,15 @@ __device__ __forceinline__ int64_t out_row(const DecodeArgs& a, int b, int g, in
   return ((int64_t)b * a.T_q + tq) * a.h_q + (int64_t)g * a.G + hh;
 }
 
-// Shared-memory tile layout.  A K (or V) tile of kTile rows x D f16 arrives as
-// consecutive TMA boxes of `rb` rows (the whole tile for contiguous K/V, one KV block
-// when paged); a box holds D/64 planes [rb][64] (the 64-column slices of the head),
-// each row of a plane 128 bytes with its 16-byte chunks swizzled (chunk ^ row % 8).
-// Offset of `row` within the tile (before the chunk and plane terms):
-template <int HALVES>
+// Shared-memory tile layout.  A K (or V) tile arrives as consecutive TMA boxes of
+// `rb` rows (the whole tile for contiguous K/V, a KV block -- or part of one -- when
+// paged); a box holds BOXP planes [rb][64]: the 64-column slices of the tile's heads
+// (D/64 per head, heads one after the other), each row of a plane 128 bytes with its
+// 16-byte chunks swizzled (chunk ^ row % 8).  Offset of `row` within the tile, before
+// the plane and chunk terms:
+template <int BOXP>
 __device__ __forceinline__ int row_offset(int row, int rb) {
-  return (row / rb) * (rb * 128 * HALVES) + (row % rb) * 128;
+  return (row / rb) * (rb * 128 * BOXP) + (row % rb) * 128;
 }
 
 // address of 16-byte chunk c (of D/8) of `row`, given row_offset(row); planes rb*128 bytes apart
@@ -190,31 +191,32 @@ __device__ __forceinline__ void reset_state(WarpState<D, NT>& st) {
 // Keys of this warp's slice past the range: zero their V rows so that 0 * (stale or
 // NaN) cannot reach O.  The rows were written by TMA; the fence orders these generic
 // writes before the next asynchronous (TMA) write into the same buffer.
-template <int HALVES>
-__device__ __forceinline__ void zero_masked_v(uint8_t* vtile, int ks, int valid, int lane, int rb) {
-  const int per_row = 8 * HALVES;                      // 16-byte chunks of one row
+// `vhead` points at the first plane of this warp's head.
+template <int HALVES, int BOXP>
+__device__ __forceinline__ void zero_masked_v(uint8_t* vhead, int ks, int valid, int lane, int rb) {
+  const int per_row = 8 * HALVES;                      // 16-byte chunks of one row of the head
   for (int i = lane; i < (16 - valid) * per_row; i += 32) {
     const int row = ks * 16 + valid + i / per_row;
     const int rem = i % per_row;
-    const int off = row_offset<HALVES>(row, rb) + (rem >> 3) * (rb * 128) + (rem & 7) * 16;
-    *reinterpret_cast<uint4*>(vtile + off) = make_uint4(0u, 0u, 0u, 0u);
+    const int off = row_offset<BOXP>(row, rb) + (rem >> 3) * (rb * 128) + (rem & 7) * 16;
+    *reinterpret_cast<uint4*>(vhead + off) = make_uint4(0u, 0u, 0u, 0u);
   }
   ptx::fence_proxy_async_smem();
   __syncwarp();
 }
 
-// One 64-key tile: this warp's 16 keys against its 8*NT query rows.
-template <int D, int NT>
+// One tile: this warp's 16 keys against its 8*NT query rows; kbase / vbase point at
+// the first plane of the warp's head.
+template <int D, int NT, int BOXP>
 __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbase, uint32_t vbase, int valid,
                                              int ks, int lane, float scale_log2, int rb) {
   constexpr int KD = WarpState<D, NT>::KD;
-  constexpr int HALVES = D / 64;
   const int gq = lane >> 2;
   const int k_row = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
   const int k_c0 = lane >> 4;
   const int v_row = ks * 16 + (lane & 7) + ((lane >> 4) & 1) * 8;
   const int v_c0 = (lane >> 3) & 1;
-  const int k_off = row_offset<HALVES>(k_row, rb), v_off = row_offset<HALVES>(v_row, rb);
+  const int k_off = row_offset<BOXP>(k_row, rb), v_off = row_offset<BOXP>(v_row, rb);
   const int plane = rb * 128;
 
   // ---- S^T = K Q^T : 16 keys x 8*NT query rows, fp32
@@ -255,16 +257,23 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbas
       sc[nt][j + 2] = p1;
     }
   }
-  // ---- rescale O^T (rows d, columns = query rows 2*tq4, 2*tq4+1)
+  // ---- rescale O^T (rows d, columns = query rows 2*tq4, 2*tq4+1); skipped when no
+  //      running max of the warp moved (alpha = 1 everywhere), the common case once the
+  //      first tiles have been seen
+  bool moved = false;
 #pragma unroll
-  for (int i = 0; i < KD; ++i)
+  for (int nt = 0; nt < NT; ++nt) moved |= (alpha[nt][0] != 1.f) | (alpha[nt][1] != 1.f);
+  if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      st.acc[i][nt][0] *= alpha[nt][0];
-      st.acc[i][nt][1] *= alpha[nt][1];
-      st.acc[i][nt][2] *= alpha[nt][0];
-      st.acc[i][nt][3] *= alpha[nt][1];
-    }
+    for (int i = 0; i < KD; ++i)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        st.acc[i][nt][0] *= alpha[nt][0];
+        st.acc[i][nt][1] *= alpha[nt][1];
+        st.acc[i][nt][2] *= alpha[nt][0];
+        st.acc[i][nt][3] *= alpha[nt][1];
+      }
+  }
   // ---- P^T as the B operand (keys x query rows): transpose 8x8 f16 blocks in registers
   uint32_t pf[NT][2];
 #pragma unroll
@@ -324,29 +333,37 @@ __device__ __forceinline__ void stash_warp(WarpState<D, NT>& st, float* scratch,
   }
 }
 
-// Combine the kWK key-slice warps of every query row of the unit and emit: the final
-// f16 output (single slice), the caller's partial (single slice, partial mode) or this
-// slice's fp32 partial in the workspace.  Consumer threads only.
-template <int D, int NT, int WN, int STAGES>
-__device__ __forceinline__ void emit_slice(const DecodeArgs& a, const float* scratch, int b, int g, int slice,
+// Combine the key-slice warps of every query row of the item's HG KV heads (g0 ..
+// g0+HG-1) and emit: the final f16 output (single slice), the caller's partial (single
+// slice, partial mode) or this slice's fp32 partial in the workspace.  With HG heads a
+// head has kWK/HG key-slice warps (hh*KS .. hh*KS+KS-1); with one head, warp col*kWK+k
+// holds key slice k of query column col.
+template <int D, int NT, int WN, int STAGES, int HG = 1>
+__device__ __forceinline__ void emit_slice(const DecodeArgs& a, const float* scratch, int b, int g0, int slice,
                                            bool single, int tid, int nthreads) {
   using C = Cfg<D, NT, WN, STAGES>;
-  for (int idx = tid; idx < a.rows * D; idx += nthreads) {
-    const int r = idx / D, d = idx - r * D;
+  constexpr int KS = kWK / HG;
+  const int per_head = a.rows * D;
+  for (int idx = tid; idx < HG * per_head; idx += nthreads) {
+    const int hh = idx / per_head;
+    const int rem = idx - hh * per_head;
+    const int r = rem / D, d = rem - r * D;
     const int col = r / C::WROWS, lr = r - col * C::WROWS;
-    float mk[kWK];
+    const int w0 = HG > 1 ? hh * KS : col * kWK;
+    const int g = g0 + hh;
+    float mk[KS];
     float M = -CUDART_INF_F;
 #pragma unroll
-    for (int k = 0; k < kWK; ++k) {
-      const float* wsp = scratch + (col * kWK + k) * C::WSCRATCH;
+    for (int k = 0; k < KS; ++k) {
+      const float* wsp = scratch + (w0 + k) * C::WSCRATCH;
       mk[k] = wsp[C::WROWS * C::OSTRIDE + lr];
       M = fmaxf(M, mk[k]);
     }
     float L = 0.f, O = 0.f;
     if (M != -CUDART_INF_F) {
 #pragma unroll
-      for (int k = 0; k < kWK; ++k) {
-        const float* wsp = scratch + (col * kWK + k) * C::WSCRATCH;
+      for (int k = 0; k < KS; ++k) {
+        const float* wsp = scratch + (w0 + k) * C::WSCRATCH;
         const float w = ptx::ex2(mk[k] - M);
         L += w * wsp[C::WROWS * C::OSTRIDE + C::WROWS + lr];
         O += w * wsp[lr * C::OSTRIDE + d];
@@ -558,8 +575,9 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     const uint32_t vbase = kbase + C::KV_BYTES;
     const int64_t key0 = key_begin + (int64_t)it * kTile + ks * 16;
     const int valid = (int)max((int64_t)0, min((int64_t)16, key_end - key0));
-    if (valid < 16) zero_masked_v<C::HALVES>(smem + s * C::STAGE_BYTES + C::KV_BYTES, ks, valid, lane, kTile);
-    if (valid > 0) consume_tile<D, NT>(st, kbase, vbase, valid, ks, lane, a.scale_log2, kTile);
+    if (valid < 16)
+      zero_masked_v<C::HALVES, C::HALVES>(smem + s * C::STAGE_BYTES + C::KV_BYTES, ks, valid, lane, kTile);
+    if (valid > 0) consume_tile<D, NT, C::HALVES>(st, kbase, vbase, valid, ks, lane, a.scale_log2, kTile);
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(empty + s));
   }
@@ -580,8 +598,8 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 // paged K/V: persistent CTAs over (sequence, partition, KV head) items
 // =====================================================================================
 struct ItemDesc {
-  int b, g, p, kind;        // kind: 0 partition, 2 no more items
-  int n_tiles, n_parts, pad0, pad1;
+  int b, g, p, kind;        // g: first KV head of the item's group; kind: 0 partition, 2 no more items
+  int n_tiles, n_parts, n_boxes, pad1;
   int64_t key_begin, key_end;
 };
 static_assert(sizeof(ItemDesc) == 48, "descriptor slot size");
@@ -589,20 +607,30 @@ static_assert(sizeof(ItemDesc) == 48, "descriptor slot size");
 // Warps: consumers 0..CONSUMERS-1, TMA producer CONSUMERS, scheduler CONSUMERS+1,
 // epilogue CONSUMERS+2.
 //  * scheduler: takes item indices from the queue (one at a time), maps an index to
-//    (sequence, partition, KV head) through a prefix sum of the sequences' partition
-//    counts (so no index is empty), reads the partition's block ids and publishes a
-//    descriptor into a kItemSlots-deep ring -- running up to kItemSlots items ahead.
-//  * producer: for each descriptor, TMA-loads the partition's K/V blocks into the ring.
+//    (sequence, partition, group of HG KV heads) through a prefix sum of the
+//    sequences' partition counts (so no index is empty), reads the partition's block
+//    ids and publishes a descriptor into a kItemSlots-deep ring -- running up to
+//    kItemSlots items ahead.
+//  * producer: for each descriptor, TMA-loads the partition's K/V blocks into the ring,
+//    one box per block (or part of a block) holding the rows of all HG heads, so a box
+//    moves HG times the bytes of a single head's rows.
+//  * consumers: with HG heads, kWK/HG key-slice warps per head (tile = 16*kWK/HG keys);
+//    with HG = 4 every warp owns one head outright.
 //  * consumers: for each descriptor, the tile loop; at its end they leave their
 //    (O, m, l) in one of EPI_BUFS scratch buffers and go on with the next item.
 //  * epilogue: combines the consumer warps of a finished item and writes the f16
 //    output (one-partition sequences) or the partition's fp32 partial; the partials
 //    are folded by gqa_paged_merge_kernel (the second pass of paged attention v2).
-template <int D, int NT, int WN, int STAGES>
+template <int D, int NT, int WN, int STAGES, int HG>
 __global__ void __launch_bounds__(Cfg<D, NT, WN, STAGES>::PTHREADS)
 gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const DecodeArgs a) {
   using C = Cfg<D, NT, WN, STAGES>;
+  static_assert(HG == 1 || HG == 2 || HG == 4, "head group");
+  static_assert(HG == 1 || WN == 1, "head groups need a single query column");
+  constexpr int KS = kWK / HG;          // key-slice warps per head
+  constexpr int TK = 16 * KS;           // keys per tile
+  constexpr int BOXP = HG * C::HALVES;  // 64-column planes per box
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* scratch = reinterpret_cast<float*>(smem + C::PSCRATCH_OFF);
@@ -615,8 +643,8 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   volatile int* flags = reinterpret_cast<volatile int*>(sfree + C::EPI_BUFS);  // [0] abort
   ItemDesc* desc = reinterpret_cast<ItemDesc*>(const_cast<int*>(flags + 4));
   ItemDesc* edesc = desc + kItemSlots;                          // item of each scratch buffer
-  int* ids = reinterpret_cast<int*>(edesc + C::EPI_BUFS);          // [kItemSlots][kMaxPagedBlocksPerPart]
-  int* pre = ids + kItemSlots * kMaxPagedBlocksPerPart;         // [N + 1] partition-count prefix
+  int* boxy = reinterpret_cast<int*>(edesc + C::EPI_BUFS);      // [kItemSlots][kMaxBoxesPerPart] box rows
+  int* pre = boxy + kItemSlots * kMaxBoxesPerPart;              // [N + 1] partition-count prefix
   int* lens_s = pre + kPagedSeqs + 1;                           // [N] clamped lengths
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -672,7 +700,9 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     ptx::prefetch_tensormap(&tmV);
   }
   __syncthreads();
-  const int64_t total = (int64_t)pre[N] * a.h_kv;
+  const int groups = a.h_kv / HG;
+  const int64_t total = (int64_t)pre[N] * groups;
+  const int br = min(a.block_size, TK);  // rows per box
   // sequences without keys get zero output rows (spread over the CTAs)
   for (int b = blockIdx.x; b < N; b += gridDim.x) {
     if (lens_s[b] != 0) continue;
@@ -693,7 +723,7 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       const ItemDesc d = edesc[buf];
       if (d.kind == 2) break;
       const float* sb = reinterpret_cast<const float*>(smem + C::PSCRATCH_OFF + buf * C::PSCRATCH_STRIDE);
-      emit_slice<D, NT, WN, STAGES>(a, sb, d.b, d.g, d.p, d.n_parts == 1, lane, 32);
+      emit_slice<D, NT, WN, STAGES, HG>(a, sb, d.b, d.g, d.p, d.n_parts == 1, lane, 32);
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(sfree + buf));
     }
@@ -717,11 +747,11 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       }
       ItemDesc d;
       d.kind = 2;
-      d.b = d.g = d.p = d.n_tiles = d.n_parts = d.pad0 = d.pad1 = 0;
+      d.b = d.g = d.p = d.n_tiles = d.n_parts = d.n_boxes = d.pad1 = 0;
       d.key_begin = d.key_end = 0;
       if ((int64_t)it < total) {
-        d.g = (int)(it % (uint32_t)a.h_kv);
-        const int j = (int)(it / (uint32_t)a.h_kv);
+        d.g = (int)(it % (uint32_t)groups) * HG;
+        const int j = (int)(it / (uint32_t)groups);
         int lo = 0, hi = N;                        // pre[lo] <= j < pre[hi]
         while (hi - lo > 1) {
           const int mid = (lo + hi) >> 1;
@@ -733,17 +763,22 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         d.kind = 0;
         d.key_begin = (int64_t)d.p * P;
         d.key_end = min(d.key_begin + P, (int64_t)lens_s[lo]);
-        d.n_tiles = (int)((d.key_end - d.key_begin + kTile - 1) / kTile);
-        const int nb = (int)((d.key_end - d.key_begin + a.block_size - 1) / a.block_size);
-        const int32_t* row = a.block_tables + (int64_t)d.b * a.max_blocks_per_seq + d.key_begin / a.block_size;
-        int* dst = ids + slot * kMaxPagedBlocksPerPart;
-        for (int i = lane; i < nb; i += 32) {
-          int id = __ldg(row + i);
+        d.n_tiles = (int)((d.key_end - d.key_begin + TK - 1) / TK);
+        d.n_boxes = (int)((d.key_end - d.key_begin + br - 1) / br);
+        // pool row of every box of the partition (-1: block id outside the pool, not loaded),
+        // so that the producer thread only reads them
+        const int bs = a.block_size;
+        const int32_t* row = a.block_tables + (int64_t)d.b * a.max_blocks_per_seq + d.key_begin / bs;
+        int* dst = boxy + slot * kMaxBoxesPerPart;
+        for (int i = lane; i < d.n_boxes; i += 32) {
+          const int rel = i * br;                   // key offset in the partition (block aligned start)
+          const int blk = rel / bs;
+          int id = __ldg(row + blk);
           if (id < 0 || id >= a.num_blocks) {
             atomicOr(a.status, kDevBadInput);
             id = -1;
           }
-          dst[i] = id;
+          dst[i] = id < 0 ? -1 : id * bs + (rel - blk * bs);
         }
       }
       __threadfence_block();
@@ -762,8 +797,7 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     if (lane == 0) {
       const uint64_t pol = ptx::policy_evict_first();
       const bool stall = a.stall_cta >= 0 && a.stall_cta == (int)blockIdx.x;
-      const int bs = a.block_size;
-      const int nblk_tile = kTile / bs;
+      const int nbox = TK / br;   // boxes per tile
       int tile_it = 0, stall_tile = -1;
       bool gave_up = false;
       for (int k = 0;; ++k) {
@@ -777,7 +811,7 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         const ItemDesc d = desc[slot];
         if (d.kind == 2) break;
         if (stall && k == 0) stall_tile = tile_it + 1;     // test hook: this tile is never loaded
-        const int* bid = ids + slot * kMaxPagedBlocksPerPart;
+        const int* by = boxy + slot * kMaxBoxesPerPart;
         for (int t = 0; t < d.n_tiles; ++t, ++tile_it) {
           const int s = tile_it % STAGES;
           const uint32_t ph = (uint32_t)(tile_it / STAGES) & 1u;
@@ -791,19 +825,18 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
           const uint32_t kdst = ptx::smem_u32(smem + s * C::STAGE_BYTES);
           const uint32_t vdst = kdst + C::KV_BYTES;
           const uint32_t fb = ptx::smem_u32(full + s);
-          const int64_t k0 = d.key_begin + (int64_t)t * kTile;
-          const int first = t * nblk_tile;
+          // box j of tile t holds keys [(t*nbox + j)*br, +br) of the partition
+          const int b0 = t * nbox;
+          const int nb_t = min(nbox, d.n_boxes - b0);
           int n_load = 0;
-          for (int j = 0; j < nblk_tile; ++j)
-            if (k0 + (int64_t)j * bs < d.key_end && bid[first + j] >= 0) ++n_load;
-          ptx::mbar_arrive_expect_tx(fb, (uint32_t)(n_load * bs * 128 * 2 * C::HALVES));
-          for (int j = 0; j < nblk_tile; ++j) {
-            if (k0 + (int64_t)j * bs >= d.key_end) break;
-            const int id = bid[first + j];
-            if (id < 0) continue;
-            const uint32_t off = j * bs * 128 * C::HALVES;
-            ptx::tma_load_3d(kdst + off, &tmK, fb, 0, id * bs, d.g * C::HALVES, pol);
-            ptx::tma_load_3d(vdst + off, &tmV, fb, 0, id * bs, d.g * C::HALVES, pol);
+          for (int j = 0; j < nb_t; ++j) n_load += by[b0 + j] >= 0 ? 1 : 0;
+          ptx::mbar_arrive_expect_tx(fb, (uint32_t)(n_load * br * 128 * 2 * BOXP));
+          for (int j = 0; j < nb_t; ++j) {
+            const int y = by[b0 + j];
+            if (y < 0) continue;
+            const uint32_t off = j * br * 128 * BOXP;
+            ptx::tma_load_3d(kdst + off, &tmK, fb, 0, y, d.g * C::HALVES, pol);
+            ptx::tma_load_3d(vdst + off, &tmV, fb, 0, y, d.g * C::HALVES, pol);
           }
         }
         ptx::mbar_arrive(ptx::smem_u32(iempty + slot));
@@ -822,8 +855,10 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   }
 
   // ---------------------------------------------------------------- consumer warps
-  const int ks = warp % kWK;
-  const int nc = warp / kWK;
+  const int hh = HG > 1 ? warp / KS : 0;           // head within the item's group
+  const int ks = HG > 1 ? warp % KS : warp % kWK;  // key slice of every tile
+  const int nc = HG > 1 ? 0 : warp / kWK;          // query column
+  const int head_off = hh * C::HALVES * br * 128;  // first plane of this warp's head in a box
   WarpState<D, NT> st;
   int tile_it = 0, kc = 0;   // tiles consumed, items handed to the epilogue warp
   for (int k = 0;; ++k) {
@@ -838,7 +873,7 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(iempty + slot));
     bool aborted = false;
     if (d.kind != 2) {
-      load_q(st, a, d.b, d.g, nc, lane);
+      load_q(st, a, d.b, d.g + hh, nc, lane);
       reset_state(st);
       for (int t = 0; t < d.n_tiles; ++t, ++tile_it) {
         const int s = tile_it % STAGES;
@@ -849,13 +884,13 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
           aborted = true;
           break;
         }
-        const uint32_t kbase = ptx::smem_u32(smem + s * C::STAGE_BYTES);
+        const uint32_t kbase = ptx::smem_u32(smem + s * C::STAGE_BYTES) + head_off;
         const uint32_t vbase = kbase + C::KV_BYTES;
-        const int64_t key0 = d.key_begin + (int64_t)t * kTile + ks * 16;
+        const int64_t key0 = d.key_begin + (int64_t)t * TK + ks * 16;
         const int valid = (int)max((int64_t)0, min((int64_t)16, d.key_end - key0));
         if (valid < 16)
-          zero_masked_v<C::HALVES>(smem + s * C::STAGE_BYTES + C::KV_BYTES, ks, valid, lane, a.block_size);
-        if (valid > 0) consume_tile<D, NT>(st, kbase, vbase, valid, ks, lane, a.scale_log2, a.block_size);
+          zero_masked_v<C::HALVES, BOXP>(smem + s * C::STAGE_BYTES + C::KV_BYTES + head_off, ks, valid, lane, br);
+        if (valid > 0) consume_tile<D, NT, BOXP>(st, kbase, vbase, valid, ks, lane, a.scale_log2, br);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(empty + s));
       }
@@ -895,6 +930,48 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   }
 }
 
+// Fold n partials of output row r: m, l at [s * rows + r], O at [(s * rows + r) * D].
+// One warp: lane j reads the (m, l) of partials j, j+32, ...; the weights exp(m - M)
+// are broadcast with shuffles and each lane accumulates its D/32 output columns over
+// all partials, the loads of different partials independent of each other.
+template <int D>
+__device__ __forceinline__ void fold_row(const float* m, const float* l, const float* op, int n, int64_t rows,
+                                         int64_t r, int lane, float& M_out, float& L_out, float (&acc)[D / 32]) {
+  constexpr int PER = D / 32;
+  float M = -CUDART_INF_F;
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, m[(int64_t)s * rows + r]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  float L = 0.f;
+  if (M != -CUDART_INF_F) {
+    const float M2 = M * kLog2e;
+    for (int c = 0; c < n; c += 32) {
+      const int s = c + lane;
+      const float w = s < n ? ptx::ex2(m[(int64_t)s * rows + r] * kLog2e - M2) : 0.f;
+      L += s < n ? w * l[(int64_t)s * rows + r] : 0.f;
+      const int cnt = min(32, n - c);
+#pragma unroll 8
+      for (int j = 0; j < cnt; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, j);
+        const float* src = op + ((int64_t)(c + j) * rows + r) * D + lane * PER;
+        if constexpr (PER == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          acc[0] += wj * v.x; acc[1] += wj * v.y; acc[2] += wj * v.z; acc[3] += wj * v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          acc[0] += wj * v.x; acc[1] += wj * v.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  }
+  M_out = M;
+  L_out = L;
+}
+
 // Second pass of paged decode: for every output row of a sequence with more than one
 // partition, fold its partitions' partials (page: _merge_running left to right, then
 // O / l) into the f16 output.  One warp per row; rows of one-partition or empty
@@ -912,29 +989,8 @@ gqa_paged_merge_kernel(const DecodeArgs a) {
   len = len < 0 ? 0 : (len > cap ? cap : len);
   const int n = (len + a.partition_size - 1) / a.partition_size;
   if (n <= 1) return;
-  float M = -CUDART_INF_F;
-  for (int s = lane; s < n; s += 32) M = fmaxf(M, a.ws_m[(int64_t)s * a.R + r]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float acc[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-  float L = 0.f;
-  const float M2 = M * kLog2e;
-#pragma unroll 4
-  for (int s = 0; s < n; ++s) {
-    const int64_t pr = (int64_t)s * a.R + r;
-    const float w = ptx::ex2(a.ws_m[pr] * kLog2e - M2);
-    L += w * a.ws_l[pr];
-    const float* src = a.ws_o + pr * D + lane * PER;
-    if constexpr (PER == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(src);
-      acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(src);
-      acc[0] += w * v.x; acc[1] += w * v.y;
-    }
-  }
+  float M, L, acc[PER];
+  fold_row<D>(a.ws_m, a.ws_l, a.ws_o, n, a.R, r, lane, M, L, acc);
   const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
   for (int i = 0; i < PER; ++i) a.o[r * D + lane * PER + i] = __float2half_rn(acc[i] * inv);
@@ -950,31 +1006,8 @@ gqa_merge_kernel(const float* __restrict__ m, const float* __restrict__ l, const
   const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
-  float M = -CUDART_INF_F;
-  for (int s = lane; s < n_parts; s += 32) M = fmaxf(M, m[(int64_t)s * rows + r]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float acc[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-  float L = 0.f;
-  if (M != -CUDART_INF_F) {
-    const float M2 = M * kLog2e;
-#pragma unroll 4
-    for (int s = 0; s < n_parts; ++s) {
-      const int64_t pr = (int64_t)s * rows + r;
-      const float w = ptx::ex2(m[pr] * kLog2e - M2);
-      L += w * l[pr];
-      const float* src = op + pr * D + lane * PER;
-      if constexpr (PER == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] += w * v.x; acc[1] += w * v.y;
-      }
-    }
-  }
+  float M, L, acc[PER];
+  fold_row<D>(m, l, op, n_parts, rows, r, lane, M, L, acc);
   if (o != nullptr) {
     const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll

@@ -1,6 +1,6 @@
-// Instances of the split-KV decode kernel: d_head = 128, paged = true.
+// Instances of the split-KV decode kernels: paged, d_head = 128.
 #include "gqa_instances.cuh"
 
 namespace gqa {
-GQA_DEFINE_UNIT(paged_d128, 128, true)
+GQA_DEFINE_PAGED_UNIT(paged_d128, 128)
 }  // namespace gqa

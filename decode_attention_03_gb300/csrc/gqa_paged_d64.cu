@@ -1,6 +1,6 @@
-// Instances of the split-KV decode kernel: d_head = 64, paged = true.
+// Instances of the split-KV decode kernels: paged, d_head = 64.
 #include "gqa_instances.cuh"
 
 namespace gqa {
-GQA_DEFINE_UNIT(paged_d64, 64, true)
+GQA_DEFINE_PAGED_UNIT(paged_d64, 64)
 }  // namespace gqa

@@ -62,9 +62,11 @@ typedef struct {
                             producer never loads its second tile, so that the waits on it run out.
                             Use with a small timeout_us; the call then reports GQA_ERR_TIMEOUT
                             through gqa_workspace_check and the workspace must be re-initialised. */
+  int paged_head_group;  /* paged calls: KV heads per work item and per TMA box, 1, 2 or 4 (must divide
+                            h_kv; 2 and 4 need h_q / h_kv <= 16); 0 = 4, 2 or 1, the largest that fits */
 } gqa_options;
 
-/* Default options: n_splits 0, merge_mode 0, timeout_us 0, test_stall_cta -1. */
+/* Default options: n_splits 0, merge_mode 0, timeout_us 0, test_stall_cta -1, paged_head_group 0. */
 gqa_options gqa_default_options(void);
 
 /* Static text for a status code. */
@@ -152,7 +154,7 @@ gqa_status gqa_merge_partial(const float* m, const float* l, const float* o_part
  *                 a length-0 sequence gets O = 0
  *   o             (num_seqs, h_q*d_head) f16, written
  * block_size in {8, 16, 32, 64}; partition_size a multiple of 64 with
- * partition_size / block_size <= 256; max_seq_len (host-known bound on seq_lens) sizes the grid.
+ * partition_size / min(block_size, 16) <= 256; max_seq_len (host-known bound on seq_lens) sizes the grid.
  * Block ids outside [0, num_blocks) are not loaded and are reported by gqa_workspace_check. */
 gqa_status gqa_decode_paged(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
                             const int32_t* block_tables, const int32_t* seq_lens, uint16_t* o,

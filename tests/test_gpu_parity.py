@@ -109,17 +109,18 @@ def ref_paged(p, seqs=None):
                                p["h_kv"], p["d_head"], p["scale"], p["block_size"], seqs=seqs)
 
 
-def test_workload_paged(gqa):
+@pytest.mark.parametrize("hg", [0, 1, 2])
+def test_workload_paged(gqa, hg):
     w = gi.WORKLOADS["paged"]
     p = gi.make_paged(w)
-    o = run_paged(gqa, p)
+    o = run_paged(gqa, p, head_group=hg)
     lens = p["seq_lens"]
     seqs = sorted(set([int(np.argmin(lens)), int(np.argmax(lens))] + list(range(0, 64, 6))))
     ref = ref_paged(p, seqs)
     assert_close(o, ref.reshape(64, -1), "paged (sampled sequences)")
     # unused tail slots of every last block filled with NaN: identical output, bit for bit
     pn = gi.make_paged(w, tail_fill="nan")
-    o2 = run_paged(gqa, pn)
+    o2 = run_paged(gqa, pn, head_group=hg)
     assert torch.equal(o, o2)
 
 
@@ -241,9 +242,11 @@ def test_chain_reduce_equals_full(gqa):
 
 # ---------------------------------------------------------------- paged edges
 @pytest.mark.parametrize("bs,part", [(16, 512), (8, 64), (32, 128), (64, 512), (16, 64)])
-def test_paged_edges(gqa, bs, part):
+@pytest.mark.parametrize("hq,hkv,hg,D", [(8, 2, 1, 128), (8, 2, 2, 128), (32, 8, 4, 128), (16, 4, 4, 64),
+                                         (32, 8, 2, 64), (64, 4, 1, 128)])
+def test_paged_edges(gqa, bs, part, hq, hkv, hg, D):
     lens = np.array([0, 1, 15, 16, 17, 511, 512, 513, 1000, 64], dtype=np.int32)
-    N, hq, hkv, D = len(lens), 8, 2, 128
+    N = len(lens)
     nblk = (lens + bs - 1) // bs
     num_blocks = int(nblk.sum()) + 3
     perm = np.random.Generator(np.random.PCG64(bs + part)).permutation(num_blocks).astype(np.int32)
@@ -258,11 +261,11 @@ def test_paged_edges(gqa, bs, part):
     vp = gi.normal_f16(900 + bs, 2, (num_blocks, bs, hkv * D))
     p = dict(q=q, k_pool=kp, v_pool=vp, block_tables=tab, seq_lens=lens, num_seqs=N, h_q=hq, h_kv=hkv,
              d_head=D, scale=1 / math.sqrt(D), block_size=bs, partition_size=part, max_seq_len=int(lens.max()))
-    o = run_paged(gqa, p)
+    o = run_paged(gqa, p, head_group=hg)
     ref = ref_paged(p)
     assert (o[0].float() == 0).all()                         # empty sequence -> zeros
     ref[0] = 0.0
-    assert_close(o, ref.reshape(N, -1), f"paged bs={bs} part={part}")
+    assert_close(o, ref.reshape(N, -1), f"paged bs={bs} part={part} hq={hq} hkv={hkv} hg={hg} D={D}")
 
 
 def test_paged_bad_block_is_reported(gqa):
