@@ -400,16 +400,26 @@ def main():
         raise RuntimeError(f"device status word set in the timed region: {status}")
     l2_hot = None
     if flush is not None:
-        # small workloads also report back-to-back steps with the inputs resident in L2
-        h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # small workloads also report back-to-back steps with the inputs resident in L2,
+        # replayed from a CUDA graph so that host submission does not pace the GPU
+        n_graph = 50
+        graph = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                for _ in range(n_graph):
+                    step()
+            graph.replay()
+            torch.cuda.synchronize()
+            h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = max(1, steps // n_graph)
             h0.record(stream)
-            for _ in range(steps):
-                step()
+            for _ in range(reps):
+                graph.replay()
             h1.record(stream)
         torch.cuda.synchronize()
-        hot_ms = h0.elapsed_time(h1) / steps
-        l2_hot = {"us_per_step": round(hot_ms * 1e3, 3), "GB/s": round(bytes_step / (hot_ms * 1e-3) / 1e9, 2)}
+        hot_ms = h0.elapsed_time(h1) / (reps * n_graph)
+        l2_hot = {"us_per_step": round(hot_ms * 1e3, 3), "GB/s": round(bytes_step / (hot_ms * 1e-3) / 1e9, 2),
+                  "how": f"CUDA graph of {n_graph} back-to-back steps, inputs L2-resident"}
     t_max = max_over_ranks(t_ms)
     ms_step = t_max / steps
     value = job_throughput(bytes_step, steps, world, t_max)

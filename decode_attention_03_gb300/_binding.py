@@ -37,7 +37,7 @@ class GQAError(RuntimeError):
 class gqa_options(ctypes.Structure):
     _fields_ = [("n_splits", ctypes.c_int), ("merge_mode", ctypes.c_int),
                 ("timeout_us", ctypes.c_uint32), ("test_stall_cta", ctypes.c_int),
-                ("paged_head_group", ctypes.c_int)]
+                ("paged_head_group", ctypes.c_int), ("causal", ctypes.c_int)]
 
 
 def _load():
@@ -114,11 +114,12 @@ def _f32(t: torch.Tensor, name: str) -> None:
         raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
 
 
-def _opts(n_splits=0, merge_mode=0, timeout_us=0, test_stall_cta=-1, paged_head_group=0):
+def _opts(n_splits=0, merge_mode=0, timeout_us=0, test_stall_cta=-1, paged_head_group=0, causal=False):
     o = gqa_options()
     o.n_splits, o.merge_mode, o.timeout_us, o.test_stall_cta = int(n_splits), int(merge_mode), int(timeout_us), \
         int(test_stall_cta)
     o.paged_head_group = int(paged_head_group)
+    o.causal = 1 if causal else 0
     return o
 
 
@@ -178,8 +179,10 @@ def _shape_qkv(q, k, v, h_q, h_kv):
 def gqa_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, h_q: int, h_kv: int,
                scale: Optional[float] = None, *, out: Optional[torch.Tensor] = None,
                workspace_tensor: Optional[torch.Tensor] = None, stream=None, n_splits: int = 0,
-               merge_mode: int = 0, timeout_us: int = 0, test_stall_cta: int = -1) -> torch.Tensor:
-    """O = softmax(scale Q K^T) V for GQA decode; q (B, T_q, h_q*D), k/v (B, S_kv, h_kv*D) f16."""
+               merge_mode: int = 0, timeout_us: int = 0, test_stall_cta: int = -1,
+               causal: bool = False) -> torch.Tensor:
+    """O = softmax(scale Q K^T) V for GQA decode; q (B, T_q, h_q*D), k/v (B, S_kv, h_kv*D) f16.
+    ``causal``: query token t sees keys j <= S_kv - T_q + t only."""
     B, T_q, S, D = _shape_qkv(q, k, v, h_q, h_kv)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if out is None:
@@ -189,7 +192,7 @@ def gqa_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, h_q: int, h_kv
     if nbytes == 0:
         raise GQAError(GQA_ERR_INVALID_ARG, "gqa_decode_workspace_size")
     ws = workspace(nbytes, q.device, stream) if workspace_tensor is None else workspace_tensor
-    opt = _opts(n_splits, merge_mode, timeout_us, test_stall_cta)
+    opt = _opts(n_splits, merge_mode, timeout_us, test_stall_cta, causal=causal)
     st = lib.gqa_decode_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T_q, S, h_q, h_kv, D, scale,
                            _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(opt))
     _check(st, "gqa_decode")
@@ -198,7 +201,7 @@ def gqa_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, h_q: int, h_kv
 
 def gqa_decode_partial(q, k, v, h_q: int, h_kv: int, s_begin: int, s_len: int, scale: Optional[float] = None, *,
                        m=None, l=None, o_part=None, workspace_tensor=None, stream=None, n_splits: int = 0,
-                       merge_mode: int = 0) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+                       merge_mode: int = 0, causal: bool = False) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Partial (m, l, O) over keys [s_begin, s_begin+s_len): m, l (B*T_q*h_q) and O (B*T_q*h_q, D) fp32."""
     B, T_q, S, D = _shape_qkv(q, k, v, h_q, h_kv)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
@@ -212,7 +215,7 @@ def gqa_decode_partial(q, k, v, h_q: int, h_kv: int, s_begin: int, s_len: int, s
     if nbytes == 0:
         raise GQAError(GQA_ERR_INVALID_ARG, "gqa_decode_workspace_size")
     ws = workspace(nbytes, dev, stream) if workspace_tensor is None else workspace_tensor
-    opt = _opts(n_splits, merge_mode)
+    opt = _opts(n_splits, merge_mode, causal=causal)
     st = lib.gqa_decode_partial_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(m), _ptr(l), _ptr(o_part), B, T_q, S,
                                    int(s_begin), int(s_len), h_q, h_kv, D, scale, _ptr(ws), ws.numel(),
                                    _stream(stream), ctypes.byref(opt))

@@ -39,8 +39,8 @@ bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 struct DevState {
   bool ready = false;
   int sms = 0;
-  int occ[2][4][4] = {};       // [d index][row class][0 contiguous, 1/2/3 paged with head group 1/2/4]
-                               // resident CTAs per SM, 0 = not prepared
+  int occ[2][4][5] = {};       // [d index][row class][kernel: see kernel_slot] resident CTAs per SM,
+                               // 0 = not prepared
 };
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
@@ -50,23 +50,25 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
-// hg = 0: contiguous kernel; hg in {1, 2, 4}: paged kernel with that head group
-cudaError_t prepare_unit(int di, int cls, int hg, int* occ) {
-  if (hg == 0) return di == 0 ? contig_d64_prepare(cls, 1, occ) : contig_d128_prepare(cls, 1, occ);
-  return di == 0 ? paged_d64_prepare(cls, hg, occ) : paged_d128_prepare(cls, hg, occ);
+// Kernel selector `kind`: 0 contiguous, 1 contiguous with the causal tail, and for the paged
+// kernel 100 + its head group (101, 102, 104).
+cudaError_t prepare_unit(int di, int cls, int kind, int* occ) {
+  if (kind < 100) return di == 0 ? contig_d64_prepare(cls, kind, occ) : contig_d128_prepare(cls, kind, occ);
+  return di == 0 ? paged_d64_prepare(cls, kind - 100, occ) : paged_d128_prepare(cls, kind - 100, occ);
 }
 
-cudaError_t launch_unit(int di, int cls, int hg, dim3 grid, cudaStream_t st, const CUtensorMap& tk,
+cudaError_t launch_unit(int di, int cls, int kind, dim3 grid, cudaStream_t st, const CUtensorMap& tk,
                         const CUtensorMap& tv, const DecodeArgs& a) {
-  if (hg == 0)
-    return di == 0 ? contig_d64_launch(cls, 1, grid, st, tk, tv, a) : contig_d128_launch(cls, 1, grid, st, tk, tv, a);
-  return di == 0 ? paged_d64_launch(cls, hg, grid, st, tk, tv, a) : paged_d128_launch(cls, hg, grid, st, tk, tv, a);
+  if (kind < 100)
+    return di == 0 ? contig_d64_launch(cls, kind, grid, st, tk, tv, a) : contig_d128_launch(cls, kind, grid, st, tk, tv, a);
+  return di == 0 ? paged_d64_launch(cls, kind - 100, grid, st, tk, tv, a)
+                 : paged_d128_launch(cls, kind - 100, grid, st, tk, tv, a);
 }
 
-int hg_slot(int hg) { return hg == 0 ? 0 : (hg == 1 ? 1 : (hg == 2 ? 2 : 3)); }
+int kernel_slot(int kind) { return kind < 100 ? kind : (kind == 101 ? 2 : (kind == 102 ? 3 : 4)); }
 
 // SM count and resident CTAs per SM of one kernel configuration on the current device
-gqa_status device_info(int di, int cls, int hg, int* sms, int* occ) {
+gqa_status device_info(int di, int cls, int kind, int* sms, int* occ) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -84,10 +86,10 @@ gqa_status device_info(int di, int cls, int hg, int* sms, int* occ) {
     }
     st.ready = true;
   }
-  int& o = st.occ[di][cls][hg_slot(hg)];
+  int& o = st.occ[di][cls][kernel_slot(kind)];
   if (o == 0) {
     int v = 0;
-    if (prepare_unit(di, cls, hg, &v) != cudaSuccess || v <= 0) return GQA_ERR_CUDA;
+    if (prepare_unit(di, cls, kind, &v) != cudaSuccess || v <= 0) return GQA_ERR_CUDA;
     o = v;
   }
   *sms = st.sms;
@@ -160,6 +162,7 @@ gqa_options defaults() {
   o.timeout_us = 0;
   o.test_stall_cta = -1;
   o.paged_head_group = 0;
+  o.causal = 0;
   return o;
 }
 
@@ -238,7 +241,8 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
   if (s != GQA_OK) return s;
   if (ws_bytes < p.lay.total) return GQA_ERR_WORKSPACE;
   int sms = 0, occ = 0;
-  s = device_info(p.di, p.cls, 0, &sms, &occ);
+  const int kind = opt.causal ? 1 : 0;
+  s = device_info(p.di, p.cls, kind, &sms, &occ);
   if (s != GQA_OK) return s;
 
   CUtensorMap tk, tv;
@@ -273,13 +277,14 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
   a.s_len = s_len;
   a.n_splits = p.n_splits;
   a.merge_in_kernel = opt.merge_mode == 0 ? 1 : 0;
+  a.causal = opt.causal ? 1 : 0;
   a.scale_log2 = scale * kLog2e;
   a.timeout_ns = opt.timeout_us ? (uint64_t)opt.timeout_us * 1000ull : kDefaultTimeoutNs;
   a.stall_cta = opt.test_stall_cta;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   dim3 grid((unsigned)h_kv, (unsigned)p.n_splits, (unsigned)B);
-  if (launch_unit(p.di, p.cls, 0, grid, st, tk, tv, a) != cudaSuccess) return GQA_ERR_CUDA;
+  if (launch_unit(p.di, p.cls, kind, grid, st, tk, tv, a) != cudaSuccess) return GQA_ERR_CUDA;
   if (p.n_splits > 1 && !a.merge_in_kernel) {
     return merge_launch(a.ws_m, a.ws_l, a.ws_o, p.n_splits, p.R, D, a.o, a.m_out, a.l_out, a.o_part_out, st);
   }
@@ -339,7 +344,7 @@ gqa_status paged_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t*
   if (hg == 0) hg = p.cls <= 1 ? (h_kv % 4 == 0 ? 4 : (h_kv % 2 == 0 ? 2 : 1)) : 1;
   if (!(hg == 1 || hg == 2 || hg == 4) || h_kv % hg != 0 || (hg > 1 && p.cls > 1)) return GQA_ERR_INVALID_ARG;
   int sms = 0, occ = 0;
-  s = device_info(p.di, p.cls, hg, &sms, &occ);
+  s = device_info(p.di, p.cls, 100 + hg, &sms, &occ);
   if (s != GQA_OK) return s;
 
   CUtensorMap tk, tv;
@@ -389,7 +394,7 @@ gqa_status paged_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t*
     a.R = (int64_t)n * h_q;
     a.total_items = (int64_t)n * p.max_parts * (h_kv / hg);   // upper bound; the kernel counts the real ones
     const int64_t ctas = std::min<int64_t>((int64_t)sms * occ, a.total_items);
-    if (launch_unit(p.di, p.cls, hg, dim3((unsigned)ctas, 1, 1), st, tk, tv, a) != cudaSuccess)
+    if (launch_unit(p.di, p.cls, 100 + hg, dim3((unsigned)ctas, 1, 1), st, tk, tv, a) != cudaSuccess)
       return GQA_ERR_CUDA;
     if (p.max_parts > 1) {
       // second pass: fold the partitions of every multi-partition sequence

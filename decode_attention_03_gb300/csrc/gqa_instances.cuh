@@ -34,7 +34,7 @@ constexpr int paged_stages_for() {
   return n < 2 ? 2 : (n > 8 ? 8 : n);
 }
 
-template <int D, int CLS>
+template <int D, int CLS, bool CAUSAL>
 struct Inst {
   static constexpr int NT = cls_nt(CLS);
   static constexpr int WN = cls_wn(CLS);
@@ -43,14 +43,14 @@ struct Inst {
   static_assert(C::SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
   static cudaError_t prepare(int* occupancy) {
-    auto fn = gqa_split_kernel<D, NT, WN, STAGES>;
+    auto fn = gqa_split_kernel<D, NT, WN, STAGES, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, fn, C::THREADS, C::SMEM_BYTES);
   }
   static cudaError_t launch(dim3 grid, cudaStream_t st, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a) {
-    gqa_split_kernel<D, NT, WN, STAGES><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tk, tv, a);
+    gqa_split_kernel<D, NT, WN, STAGES, CAUSAL><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tk, tv, a);
     return cudaGetLastError();
   }
 };
@@ -76,50 +76,45 @@ struct PagedInst {
   }
 };
 
-// Contiguous units: cls in [0, 4).  Paged units: cls in [0, 4) and head group hg in
-// {1, 2, 4} (hg > 1 only for cls 0 and 1).
+// Contiguous units: cls in [0, 4), variant = causal (0 / 1).  Paged units: cls in [0, 4),
+// variant = head group in {1, 2, 4} (2 and 4 only for cls 0 and 1).
 #define GQA_DECLARE_UNIT(NAME)                                                                   \
-  cudaError_t NAME##_prepare(int cls, int hg, int* occupancy);                                   \
-  cudaError_t NAME##_launch(int cls, int hg, dim3 grid, cudaStream_t st, const CUtensorMap& tk,  \
+  cudaError_t NAME##_prepare(int cls, int variant, int* occupancy);                              \
+  cudaError_t NAME##_launch(int cls, int variant, dim3 grid, cudaStream_t st, const CUtensorMap& tk, \
                             const CUtensorMap& tv, const DecodeArgs& a);
 
+#define GQA_CONTIG_CASES(D, CALL)                                                                \
+  if (cls == 0) return variant ? Inst<D, 0, true>::CALL : Inst<D, 0, false>::CALL;               \
+  if (cls == 1) return variant ? Inst<D, 1, true>::CALL : Inst<D, 1, false>::CALL;               \
+  if (cls == 2) return variant ? Inst<D, 2, true>::CALL : Inst<D, 2, false>::CALL;               \
+  if (cls == 3) return variant ? Inst<D, 3, true>::CALL : Inst<D, 3, false>::CALL;               \
+  return cudaErrorInvalidValue;
+
 #define GQA_DEFINE_CONTIG_UNIT(NAME, D)                                                          \
-  cudaError_t NAME##_prepare(int cls, int, int* occupancy) {                                     \
-    switch (cls) {                                                                               \
-      case 0: return Inst<D, 0>::prepare(occupancy);                                             \
-      case 1: return Inst<D, 1>::prepare(occupancy);                                             \
-      case 2: return Inst<D, 2>::prepare(occupancy);                                             \
-      case 3: return Inst<D, 3>::prepare(occupancy);                                             \
-    }                                                                                            \
-    return cudaErrorInvalidValue;                                                                \
+  cudaError_t NAME##_prepare(int cls, int variant, int* occupancy) {                             \
+    GQA_CONTIG_CASES(D, prepare(occupancy))                                                      \
   }                                                                                              \
-  cudaError_t NAME##_launch(int cls, int, dim3 grid, cudaStream_t st, const CUtensorMap& tk,     \
+  cudaError_t NAME##_launch(int cls, int variant, dim3 grid, cudaStream_t st, const CUtensorMap& tk, \
                             const CUtensorMap& tv, const DecodeArgs& a) {                        \
-    switch (cls) {                                                                               \
-      case 0: return Inst<D, 0>::launch(grid, st, tk, tv, a);                                    \
-      case 1: return Inst<D, 1>::launch(grid, st, tk, tv, a);                                    \
-      case 2: return Inst<D, 2>::launch(grid, st, tk, tv, a);                                    \
-      case 3: return Inst<D, 3>::launch(grid, st, tk, tv, a);                                    \
-    }                                                                                            \
-    return cudaErrorInvalidValue;                                                                \
+    GQA_CONTIG_CASES(D, launch(grid, st, tk, tv, a))                                             \
   }
 
 #define GQA_PAGED_CASES(D, CALL)                                                                 \
-  if (cls == 0 && hg == 1) return PagedInst<D, 0, 1>::CALL;                                      \
-  if (cls == 0 && hg == 2) return PagedInst<D, 0, 2>::CALL;                                      \
-  if (cls == 0 && hg == 4) return PagedInst<D, 0, 4>::CALL;                                      \
-  if (cls == 1 && hg == 1) return PagedInst<D, 1, 1>::CALL;                                      \
-  if (cls == 1 && hg == 2) return PagedInst<D, 1, 2>::CALL;                                      \
-  if (cls == 1 && hg == 4) return PagedInst<D, 1, 4>::CALL;                                      \
-  if (cls == 2 && hg == 1) return PagedInst<D, 2, 1>::CALL;                                      \
-  if (cls == 3 && hg == 1) return PagedInst<D, 3, 1>::CALL;                                      \
+  if (cls == 0 && variant == 1) return PagedInst<D, 0, 1>::CALL;                                 \
+  if (cls == 0 && variant == 2) return PagedInst<D, 0, 2>::CALL;                                 \
+  if (cls == 0 && variant == 4) return PagedInst<D, 0, 4>::CALL;                                 \
+  if (cls == 1 && variant == 1) return PagedInst<D, 1, 1>::CALL;                                 \
+  if (cls == 1 && variant == 2) return PagedInst<D, 1, 2>::CALL;                                 \
+  if (cls == 1 && variant == 4) return PagedInst<D, 1, 4>::CALL;                                 \
+  if (cls == 2 && variant == 1) return PagedInst<D, 2, 1>::CALL;                                 \
+  if (cls == 3 && variant == 1) return PagedInst<D, 3, 1>::CALL;                                 \
   return cudaErrorInvalidValue;
 
 #define GQA_DEFINE_PAGED_UNIT(NAME, D)                                                           \
-  cudaError_t NAME##_prepare(int cls, int hg, int* occupancy) {                                  \
+  cudaError_t NAME##_prepare(int cls, int variant, int* occupancy) {                             \
     GQA_PAGED_CASES(D, prepare(occupancy))                                                       \
   }                                                                                              \
-  cudaError_t NAME##_launch(int cls, int hg, dim3 grid, cudaStream_t st, const CUtensorMap& tk,  \
+  cudaError_t NAME##_launch(int cls, int variant, dim3 grid, cudaStream_t st, const CUtensorMap& tk, \
                             const CUtensorMap& tv, const DecodeArgs& a) {                        \
     GQA_PAGED_CASES(D, launch(grid, st, tk, tv, a))                                              \
   }

@@ -23,7 +23,8 @@
 //    running (m, l, O) over its keys; the warps' states are merged through shared
 //    memory at the end of the slice.
 //
-// gqa_split_kernel: one CTA per (KV head, split, sequence) of a contiguous K/V.
+// gqa_split_kernel: one CTA per (KV head, split, sequence) of a contiguous K/V (CAUSAL:
+//   the speculative-verification tail mask, a separate instantiation).
 // gqa_paged_kernel: persistent, one CTA per SM; a scheduler warp takes
 //   (sequence, partition, KV head) items from an atomic queue and reads the
 //   partition's block ids ahead of time, the producer warp streams the items'
@@ -77,9 +78,11 @@ struct DecodeArgs {
   int64_t s_begin, s_len;           // contiguous: key range swept
   int n_splits;                     // contiguous: splits per unit; paged: max partitions per sequence
   int merge_in_kernel;              // last CTA of a unit merges the splits
+  int causal;                       // query token t sees keys j <= S_kv - T_q + t only
   float scale_log2;                 // scale * log2(e)
   uint64_t timeout_ns;
-  int stall_cta;                    // test hook: CTA whose producer withholds a tile (-1 none)
+  int stall_cta;                    // test hook (-1 none): contiguous, the CTA whose producer withholds
+                                    // its second tile; paged, the queue item whose second tile is withheld
 };
 
 template <int D, int NT, int WN, int STAGES>
@@ -150,12 +153,21 @@ struct WarpState {
   float acc[KD][NT][4];               // O^T accumulators (rows d, columns query rows)
   float m_run[NT][2];                 // running max (log2 domain), query rows 2*tq4, 2*tq4+1
   float l_run[NT][2];                 // running sum over this lane's keys
+  int lim[NT][2];                     // last key index those rows may see (causal tail), else INT_MAX
 };
 
 // Q^T fragments: b0 = Q[row gq][16kk + 2tq4 ..+1], b1 = the same 8 columns further
 template <int D, int NT>
 __device__ __forceinline__ void load_q(WarpState<D, NT>& st, const DecodeArgs& a, int b, int g, int nc, int lane) {
   const int gq = lane >> 2, tq4 = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      // rows of the score fragment held by this lane: 2*tq4 + j of n-tile nt (token r / G)
+      const int r = (nc * NT + nt) * 8 + 2 * tq4 + j;
+      st.lim[nt][j] = a.causal ? (int)(a.S_kv - a.T_q + r / a.G) : 0x7fffffff;
+    }
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int r = (nc * NT + nt) * 8 + gq;
@@ -207,9 +219,9 @@ __device__ __forceinline__ void zero_masked_v(uint8_t* vhead, int ks, int valid,
 
 // One tile: this warp's 16 keys against its 8*NT query rows; kbase / vbase point at
 // the first plane of the warp's head.
-template <int D, int NT, int BOXP>
+template <int D, int NT, int BOXP, bool CAUSAL = false>
 __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbase, uint32_t vbase, int valid,
-                                             int ks, int lane, float scale_log2, int rb) {
+                                             int key0, int ks, int lane, float scale_log2, int rb) {
   constexpr int KD = WarpState<D, NT>::KD;
   const int gq = lane >> 2;
   const int k_row = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -235,10 +247,21 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbas
   float alpha[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
+    if constexpr (CAUSAL) {
+      // last key of the slice each of this lane's two rows may see (range end, causal tail)
+      const int last0 = min(valid - 1, st.lim[nt][0] - key0);
+      const int last1 = min(valid - 1, st.lim[nt][1] - key0);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int key = gq + ((c >> 1) << 3);
-      sc[nt][c] = key < valid ? sc[nt][c] * scale_log2 : -CUDART_INF_F;
+      for (int c = 0; c < 4; ++c) {
+        const int key = gq + ((c >> 1) << 3);
+        sc[nt][c] = key <= ((c & 1) ? last1 : last0) ? sc[nt][c] * scale_log2 : -CUDART_INF_F;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int key = gq + ((c >> 1) << 3);
+        sc[nt][c] = key < valid ? sc[nt][c] * scale_log2 : -CUDART_INF_F;
+      }
     }
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -259,7 +282,7 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbas
   }
   // ---- rescale O^T (rows d, columns = query rows 2*tq4, 2*tq4+1); skipped when no
   //      running max of the warp moved (alpha = 1 everywhere), the common case once the
-  //      first tiles have been seen
+  //      first tiles have been seen (G*T_q = 32: 94.5 -> 92.9 us; no change at G*T_q = 4)
   bool moved = false;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) moved |= (alpha[nt][0] != 1.f) | (alpha[nt][1] != 1.f);
@@ -409,8 +432,8 @@ __device__ __forceinline__ bool last_to_arrive(const DecodeArgs& a, int unit, in
 
 // Fold the n partials of unit (b, g) (page: _merge_running applied left to right) and
 // write the output (O / l) or the merged partial; resets the unit's counter.  Each
-// thread folds IPT items (4 consecutive d of one row) at once, so all loads of one
-// partial step are in flight together.
+// thread folds IPT items (4 consecutive d of one row) over chunks of partials whose
+// loads are all issued before the folds.
 template <int D, int NT, int WN, int STAGES>
 __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int g, int unit, int n) {
   using C = Cfg<D, NT, WN, STAGES>;
@@ -431,28 +454,38 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int g, in
     L[i] = 0.f;
     O[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-#pragma unroll 2
-  for (int s2 = 0; s2 < n; ++s2) {
-    float ms[IPT], ls[IPT];
-    float4 os[IPT];
+  // chunks of UNR partials: all UNR x IPT loads are issued before any is used, about 16
+  // float4 loads in flight per thread
+  constexpr int UNR = IPT >= 4 ? 4 : 16 / IPT;
+  for (int s0 = 0; s0 < n; s0 += UNR) {
+    float ms[UNR][IPT], ls[UNR][IPT];
+    float4 os[UNR][IPT];
 #pragma unroll
-    for (int i = 0; i < IPT; ++i) {
-      const int64_t prow = (int64_t)s2 * a.R + orow_i[i];
-      ms[i] = __ldcg(a.ws_m + prow) * kLog2e;
-      ls[i] = __ldcg(a.ws_l + prow);
-      os[i] = __ldcg(reinterpret_cast<const float4*>(a.ws_o + prow * D) + c4_i[i]);
+    for (int u = 0; u < UNR; ++u) {
+      const bool have = s0 + u < n;
+#pragma unroll
+      for (int i = 0; i < IPT; ++i) {
+        const int64_t prow = (int64_t)(have ? s0 + u : 0) * a.R + orow_i[i];
+        ms[u][i] = have ? __ldcg(a.ws_m + prow) * kLog2e : -CUDART_INF_F;
+        ls[u][i] = have ? __ldcg(a.ws_l + prow) : 0.f;
+        os[u][i] = have ? __ldcg(reinterpret_cast<const float4*>(a.ws_o + prow * D) + c4_i[i])
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
 #pragma unroll
-    for (int i = 0; i < IPT; ++i) {
-      const float m_new = fmaxf(M[i], ms[i]);
-      const float ref = m_new == -CUDART_INF_F ? 0.f : m_new;   // both sides empty so far
-      const float so = ptx::ex2(M[i] - ref), sn = ptx::ex2(ms[i] - ref);
-      L[i] = L[i] * so + ls[i] * sn;
-      O[i].x = O[i].x * so + os[i].x * sn;
-      O[i].y = O[i].y * so + os[i].y * sn;
-      O[i].z = O[i].z * so + os[i].z * sn;
-      O[i].w = O[i].w * so + os[i].w * sn;
-      M[i] = m_new;
+    for (int u = 0; u < UNR; ++u) {
+#pragma unroll
+      for (int i = 0; i < IPT; ++i) {
+        const float m_new = fmaxf(M[i], ms[u][i]);
+        const float ref = m_new == -CUDART_INF_F ? 0.f : m_new;   // both sides empty so far
+        const float so = ptx::ex2(M[i] - ref), sn = ptx::ex2(ms[u][i] - ref);
+        L[i] = L[i] * so + ls[u][i] * sn;
+        O[i].x = O[i].x * so + os[u][i].x * sn;
+        O[i].y = O[i].y * so + os[u][i].y * sn;
+        O[i].z = O[i].z * so + os[u][i].z * sn;
+        O[i].w = O[i].w * so + os[u][i].w * sn;
+        M[i] = m_new;
+      }
     }
   }
 #pragma unroll
@@ -478,7 +511,7 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int g, in
 // =====================================================================================
 // contiguous K/V: one CTA per (KV head, split, sequence)
 // =====================================================================================
-template <int D, int NT, int WN, int STAGES>
+template <int D, int NT, int WN, int STAGES, bool CAUSAL>
 __global__ void __launch_bounds__(Cfg<D, NT, WN, STAGES>::THREADS)
 gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const DecodeArgs a) {
@@ -577,7 +610,8 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     const int valid = (int)max((int64_t)0, min((int64_t)16, key_end - key0));
     if (valid < 16)
       zero_masked_v<C::HALVES, C::HALVES>(smem + s * C::STAGE_BYTES + C::KV_BYTES, ks, valid, lane, kTile);
-    if (valid > 0) consume_tile<D, NT, C::HALVES>(st, kbase, vbase, valid, ks, lane, a.scale_log2, kTile);
+    if (valid > 0)
+      consume_tile<D, NT, C::HALVES, CAUSAL>(st, kbase, vbase, valid, (int)key0, ks, lane, a.scale_log2, kTile);
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(empty + s));
   }
@@ -599,7 +633,7 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 // =====================================================================================
 struct ItemDesc {
   int b, g, p, kind;        // g: first KV head of the item's group; kind: 0 partition, 2 no more items
-  int n_tiles, n_parts, n_boxes, pad1;
+  int n_tiles, n_parts, n_boxes, item;   // item: queue index (test hook)
   int64_t key_begin, key_end;
 };
 static_assert(sizeof(ItemDesc) == 48, "descriptor slot size");
@@ -747,7 +781,8 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       }
       ItemDesc d;
       d.kind = 2;
-      d.b = d.g = d.p = d.n_tiles = d.n_parts = d.n_boxes = d.pad1 = 0;
+      d.b = d.g = d.p = d.n_tiles = d.n_parts = d.n_boxes = 0;
+      d.item = (int)it;
       d.key_begin = d.key_end = 0;
       if ((int64_t)it < total) {
         d.g = (int)(it % (uint32_t)groups) * HG;
@@ -796,7 +831,6 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   if (warp == C::CONSUMERS) {
     if (lane == 0) {
       const uint64_t pol = ptx::policy_evict_first();
-      const bool stall = a.stall_cta >= 0 && a.stall_cta == (int)blockIdx.x;
       const int nbox = TK / br;   // boxes per tile
       int tile_it = 0, stall_tile = -1;
       bool gave_up = false;
@@ -810,7 +844,8 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         }
         const ItemDesc d = desc[slot];
         if (d.kind == 2) break;
-        if (stall && k == 0) stall_tile = tile_it + 1;     // test hook: this tile is never loaded
+        // test hook: the second tile of queue item stall_cta is never loaded
+        if (a.stall_cta >= 0 && d.item == a.stall_cta && d.n_tiles > 1) stall_tile = tile_it + 1;
         const int* by = boxy + slot * kMaxBoxesPerPart;
         for (int t = 0; t < d.n_tiles; ++t, ++tile_it) {
           const int s = tile_it % STAGES;
@@ -890,7 +925,7 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         const int valid = (int)max((int64_t)0, min((int64_t)16, d.key_end - key0));
         if (valid < 16)
           zero_masked_v<C::HALVES, BOXP>(smem + s * C::STAGE_BYTES + C::KV_BYTES + head_off, ks, valid, lane, br);
-        if (valid > 0) consume_tile<D, NT, BOXP>(st, kbase, vbase, valid, ks, lane, a.scale_log2, br);
+        if (valid > 0) consume_tile<D, NT, BOXP>(st, kbase, vbase, valid, (int)key0, ks, lane, a.scale_log2, br);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(empty + s));
       }

@@ -58,15 +58,22 @@ typedef struct {
   int n_splits;          /* contiguous calls: splits per (sequence, KV head); 0 = heuristic */
   int merge_mode;        /* 0 = last-arriving CTA merges in the same kernel; 1 = separate merge kernel */
   uint32_t timeout_us;   /* limit of every device wait; 0 = 1,000,000 us */
-  int test_stall_cta;    /* test hook, -1 = off: linear id (x + X*(y + Y*z)) of one CTA whose
-                            producer never loads its second tile, so that the waits on it run out.
-                            Use with a small timeout_us; the call then reports GQA_ERR_TIMEOUT
-                            through gqa_workspace_check and the workspace must be re-initialised. */
+  int test_stall_cta;    /* test hook, -1 = off.  Contiguous calls: linear id (x + X*(y + Y*z)) of
+                            one CTA whose producer never loads its second tile; paged calls: the
+                            index of one work item (partition x head group, in queue order) whose
+                            second tile is never loaded.  The waits on that tile run out; use with
+                            a small timeout_us.  The call then reports GQA_ERR_TIMEOUT through
+                            gqa_workspace_check and the workspace must be re-initialised. */
   int paged_head_group;  /* paged calls: KV heads per work item and per TMA box, 1, 2 or 4 (must divide
                             h_kv; 2 and 4 need h_q / h_kv <= 16); 0 = 4, 2 or 1, the largest that fits */
+  int causal;            /* contiguous calls with T_q > 1 (speculative verification): query token t
+                            sees only the keys j <= S_kv - T_q + t (the T_q new tokens are the last
+                            T_q keys); 0 = every token sees all S_kv keys.  No counterpart on the
+                            pages (their kernel is stated for T_q = 1). */
 } gqa_options;
 
-/* Default options: n_splits 0, merge_mode 0, timeout_us 0, test_stall_cta -1, paged_head_group 0. */
+/* Default options: n_splits 0, merge_mode 0, timeout_us 0, test_stall_cta -1, paged_head_group 0,
+ * causal 0. */
 gqa_options gqa_default_options(void);
 
 /* Static text for a status code. */

@@ -20,7 +20,9 @@ design notes with its reason):
   shortcut valid only for zero / symmetric inputs, per its own caveat);
 * query head ``h`` reads KV head ``h // G`` (contiguous groups, matching the
   page's contiguous ``(G*T_q, d_head)`` query load per KV head);
-* every query token attends to all keys, no causal mask;
+* every query token attends to all keys, no causal mask -- unless ``causal`` is
+  asked for (the speculative-verification variant): then query token ``t`` of
+  ``T_q`` sees the keys ``j <= S_kv - T_q + t`` only;
 * every key is attended exactly once (the page's ``S_kv // n_ranks`` drops a
   remainder; the method does not);
 * an empty key range gives the partial ``(m, l, O) = (-inf, 0, 0)``; merging
@@ -138,23 +140,35 @@ def _unit_rows(q, b: int, g: int, T_q: int, G: int, D: int):
 
 
 def decode_unit(q, k, v, b: int, g: int, h_q: int, h_kv: int, D: int, scale: float,
-                s_begin: int = 0, s_len: Optional[int] = None):
+                s_begin: int = 0, s_len: Optional[int] = None, causal: bool = False):
     """Partial ``(m, l, O)`` of all query rows of KV head ``g`` of sequence ``b``
-    over keys ``[s_begin, s_begin + s_len)``; shapes ``(T_q, G)`` and ``(T_q, G, D)``."""
+    over keys ``[s_begin, s_begin + s_len)``; shapes ``(T_q, G)`` and ``(T_q, G, D)``.
+    With ``causal``, token ``t`` uses only the keys ``j <= S_kv - T_q + t`` of that range."""
     B, T_q, _ = q.shape
     S = k.shape[1]
     G = h_q // h_kv
     if s_len is None:
         s_len = S - s_begin
     qr = _unit_rows(q, b, g, T_q, G, D)
-    kr = k[b, s_begin:s_begin + s_len, g * D:(g + 1) * D]
-    vr = v[b, s_begin:s_begin + s_len, g * D:(g + 1) * D]
-    m, l, o = partial_rows(qr, kr, vr, scale)
-    return m.reshape(T_q, G), l.reshape(T_q, G), o.reshape(T_q, G, D)
+    if not causal:
+        kr = k[b, s_begin:s_begin + s_len, g * D:(g + 1) * D]
+        vr = v[b, s_begin:s_begin + s_len, g * D:(g + 1) * D]
+        m, l, o = partial_rows(qr, kr, vr, scale)
+        return m.reshape(T_q, G), l.reshape(T_q, G), o.reshape(T_q, G, D)
+    m = torch.empty(T_q, G, dtype=torch.float64)
+    l = torch.empty(T_q, G, dtype=torch.float64)
+    o = torch.empty(T_q, G, D, dtype=torch.float64)
+    for t in range(T_q):
+        hi = max(s_begin, min(s_begin + s_len, S - T_q + t + 1))      # keys [s_begin, hi) visible
+        kr = k[b, s_begin:hi, g * D:(g + 1) * D]
+        vr = v[b, s_begin:hi, g * D:(g + 1) * D]
+        mt, lt, ot = partial_rows(qr[t * G:(t + 1) * G], kr, vr, scale)
+        m[t], l[t], o[t] = mt, lt, ot
+    return m, l, o
 
 
 def decode_partial(q, k, v, h_q: int, h_kv: int, D: int, scale: float,
-                   s_begin: int = 0, s_len: Optional[int] = None):
+                   s_begin: int = 0, s_len: Optional[int] = None, causal: bool = False):
     """Partials of every query row over keys ``[s_begin, s_begin + s_len)``.
 
     Returns ``m, l`` of shape ``(B, T_q, h_q)`` and unnormalised ``O`` of shape
@@ -166,7 +180,7 @@ def decode_partial(q, k, v, h_q: int, h_kv: int, D: int, scale: float,
     o = torch.empty(B, T_q, h_q, D, dtype=torch.float64)
     for b in range(B):
         for g in range(h_kv):
-            mu, lu, ou = decode_unit(q, k, v, b, g, h_q, h_kv, D, scale, s_begin, s_len)
+            mu, lu, ou = decode_unit(q, k, v, b, g, h_q, h_kv, D, scale, s_begin, s_len, causal)
             m[b, :, g * G:(g + 1) * G] = mu
             l[b, :, g * G:(g + 1) * G] = lu
             o[b, :, g * G:(g + 1) * G, :] = ou
@@ -174,7 +188,7 @@ def decode_partial(q, k, v, h_q: int, h_kv: int, D: int, scale: float,
 
 
 def decode(q, k, v, h_q: int, h_kv: int, D: int, scale: float,
-           units: Optional[Iterable[Tuple[int, int]]] = None):
+           units: Optional[Iterable[Tuple[int, int]]] = None, causal: bool = False):
     """Attention output ``(B, T_q, h_q*D)`` in float64.
 
     ``units`` restricts the work to the listed ``(b, g)`` pairs (sequence, KV
@@ -185,7 +199,7 @@ def decode(q, k, v, h_q: int, h_kv: int, D: int, scale: float,
     out = torch.full((B, T_q, h_q * D), float("nan"), dtype=torch.float64)
     todo = [(b, g) for b in range(B) for g in range(h_kv)] if units is None else list(units)
     for b, g in todo:
-        _, l, o = decode_unit(q, k, v, b, g, h_q, h_kv, D, scale)
+        _, l, o = decode_unit(q, k, v, b, g, h_q, h_kv, D, scale, causal=causal)
         res = normalize(l, o)                                  # (T_q, G, D)
         out[b, :, g * G * D:(g + 1) * G * D] = res.reshape(T_q, G * D)
     return out

@@ -48,7 +48,8 @@ def test_version_and_status_strings(binding):
 
 def test_default_options(binding):
     o = binding.lib.gqa_default_options()
-    assert (o.n_splits, o.merge_mode, o.timeout_us, o.test_stall_cta, o.paged_head_group) == (0, 0, 0, -1, 0)
+    assert (o.n_splits, o.merge_mode, o.timeout_us, o.test_stall_cta, o.paged_head_group, o.causal) == \
+        (0, 0, 0, -1, 0, 0)
 
 
 def _fake(n=1 << 12):
@@ -80,7 +81,7 @@ def test_validation_codes_without_gpu(binding):
     assert dec(B=2, S=(1 << 30)) == binding.GQA_ERR_INVALID_ARG      # batch*S_kv >= 2^31
     assert lib.gqa_decode(p, p, p, p, 1, 1, 16, 8, 2, 64, float("nan"), p, 4096, st) == binding.GQA_ERR_INVALID_ARG
     # workspace too small (forced split count: sized without a device)
-    opt = binding.gqa_options(8, 0, 0, -1, 0)
+    opt = binding.gqa_options(8, 0, 0, -1, 0, 0)
     need = lib.gqa_decode_workspace_size(1, 1, 4096, 8, 2, 64, 8)
     assert need > 256
     r = lib.gqa_decode_ex(p, p, p, p, 1, 1, 4096, 8, 2, 64, s, p, need - 1, st, ctypes.byref(opt))
@@ -118,10 +119,10 @@ def test_paged_validation(binding):
     assert paged(maxlen=-1) == binding.GQA_ERR_INVALID_ARG
     assert paged(N=0) == binding.GQA_OK
     assert paged(wsb=255) == binding.GQA_ERR_WORKSPACE
-    opt = binding.gqa_options(0, 0, 0, -1, 3)                        # head group must be 1, 2 or 4
+    opt = binding.gqa_options(0, 0, 0, -1, 3, 0)                        # head group must be 1, 2 or 4
     assert lib.gqa_decode_paged_ex(p, p, p, p, p, p, 2, 64, 100, 16, 512, 8, 2, 128, 0.1, 1000, p, 1 << 20, st,
                                    ctypes.byref(opt)) == binding.GQA_ERR_INVALID_ARG
-    opt = binding.gqa_options(0, 0, 0, -1, 4)                        # ... and divide h_kv
+    opt = binding.gqa_options(0, 0, 0, -1, 4, 0)                        # ... and divide h_kv
     assert lib.gqa_decode_paged_ex(p, p, p, p, p, p, 2, 64, 100, 16, 512, 8, 2, 128, 0.1, 1000, p, 1 << 20, st,
                                    ctypes.byref(opt)) == binding.GQA_ERR_INVALID_ARG
     assert lib.gqa_paged_workspace_size(64, 32, 8, 128, 16384, 512) > 0

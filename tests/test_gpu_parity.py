@@ -329,3 +329,34 @@ def test_paged_timeout_is_reported_not_hung(gqa):
     o = run_paged(gqa, p, workspace_tensor=ws)
     assert gqa.gqa_workspace_check(ws) == gqa.GQA_OK
     assert_close(o, ref_paged(p).reshape(8, -1), "paged after a timeout")
+
+
+# ---------------------------------------------------------------- causal tail (speculative verify)
+@pytest.mark.parametrize("hq,hkv,T,S,D", [(32, 8, 4, 5000, 128), (64, 8, 4, 20000, 128), (16, 16, 3, 777, 64),
+                                          (8, 2, 2, 64, 128), (32, 4, 8, 3000, 128), (16, 2, 4, 5, 64)])
+@pytest.mark.parametrize("n_splits", [0, 1, 7])
+def test_causal_tail(gqa, hq, hkv, T, S, D, n_splits):
+    x = gi.make_contiguous(gi.custom(2, T, S, hq, hkv, D, 1300 + S + T))
+    ref = oracle.decode(x["q"], x["k"], x["v"], hq, hkv, D, x["scale"], causal=True)
+    o = run_contig(gqa, x, causal=True, n_splits=n_splits)
+    assert_close(o, ref, f"causal hq={hq} hkv={hkv} T={T} S={S} D={D} splits={n_splits}")
+
+
+def test_causal_partial_with_empty_rows(gqa):
+    """A key range past some tokens' causal limit: those rows get the empty partial."""
+    T, S, hq, hkv, D = 4, 600, 16, 4, 128
+    x = gi.make_contiguous(gi.custom(1, T, S, hq, hkv, D, 1401))
+    q, k, v = cuda(x["q"]), cuda(x["k"]), cuda(x["v"])
+    for s0, n in [(S - 3, 3), (0, S), (100, 400), (S - 1, 1)]:
+        m, l, op = gqa.gqa_decode_partial(q, k, v, hq, hkv, s0, n, x["scale"], causal=True)
+        torch.cuda.synchronize()
+        rm, rl, ro = oracle.decode_partial(x["q"], x["k"], x["v"], hq, hkv, D, x["scale"], s0, n, causal=True)
+        rm, rl, ro = rm.reshape(-1), rl.reshape(-1), ro.reshape(-1, D)
+        m, l, op = m.double().cpu(), l.double().cpu(), op.double().cpu()
+        empty = torch.isneginf(rm)
+        assert torch.equal(torch.isneginf(m), empty)
+        assert (l[empty] == 0).all() and (op[empty] == 0).all()
+        keep = ~empty
+        assert ((m[keep] - rm[keep]).abs() <= 1e-5 * (1 + rm[keep].abs())).all()
+        assert ((l[keep] - rl[keep]).abs() <= 2e-3 * rl[keep]).all()
+        assert_close(op[keep] / l[keep][:, None], oracle.normalize(rl[keep], ro[keep]), f"causal partial {s0},{n}")

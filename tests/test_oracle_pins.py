@@ -254,6 +254,31 @@ def pin_paged(orc) -> bool:
     return ok
 
 
+def pin_causal(orc) -> bool:
+    """Causal tail (token t of T_q sees keys j <= S - T_q + t): equals PyTorch SDPA with the
+    explicit bottom-right mask, equals the plain decode of each token over its visible
+    prefix, and is the plain decode when T_q = 1."""
+    ok = True
+    for (B, T_q, S, h_q, h_kv, D, seed) in [(2, 4, 37, 8, 2, 16, 121), (1, 3, 5, 4, 1, 8, 122)]:
+        x = _inputs(B, T_q, S, h_q, h_kv, D, seed)
+        scale = 1.0 / math.sqrt(D)
+        got = orc.decode(x["q"], x["k"], x["v"], h_q, h_kv, D, scale, causal=True)
+        q = torch.from_numpy(x["q"]).double().view(B, T_q, h_q, D).permute(0, 2, 1, 3)
+        k = torch.from_numpy(x["k"]).double().view(B, S, h_kv, D).permute(0, 2, 1, 3)
+        v = torch.from_numpy(x["v"]).double().view(B, S, h_kv, D).permute(0, 2, 1, 3)
+        mask = torch.arange(S)[None, :] <= (S - T_q + torch.arange(T_q))[:, None]
+        ref = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale, enable_gqa=True)
+        ok &= _close(got, ref.permute(0, 2, 1, 3).reshape(B, T_q, h_q * D), 1e-11)
+        for t in range(T_q):
+            hi = S - T_q + t + 1
+            one = orc.decode(x["q"][:, t:t + 1], x["k"][:, :hi], x["v"][:, :hi], h_q, h_kv, D, scale)
+            ok &= _close(got[:, t:t + 1], one)
+    x = _inputs(2, 1, 20, 4, 2, 8, 123)
+    ok &= _close(orc.decode(x["q"], x["k"], x["v"], 4, 2, 8, 0.3, causal=True),
+                 orc.decode(x["q"], x["k"], x["v"], 4, 2, 8, 0.3))
+    return ok
+
+
 def pin_golden(orc) -> bool:
     """Hand-worked examples under ``tests/golden/``."""
     ok = True
@@ -305,7 +330,7 @@ def _read_golden(path: str) -> dict:
 
 
 PINS = [pin_brute_force, pin_sdpa, pin_constant_scores, pin_one_hot, pin_single_key,
-        pin_split_merge, pin_merge_closed_form, pin_permutation, pin_shift, pin_paged, pin_golden]
+        pin_split_merge, pin_merge_closed_form, pin_permutation, pin_shift, pin_paged, pin_causal, pin_golden]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -408,6 +433,24 @@ def _m_gather_off_by_one(pool, table_row, length, block_size):
     return np.asarray(pool)[blocks, slots]
 
 
+def _m_causal_off_by_one(q, k, v, b, g, h_q, h_kv, D, scale, s_begin=0, s_len=None, causal=False):
+    B, T_q, _ = q.shape
+    S = k.shape[1]
+    G = h_q // h_kv
+    if s_len is None:
+        s_len = S - s_begin
+    qr = _unit_rows(q, b, g, T_q, G, D)
+    m = torch.empty(T_q, G, dtype=torch.float64)
+    l = torch.empty(T_q, G, dtype=torch.float64)
+    o = torch.empty(T_q, G, D, dtype=torch.float64)
+    for t in range(T_q):
+        hi = s_begin + s_len if not causal else max(s_begin, min(s_begin + s_len, S - T_q + t))
+        mt, lt, ot = partial_rows(qr[t * G:(t + 1) * G], k[b, s_begin:hi, g * D:(g + 1) * D],
+                                  v[b, s_begin:hi, g * D:(g + 1) * D], scale)
+        m[t], l[t], o[t] = mt, lt, ot
+    return m, l, o
+
+
 MUTANTS = {
     "no_scale": dict(partial_rows=_m_no_scale),
     "k_reshaped_not_transposed": dict(partial_rows=_m_reshape_k),
@@ -417,6 +460,7 @@ MUTANTS = {
     "merge_drops_l_term": dict(merge_pair=_m_merge_drop_l),
     "no_normalize": dict(normalize=_m_no_normalize),
     "paged_slot_off_by_one": dict(gather_paged=_m_gather_off_by_one),
+    "causal_limit_off_by_one": dict(decode_unit=_m_causal_off_by_one),
 }
 
 
@@ -438,3 +482,5 @@ def _safe(pin, mod) -> bool:
 # these names are referenced by the mutant bodies (resolved in the mutant namespace)
 _f64 = gqa_oracle._f64
 NEG_INF = gqa_oracle.NEG_INF
+_unit_rows = gqa_oracle._unit_rows
+partial_rows = gqa_oracle.partial_rows
