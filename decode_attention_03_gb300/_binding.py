@@ -37,7 +37,7 @@ class GQAError(RuntimeError):
 class gqa_options(ctypes.Structure):
     _fields_ = [("n_splits", ctypes.c_int), ("merge_mode", ctypes.c_int),
                 ("timeout_us", ctypes.c_uint32), ("test_stall_cta", ctypes.c_int),
-                ("paged_head_group", ctypes.c_int), ("causal", ctypes.c_int)]
+                ("paged_head_group", ctypes.c_int), ("causal", ctypes.c_int), ("bf16", ctypes.c_int)]
 
 
 def _load():
@@ -109,17 +109,27 @@ def _f16(t: torch.Tensor, name: str) -> None:
         raise ValueError(f"{name} must be a contiguous float16 CUDA tensor")
 
 
+def _h16(t: torch.Tensor, name: str, dtype=None) -> None:
+    """float16 or bfloat16 (and equal to ``dtype`` when given)."""
+    if not (t.is_cuda and t.dtype in (torch.float16, torch.bfloat16) and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous float16 or bfloat16 CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must have dtype {dtype}")
+
+
 def _f32(t: torch.Tensor, name: str) -> None:
     if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
         raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
 
 
-def _opts(n_splits=0, merge_mode=0, timeout_us=0, test_stall_cta=-1, paged_head_group=0, causal=False):
+def _opts(n_splits=0, merge_mode=0, timeout_us=0, test_stall_cta=-1, paged_head_group=0, causal=False,
+          bf16=False):
     o = gqa_options()
     o.n_splits, o.merge_mode, o.timeout_us, o.test_stall_cta = int(n_splits), int(merge_mode), int(timeout_us), \
         int(test_stall_cta)
     o.paged_head_group = int(paged_head_group)
     o.causal = 1 if causal else 0
+    o.bf16 = 1 if bf16 else 0
     return o
 
 
@@ -166,7 +176,7 @@ def gqa_workspace_check(ws: torch.Tensor, stream=None) -> int:
 
 # ---------------------------------------------------------------- calls
 def _shape_qkv(q, k, v, h_q, h_kv):
-    _f16(q, "q"), _f16(k, "k"), _f16(v, "v")
+    _h16(q, "q"), _h16(k, "k", q.dtype), _h16(v, "v", q.dtype)
     if q.dim() != 3 or k.dim() != 3 or k.shape != v.shape or k.shape[0] != q.shape[0]:
         raise ValueError("q must be (batch, T_q, h_q*d_head), k and v (batch, S_kv, h_kv*d_head)")
     B, T_q, qc = q.shape
@@ -181,18 +191,19 @@ def gqa_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, h_q: int, h_kv
                workspace_tensor: Optional[torch.Tensor] = None, stream=None, n_splits: int = 0,
                merge_mode: int = 0, timeout_us: int = 0, test_stall_cta: int = -1,
                causal: bool = False) -> torch.Tensor:
-    """O = softmax(scale Q K^T) V for GQA decode; q (B, T_q, h_q*D), k/v (B, S_kv, h_kv*D) f16.
+    """O = softmax(scale Q K^T) V for GQA decode; q (B, T_q, h_q*D), k/v (B, S_kv, h_kv*D) float16 or
+    bfloat16 (all the same; the output has that dtype too).
     ``causal``: query token t sees keys j <= S_kv - T_q + t only."""
     B, T_q, S, D = _shape_qkv(q, k, v, h_q, h_kv)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if out is None:
         out = torch.empty_like(q)
-    _f16(out, "out")
+    _h16(out, "out", q.dtype)
     nbytes = gqa_decode_workspace_size(B, T_q, S, h_q, h_kv, D, n_splits)
     if nbytes == 0:
         raise GQAError(GQA_ERR_INVALID_ARG, "gqa_decode_workspace_size")
     ws = workspace(nbytes, q.device, stream) if workspace_tensor is None else workspace_tensor
-    opt = _opts(n_splits, merge_mode, timeout_us, test_stall_cta, causal=causal)
+    opt = _opts(n_splits, merge_mode, timeout_us, test_stall_cta, causal=causal, bf16=q.dtype == torch.bfloat16)
     st = lib.gqa_decode_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T_q, S, h_q, h_kv, D, scale,
                            _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(opt))
     _check(st, "gqa_decode")
@@ -215,7 +226,7 @@ def gqa_decode_partial(q, k, v, h_q: int, h_kv: int, s_begin: int, s_len: int, s
     if nbytes == 0:
         raise GQAError(GQA_ERR_INVALID_ARG, "gqa_decode_workspace_size")
     ws = workspace(nbytes, dev, stream) if workspace_tensor is None else workspace_tensor
-    opt = _opts(n_splits, merge_mode, causal=causal)
+    opt = _opts(n_splits, merge_mode, causal=causal, bf16=q.dtype == torch.bfloat16)
     st = lib.gqa_decode_partial_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(m), _ptr(l), _ptr(o_part), B, T_q, S,
                                    int(s_begin), int(s_len), h_q, h_kv, D, scale, _ptr(ws), ws.numel(),
                                    _stream(stream), ctypes.byref(opt))
@@ -251,8 +262,9 @@ def gqa_decode_paged(q, k_pool, v_pool, block_tables, seq_lens, h_q: int, h_kv: 
                      *, max_seq_len: int, partition_size: int = 512, out=None, workspace_tensor=None,
                      stream=None, timeout_us: int = 0, test_stall_cta: int = -1,
                      head_group: int = 0) -> torch.Tensor:
-    """Paged decode; q (N, h_q*D), pools (num_blocks, block_size, h_kv*D), tables (N, max_blocks) int32."""
-    _f16(q, "q"), _f16(k_pool, "k_pool"), _f16(v_pool, "v_pool")
+    """Paged decode; q (N, h_q*D), pools (num_blocks, block_size, h_kv*D) float16 or bfloat16,
+    tables (N, max_blocks) int32."""
+    _h16(q, "q"), _h16(k_pool, "k_pool", q.dtype), _h16(v_pool, "v_pool", q.dtype)
     if not (block_tables.is_cuda and block_tables.dtype == torch.int32 and block_tables.is_contiguous()):
         raise ValueError("block_tables must be a contiguous int32 CUDA tensor")
     if not (seq_lens.is_cuda and seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()):
@@ -265,12 +277,12 @@ def gqa_decode_paged(q, k_pool, v_pool, block_tables, seq_lens, h_q: int, h_kv: 
     D = qc // h_q
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     out = torch.empty_like(q2) if out is None else out
-    _f16(out, "out")
+    _h16(out, "out", q.dtype)
     nbytes = gqa_paged_workspace_size(N, h_q, h_kv, D, max_seq_len, partition_size)
     if nbytes == 0:
         raise GQAError(GQA_ERR_INVALID_ARG, "gqa_paged_workspace_size")
     ws = workspace(nbytes, q.device, stream) if workspace_tensor is None else workspace_tensor
-    opt = _opts(0, 0, timeout_us, test_stall_cta, head_group)
+    opt = _opts(0, 0, timeout_us, test_stall_cta, head_group, bf16=q.dtype == torch.bfloat16)
     st = lib.gqa_decode_paged_ex(_ptr(q2), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens),
                                  _ptr(out), N, block_tables.shape[1], num_blocks, block_size, partition_size,
                                  h_q, h_kv, D, scale, int(max_seq_len), _ptr(ws), ws.numel(), _stream(stream),
@@ -290,6 +302,7 @@ def gqa_decode_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, h_q: i
     For callers that cannot allocate device memory.  Calls on one device share that array,
     so they must not overlap on the GPU; shapes needing more than 8 MiB of workspace raise."""
     B, T_q, S, D = _shape_qkv(q, k, v, h_q, h_kv)
+    _f16(q, "q")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if out is None:
         out = torch.empty_like(q)

@@ -39,8 +39,8 @@ bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 struct DevState {
   bool ready = false;
   int sms = 0;
-  int occ[2][4][5] = {};       // [d index][row class][kernel: see kernel_slot] resident CTAs per SM,
-                               // 0 = not prepared
+  int occ[2][4][5][2] = {};    // [d index][row class][kernel: see kernel_slot][bf16] resident CTAs
+                               // per SM, 0 = not prepared
 };
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
@@ -52,23 +52,34 @@ EncodeTiledFn g_encode = nullptr;
 
 // Kernel selector `kind`: 0 contiguous, 1 contiguous with the causal tail, and for the paged
 // kernel 100 + its head group (101, 102, 104).
-cudaError_t prepare_unit(int di, int cls, int kind, int* occ) {
-  if (kind < 100) return di == 0 ? contig_d64_prepare(cls, kind, occ) : contig_d128_prepare(cls, kind, occ);
-  return di == 0 ? paged_d64_prepare(cls, kind - 100, occ) : paged_d128_prepare(cls, kind - 100, occ);
+typedef cudaError_t (*PrepareFn)(int, int, int*);
+typedef cudaError_t (*LaunchFn)(int, int, dim3, cudaStream_t, const CUtensorMap&, const CUtensorMap&,
+                                const DecodeArgs&);
+// [paged][d index][bf16]
+const PrepareFn kPrepare[2][2][2] = {{{contig_d64_prepare, contig_d64_bf16_prepare},
+                                      {contig_d128_prepare, contig_d128_bf16_prepare}},
+                                     {{paged_d64_prepare, paged_d64_bf16_prepare},
+                                      {paged_d128_prepare, paged_d128_bf16_prepare}}};
+const LaunchFn kLaunch[2][2][2] = {{{contig_d64_launch, contig_d64_bf16_launch},
+                                    {contig_d128_launch, contig_d128_bf16_launch}},
+                                   {{paged_d64_launch, paged_d64_bf16_launch},
+                                    {paged_d128_launch, paged_d128_bf16_launch}}};
+
+cudaError_t prepare_unit(int di, int cls, int kind, int bf16, int* occ) {
+  const int paged = kind >= 100;
+  return kPrepare[paged][di][bf16](cls, paged ? kind - 100 : kind, occ);
 }
 
-cudaError_t launch_unit(int di, int cls, int kind, dim3 grid, cudaStream_t st, const CUtensorMap& tk,
+cudaError_t launch_unit(int di, int cls, int kind, int bf16, dim3 grid, cudaStream_t st, const CUtensorMap& tk,
                         const CUtensorMap& tv, const DecodeArgs& a) {
-  if (kind < 100)
-    return di == 0 ? contig_d64_launch(cls, kind, grid, st, tk, tv, a) : contig_d128_launch(cls, kind, grid, st, tk, tv, a);
-  return di == 0 ? paged_d64_launch(cls, kind - 100, grid, st, tk, tv, a)
-                 : paged_d128_launch(cls, kind - 100, grid, st, tk, tv, a);
+  const int paged = kind >= 100;
+  return kLaunch[paged][di][bf16](cls, paged ? kind - 100 : kind, grid, st, tk, tv, a);
 }
 
 int kernel_slot(int kind) { return kind < 100 ? kind : (kind == 101 ? 2 : (kind == 102 ? 3 : 4)); }
 
 // SM count and resident CTAs per SM of one kernel configuration on the current device
-gqa_status device_info(int di, int cls, int kind, int* sms, int* occ) {
+gqa_status device_info(int di, int cls, int kind, int bf16, int* sms, int* occ) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -86,10 +97,10 @@ gqa_status device_info(int di, int cls, int kind, int* sms, int* occ) {
     }
     st.ready = true;
   }
-  int& o = st.occ[di][cls][kernel_slot(kind)];
+  int& o = st.occ[di][cls][kernel_slot(kind)][bf16];
   if (o == 0) {
     int v = 0;
-    if (prepare_unit(di, cls, kind, &v) != cudaSuccess || v <= 0) return GQA_ERR_CUDA;
+    if (prepare_unit(di, cls, kind, bf16, &v) != cudaSuccess || v <= 0) return GQA_ERR_CUDA;
     o = v;
   }
   *sms = st.sms;
@@ -97,17 +108,18 @@ gqa_status device_info(int di, int cls, int kind, int* sms, int* occ) {
   return GQA_OK;
 }
 
-// 3-D map over a (rows, cols) f16 matrix seen as (64-column planes, rows, 64 columns):
+// 3-D map over a (rows, cols) f16 / bf16 matrix seen as (64-column planes, rows, 64 columns):
 // dims {64, rows, cols / 64} with strides {cols * 2 bytes, 128 bytes}.  A box of
 // {64, box_rows, planes} lands in shared memory as `planes` consecutive [box_rows][64]
 // arrays, rows 128 bytes with the 128-byte swizzle.
 gqa_status encode_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows,
-                      uint32_t planes) {
+                      uint32_t planes, int bf16) {
   cuuint64_t dims[3] = {64, rows > 0 ? rows : 1, cols / 64};
   cuuint64_t strides[2] = {cols * 2, 128};
   cuuint32_t box[3] = {64, box_rows, planes};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                        const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GQA_OK : GQA_ERR_CUDA;
@@ -163,6 +175,7 @@ gqa_options defaults() {
   o.test_stall_cta = -1;
   o.paged_head_group = 0;
   o.causal = 0;
+  o.bf16 = 0;
   return o;
 }
 
@@ -195,7 +208,7 @@ gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_
     p->n_splits = (int)n;
   } else if (need_device) {
     int sms = 0, occ = 0;
-    gqa_status s = device_info(p->di, p->cls, 0, &sms, &occ);
+    gqa_status s = device_info(p->di, p->cls, 0, 0, &sms, &occ);
     if (s != GQA_OK) return s;
     p->n_splits = heuristic_splits(p->units, p->tiles, sms, occ);
   } else {
@@ -206,15 +219,16 @@ gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_
 }
 
 gqa_status merge_launch(const float* m, const float* l, const float* op, int n_parts, int64_t rows, int D,
-                        __half* o, float* mo, float* lo, float* oo, cudaStream_t st) {
+                        __half* o, float* mo, float* lo, float* oo, cudaStream_t st, int bf16 = 0) {
   if (rows == 0) return GQA_OK;
   const int warps = 8;
   const int64_t blocks = (rows + warps - 1) / warps;
   if (blocks > 2147483647LL) return GQA_ERR_INVALID_ARG;
-  if (D == 64)
-    gqa_merge_kernel<64><<<(unsigned)blocks, warps * 32, 0, st>>>(m, l, op, n_parts, rows, o, mo, lo, oo);
-  else
-    gqa_merge_kernel<128><<<(unsigned)blocks, warps * 32, 0, st>>>(m, l, op, n_parts, rows, o, mo, lo, oo);
+  const unsigned g = (unsigned)blocks;
+  if (D == 64 && !bf16) gqa_merge_kernel<64, false><<<g, warps * 32, 0, st>>>(m, l, op, n_parts, rows, o, mo, lo, oo);
+  if (D == 64 && bf16) gqa_merge_kernel<64, true><<<g, warps * 32, 0, st>>>(m, l, op, n_parts, rows, o, mo, lo, oo);
+  if (D == 128 && !bf16) gqa_merge_kernel<128, false><<<g, warps * 32, 0, st>>>(m, l, op, n_parts, rows, o, mo, lo, oo);
+  if (D == 128 && bf16) gqa_merge_kernel<128, true><<<g, warps * 32, 0, st>>>(m, l, op, n_parts, rows, o, mo, lo, oo);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
@@ -242,13 +256,14 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
   if (ws_bytes < p.lay.total) return GQA_ERR_WORKSPACE;
   int sms = 0, occ = 0;
   const int kind = opt.causal ? 1 : 0;
-  s = device_info(p.di, p.cls, kind, &sms, &occ);
+  const int bf16 = opt.bf16 ? 1 : 0;
+  s = device_info(p.di, p.cls, kind, bf16, &sms, &occ);
   if (s != GQA_OK) return s;
 
   CUtensorMap tk, tv;
   const uint64_t cols = (uint64_t)h_kv * D, nrows = (uint64_t)B * (uint64_t)S_kv;
-  if ((s = encode_map(&tk, k, cols, nrows, kTile, (uint32_t)D / 64)) != GQA_OK) return s;
-  if ((s = encode_map(&tv, v, cols, nrows, kTile, (uint32_t)D / 64)) != GQA_OK) return s;
+  if ((s = encode_map(&tk, k, cols, nrows, kTile, (uint32_t)D / 64, bf16)) != GQA_OK) return s;
+  if ((s = encode_map(&tv, v, cols, nrows, kTile, (uint32_t)D / 64, bf16)) != GQA_OK) return s;
 
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   DecodeArgs a;
@@ -284,9 +299,9 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   dim3 grid((unsigned)h_kv, (unsigned)p.n_splits, (unsigned)B);
-  if (launch_unit(p.di, p.cls, kind, grid, st, tk, tv, a) != cudaSuccess) return GQA_ERR_CUDA;
+  if (launch_unit(p.di, p.cls, kind, bf16, grid, st, tk, tv, a) != cudaSuccess) return GQA_ERR_CUDA;
   if (p.n_splits > 1 && !a.merge_in_kernel) {
-    return merge_launch(a.ws_m, a.ws_l, a.ws_o, p.n_splits, p.R, D, a.o, a.m_out, a.l_out, a.o_part_out, st);
+    return merge_launch(a.ws_m, a.ws_l, a.ws_o, p.n_splits, p.R, D, a.o, a.m_out, a.l_out, a.o_part_out, st, bf16);
   }
   return GQA_OK;
 }
@@ -344,15 +359,16 @@ gqa_status paged_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t*
   if (hg == 0) hg = p.cls <= 1 ? (h_kv % 4 == 0 ? 4 : (h_kv % 2 == 0 ? 2 : 1)) : 1;
   if (!(hg == 1 || hg == 2 || hg == 4) || h_kv % hg != 0 || (hg > 1 && p.cls > 1)) return GQA_ERR_INVALID_ARG;
   int sms = 0, occ = 0;
-  s = device_info(p.di, p.cls, 100 + hg, &sms, &occ);
+  const int bf16 = opt.bf16 ? 1 : 0;
+  s = device_info(p.di, p.cls, 100 + hg, bf16, &sms, &occ);
   if (s != GQA_OK) return s;
 
   CUtensorMap tk, tv;
   const uint64_t cols = (uint64_t)h_kv * D, nrows = (uint64_t)num_blocks * block_size;
   const uint32_t box_rows = (uint32_t)std::min(block_size, 16 * (4 / hg));   // min(block, keys per tile)
   const uint32_t planes = (uint32_t)(hg * D / 64);
-  if ((s = encode_map(&tk, k_pool, cols, nrows, box_rows, planes)) != GQA_OK) return s;
-  if ((s = encode_map(&tv, v_pool, cols, nrows, box_rows, planes)) != GQA_OK) return s;
+  if ((s = encode_map(&tk, k_pool, cols, nrows, box_rows, planes, bf16)) != GQA_OK) return s;
+  if ((s = encode_map(&tv, v_pool, cols, nrows, box_rows, planes, bf16)) != GQA_OK) return s;
 
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   DecodeArgs a;
@@ -394,15 +410,15 @@ gqa_status paged_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t*
     a.R = (int64_t)n * h_q;
     a.total_items = (int64_t)n * p.max_parts * (h_kv / hg);   // upper bound; the kernel counts the real ones
     const int64_t ctas = std::min<int64_t>((int64_t)sms * occ, a.total_items);
-    if (launch_unit(p.di, p.cls, 100 + hg, dim3((unsigned)ctas, 1, 1), st, tk, tv, a) != cudaSuccess)
+    if (launch_unit(p.di, p.cls, 100 + hg, bf16, dim3((unsigned)ctas, 1, 1), st, tk, tv, a) != cudaSuccess)
       return GQA_ERR_CUDA;
     if (p.max_parts > 1) {
       // second pass: fold the partitions of every multi-partition sequence
       const unsigned blocks = (unsigned)((a.R + 7) / 8);
-      if (D == 64)
-        gqa_paged_merge_kernel<64><<<blocks, 256, 0, st>>>(a);
-      else
-        gqa_paged_merge_kernel<128><<<blocks, 256, 0, st>>>(a);
+      if (D == 64 && !bf16) gqa_paged_merge_kernel<64, false><<<blocks, 256, 0, st>>>(a);
+      if (D == 64 && bf16) gqa_paged_merge_kernel<64, true><<<blocks, 256, 0, st>>>(a);
+      if (D == 128 && !bf16) gqa_paged_merge_kernel<128, false><<<blocks, 256, 0, st>>>(a);
+      if (D == 128 && bf16) gqa_paged_merge_kernel<128, true><<<blocks, 256, 0, st>>>(a);
       if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     }
   }

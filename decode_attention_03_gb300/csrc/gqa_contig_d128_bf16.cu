@@ -1,0 +1,6 @@
+// Instances of the split-KV decode kernels: contiguous K/V, d_head = 128, bf16 elements.
+#include "gqa_instances.cuh"
+
+namespace gqa {
+GQA_DEFINE_CONTIG_UNIT(contig_d128_bf16, 128, true)
+}  // namespace gqa

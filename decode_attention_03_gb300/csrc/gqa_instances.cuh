@@ -34,7 +34,7 @@ constexpr int paged_stages_for() {
   return n < 2 ? 2 : (n > 8 ? 8 : n);
 }
 
-template <int D, int CLS, bool CAUSAL>
+template <int D, int CLS, bool CAUSAL, bool BF16>
 struct Inst {
   static constexpr int NT = cls_nt(CLS);
   static constexpr int WN = cls_wn(CLS);
@@ -43,19 +43,19 @@ struct Inst {
   static_assert(C::SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
   static cudaError_t prepare(int* occupancy) {
-    auto fn = gqa_split_kernel<D, NT, WN, STAGES, CAUSAL>;
+    auto fn = gqa_split_kernel<D, NT, WN, STAGES, CAUSAL, BF16>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, fn, C::THREADS, C::SMEM_BYTES);
   }
   static cudaError_t launch(dim3 grid, cudaStream_t st, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a) {
-    gqa_split_kernel<D, NT, WN, STAGES, CAUSAL><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tk, tv, a);
+    gqa_split_kernel<D, NT, WN, STAGES, CAUSAL, BF16><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tk, tv, a);
     return cudaGetLastError();
   }
 };
 
-template <int D, int CLS, int HG>
+template <int D, int CLS, int HG, bool BF16>
 struct PagedInst {
   static constexpr int NT = cls_nt(CLS);
   static constexpr int WN = cls_wn(CLS);
@@ -64,64 +64,69 @@ struct PagedInst {
   static_assert(C::PSMEM_BYTES <= 227 * 1024, "shared memory budget");
 
   static cudaError_t prepare(int* occupancy) {
-    auto fn = gqa_paged_kernel<D, NT, WN, STAGES, HG>;
+    auto fn = gqa_paged_kernel<D, NT, WN, STAGES, HG, BF16>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::PSMEM_BYTES);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, fn, C::PTHREADS, C::PSMEM_BYTES);
   }
   static cudaError_t launch(dim3 grid, cudaStream_t st, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a) {
-    gqa_paged_kernel<D, NT, WN, STAGES, HG><<<grid, C::PTHREADS, C::PSMEM_BYTES, st>>>(tk, tv, a);
+    gqa_paged_kernel<D, NT, WN, STAGES, HG, BF16><<<grid, C::PTHREADS, C::PSMEM_BYTES, st>>>(tk, tv, a);
     return cudaGetLastError();
   }
 };
 
-// Contiguous units: cls in [0, 4), variant = causal (0 / 1).  Paged units: cls in [0, 4),
-// variant = head group in {1, 2, 4} (2 and 4 only for cls 0 and 1).
+// One unit (translation unit) per (kernel kind, d_head, element type).  Contiguous units:
+// cls in [0, 4), variant = causal (0 / 1).  Paged units: cls in [0, 4), variant = head
+// group in {1, 2, 4} (2 and 4 only for cls 0 and 1).
 #define GQA_DECLARE_UNIT(NAME)                                                                   \
   cudaError_t NAME##_prepare(int cls, int variant, int* occupancy);                              \
   cudaError_t NAME##_launch(int cls, int variant, dim3 grid, cudaStream_t st, const CUtensorMap& tk, \
                             const CUtensorMap& tv, const DecodeArgs& a);
 
-#define GQA_CONTIG_CASES(D, CALL)                                                                \
-  if (cls == 0) return variant ? Inst<D, 0, true>::CALL : Inst<D, 0, false>::CALL;               \
-  if (cls == 1) return variant ? Inst<D, 1, true>::CALL : Inst<D, 1, false>::CALL;               \
-  if (cls == 2) return variant ? Inst<D, 2, true>::CALL : Inst<D, 2, false>::CALL;               \
-  if (cls == 3) return variant ? Inst<D, 3, true>::CALL : Inst<D, 3, false>::CALL;               \
+#define GQA_CONTIG_CASES(D, BF, CALL)                                                            \
+  if (cls == 0) return variant ? Inst<D, 0, true, BF>::CALL : Inst<D, 0, false, BF>::CALL;       \
+  if (cls == 1) return variant ? Inst<D, 1, true, BF>::CALL : Inst<D, 1, false, BF>::CALL;       \
+  if (cls == 2) return variant ? Inst<D, 2, true, BF>::CALL : Inst<D, 2, false, BF>::CALL;       \
+  if (cls == 3) return variant ? Inst<D, 3, true, BF>::CALL : Inst<D, 3, false, BF>::CALL;       \
   return cudaErrorInvalidValue;
 
-#define GQA_DEFINE_CONTIG_UNIT(NAME, D)                                                          \
+#define GQA_DEFINE_CONTIG_UNIT(NAME, D, BF)                                                      \
   cudaError_t NAME##_prepare(int cls, int variant, int* occupancy) {                             \
-    GQA_CONTIG_CASES(D, prepare(occupancy))                                                      \
+    GQA_CONTIG_CASES(D, BF, prepare(occupancy))                                                  \
   }                                                                                              \
   cudaError_t NAME##_launch(int cls, int variant, dim3 grid, cudaStream_t st, const CUtensorMap& tk, \
                             const CUtensorMap& tv, const DecodeArgs& a) {                        \
-    GQA_CONTIG_CASES(D, launch(grid, st, tk, tv, a))                                             \
+    GQA_CONTIG_CASES(D, BF, launch(grid, st, tk, tv, a))                                         \
   }
 
-#define GQA_PAGED_CASES(D, CALL)                                                                 \
-  if (cls == 0 && variant == 1) return PagedInst<D, 0, 1>::CALL;                                 \
-  if (cls == 0 && variant == 2) return PagedInst<D, 0, 2>::CALL;                                 \
-  if (cls == 0 && variant == 4) return PagedInst<D, 0, 4>::CALL;                                 \
-  if (cls == 1 && variant == 1) return PagedInst<D, 1, 1>::CALL;                                 \
-  if (cls == 1 && variant == 2) return PagedInst<D, 1, 2>::CALL;                                 \
-  if (cls == 1 && variant == 4) return PagedInst<D, 1, 4>::CALL;                                 \
-  if (cls == 2 && variant == 1) return PagedInst<D, 2, 1>::CALL;                                 \
-  if (cls == 3 && variant == 1) return PagedInst<D, 3, 1>::CALL;                                 \
+#define GQA_PAGED_CASES(D, BF, CALL)                                                             \
+  if (cls == 0 && variant == 1) return PagedInst<D, 0, 1, BF>::CALL;                             \
+  if (cls == 0 && variant == 2) return PagedInst<D, 0, 2, BF>::CALL;                             \
+  if (cls == 0 && variant == 4) return PagedInst<D, 0, 4, BF>::CALL;                             \
+  if (cls == 1 && variant == 1) return PagedInst<D, 1, 1, BF>::CALL;                             \
+  if (cls == 1 && variant == 2) return PagedInst<D, 1, 2, BF>::CALL;                             \
+  if (cls == 1 && variant == 4) return PagedInst<D, 1, 4, BF>::CALL;                             \
+  if (cls == 2 && variant == 1) return PagedInst<D, 2, 1, BF>::CALL;                             \
+  if (cls == 3 && variant == 1) return PagedInst<D, 3, 1, BF>::CALL;                             \
   return cudaErrorInvalidValue;
 
-#define GQA_DEFINE_PAGED_UNIT(NAME, D)                                                           \
+#define GQA_DEFINE_PAGED_UNIT(NAME, D, BF)                                                       \
   cudaError_t NAME##_prepare(int cls, int variant, int* occupancy) {                             \
-    GQA_PAGED_CASES(D, prepare(occupancy))                                                       \
+    GQA_PAGED_CASES(D, BF, prepare(occupancy))                                                   \
   }                                                                                              \
   cudaError_t NAME##_launch(int cls, int variant, dim3 grid, cudaStream_t st, const CUtensorMap& tk, \
                             const CUtensorMap& tv, const DecodeArgs& a) {                        \
-    GQA_PAGED_CASES(D, launch(grid, st, tk, tv, a))                                              \
+    GQA_PAGED_CASES(D, BF, launch(grid, st, tk, tv, a))                                          \
   }
 
 GQA_DECLARE_UNIT(contig_d64)
 GQA_DECLARE_UNIT(contig_d128)
 GQA_DECLARE_UNIT(paged_d64)
 GQA_DECLARE_UNIT(paged_d128)
+GQA_DECLARE_UNIT(contig_d64_bf16)
+GQA_DECLARE_UNIT(contig_d128_bf16)
+GQA_DECLARE_UNIT(paged_d64_bf16)
+GQA_DECLARE_UNIT(paged_d128_bf16)
 
 }  // namespace gqa

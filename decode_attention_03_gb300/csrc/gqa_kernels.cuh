@@ -11,6 +11,9 @@
 // partition, then a cross-partition merge).
 //
 // CTA layout: kWK*WN consumer warps + 1 producer warp.
+// Q, K, V and O are f16 or bf16 (one instantiation each); scores, softmax statistics,
+// partials and accumulation are fp32.
+//
 //  * producer: TMA 3-D tensor loads (64 columns x rows x the head's 64-column
 //    planes, 128-byte swizzle) of each 64-key K and V tile into a STAGES-deep ring of
 //    shared-memory buffers, signalled through mbarriers (full / empty).  One box
@@ -32,6 +35,7 @@
 //   overlaps the previous one's tail.
 #pragma once
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
 #include <stdint.h>
@@ -143,6 +147,29 @@ __device__ __forceinline__ void raise_timeout(const DecodeArgs& a, volatile int*
   flags[0] = 1;
 }
 
+// Element type of Q, K, V and O: IEEE binary16 (BF16 = false) or bfloat16.  The MMA
+// consumes the raw 16-bit values; only the MMA kind, the packing of P and the output
+// rounding depend on the type.
+template <bool BF16>
+struct Elem {
+  static __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    if constexpr (BF16) ptx::mma_16816_bf16(d, a, b); else ptx::mma_16816(d, a, b);
+  }
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    if constexpr (BF16) return ptx::pack_bf162(lo, hi); else return ptx::pack_half2(lo, hi);
+  }
+  static __device__ __forceinline__ void store(__half* base, int64_t i, float x) {
+    if constexpr (BF16) {
+      reinterpret_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(x);
+    } else {
+      base[i] = __float2half_rn(x);
+    }
+  }
+  static __device__ __forceinline__ void store2(__half* base, int64_t i, float lo, float hi) {
+    reinterpret_cast<uint32_t*>(base + i)[0] = pack(lo, hi);
+  }
+};
+
 // =====================================================================================
 // consumer warp state and per-tile math
 // =====================================================================================
@@ -219,7 +246,7 @@ __device__ __forceinline__ void zero_masked_v(uint8_t* vhead, int ks, int valid,
 
 // One tile: this warp's 16 keys against its 8*NT query rows; kbase / vbase point at
 // the first plane of the warp's head.
-template <int D, int NT, int BOXP, bool CAUSAL = false>
+template <int D, int NT, int BOXP, bool CAUSAL = false, bool BF16 = false>
 __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbase, uint32_t vbase, int valid,
                                              int key0, int ks, int lane, float scale_log2, int rb) {
   constexpr int KD = WarpState<D, NT>::KD;
@@ -240,7 +267,7 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbas
     uint32_t af[4];
     ptx::ldmatrix_x4(af, chunk_addr(kbase, k_off, k_row, kk * 2 + k_c0, plane));
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) ptx::mma_16816(sc[nt], af, st.qf[nt][kk]);
+    for (int nt = 0; nt < NT; ++nt) Elem<BF16>::mma(sc[nt], af, st.qf[nt][kk]);
   }
   // ---- scale (log2 domain), mask, online softmax.  sc[nt][c]: key gq (c<2) or gq+8,
   //      query row 2*tq4 + (c&1) of n-tile nt
@@ -301,8 +328,8 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbas
   uint32_t pf[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    pf[nt][0] = ptx::movmatrix_trans(ptx::pack_half2(sc[nt][0], sc[nt][1]));
-    pf[nt][1] = ptx::movmatrix_trans(ptx::pack_half2(sc[nt][2], sc[nt][3]));
+    pf[nt][0] = ptx::movmatrix_trans(Elem<BF16>::pack(sc[nt][0], sc[nt][1]));
+    pf[nt][1] = ptx::movmatrix_trans(Elem<BF16>::pack(sc[nt][2], sc[nt][3]));
   }
   // ---- O^T += V^T P^T
 #pragma unroll
@@ -310,7 +337,7 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbas
     uint32_t af[4];
     ptx::ldmatrix_x4_trans(af, chunk_addr(vbase, v_off, v_row, i * 2 + v_c0, plane));
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) ptx::mma_16816(st.acc[i][nt], af, pf[nt]);
+    for (int nt = 0; nt < NT; ++nt) Elem<BF16>::mma(st.acc[i][nt], af, pf[nt]);
   }
 }
 
@@ -361,7 +388,7 @@ __device__ __forceinline__ void stash_warp(WarpState<D, NT>& st, float* scratch,
 // slice, partial mode) or this slice's fp32 partial in the workspace.  With HG heads a
 // head has kWK/HG key-slice warps (hh*KS .. hh*KS+KS-1); with one head, warp col*kWK+k
 // holds key slice k of query column col.
-template <int D, int NT, int WN, int STAGES, int HG = 1>
+template <int D, int NT, int WN, int STAGES, int HG = 1, bool BF16 = false>
 __device__ __forceinline__ void emit_slice(const DecodeArgs& a, const float* scratch, int b, int g0, int slice,
                                            bool single, int tid, int nthreads) {
   using C = Cfg<D, NT, WN, STAGES>;
@@ -395,7 +422,7 @@ __device__ __forceinline__ void emit_slice(const DecodeArgs& a, const float* scr
     const int64_t orow = out_row(a, b, g, r);
     if (single) {
       if (a.o != nullptr) {
-        a.o[orow * D + d] = __float2half_rn(L > 0.f ? O / L : 0.f);
+        Elem<BF16>::store(a.o, orow * D + d, L > 0.f ? O / L : 0.f);
       } else {
         if (d == 0) {
           a.m_out[orow] = M * kLn2;
@@ -434,7 +461,7 @@ __device__ __forceinline__ bool last_to_arrive(const DecodeArgs& a, int unit, in
 // write the output (O / l) or the merged partial; resets the unit's counter.  Each
 // thread folds IPT items (4 consecutive d of one row) over chunks of partials whose
 // loads are all issued before the folds.
-template <int D, int NT, int WN, int STAGES>
+template <int D, int NT, int WN, int STAGES, bool BF16 = false>
 __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int g, int unit, int n) {
   using C = Cfg<D, NT, WN, STAGES>;
   constexpr int DQ = D / 4;
@@ -494,9 +521,8 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int g, in
     const int64_t orow = orow_i[i];
     if (a.o != nullptr) {
       const float inv = L[i] > 0.f ? 1.f / L[i] : 0.f;
-      __half2* dst = reinterpret_cast<__half2*>(a.o + orow * D + c4_i[i] * 4);
-      dst[0] = __floats2half2_rn(O[i].x * inv, O[i].y * inv);
-      dst[1] = __floats2half2_rn(O[i].z * inv, O[i].w * inv);
+      Elem<BF16>::store2(a.o, orow * D + c4_i[i] * 4, O[i].x * inv, O[i].y * inv);
+      Elem<BF16>::store2(a.o, orow * D + c4_i[i] * 4 + 2, O[i].z * inv, O[i].w * inv);
     } else {
       if (c4_i[i] == 0) {
         a.m_out[orow] = M[i] * kLn2;
@@ -511,7 +537,7 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int g, in
 // =====================================================================================
 // contiguous K/V: one CTA per (KV head, split, sequence)
 // =====================================================================================
-template <int D, int NT, int WN, int STAGES, bool CAUSAL>
+template <int D, int NT, int WN, int STAGES, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(Cfg<D, NT, WN, STAGES>::THREADS)
 gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const DecodeArgs a) {
@@ -611,7 +637,7 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     if (valid < 16)
       zero_masked_v<C::HALVES, C::HALVES>(smem + s * C::STAGE_BYTES + C::KV_BYTES, ks, valid, lane, kTile);
     if (valid > 0)
-      consume_tile<D, NT, C::HALVES, CAUSAL>(st, kbase, vbase, valid, (int)key0, ks, lane, a.scale_log2, kTile);
+      consume_tile<D, NT, C::HALVES, CAUSAL, BF16>(st, kbase, vbase, valid, (int)key0, ks, lane, a.scale_log2, kTile);
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(empty + s));
   }
@@ -622,10 +648,10 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   stash_warp<D, NT, WN, STAGES>(st, scratch, warp, lane);
   ptx::named_bar_sync(1, C::CTHREADS);
   const bool single = (a.n_splits == 1);
-  emit_slice<D, NT, WN, STAGES>(a, scratch, b, g_kv, split, single, threadIdx.x, C::CTHREADS);
+  emit_slice<D, NT, WN, STAGES, 1, BF16>(a, scratch, b, g_kv, split, single, threadIdx.x, C::CTHREADS);
   if (single || !a.merge_in_kernel) return;
   if (last_to_arrive<C::CTHREADS>(a, unit, a.n_splits, flags))
-    merge_unit<D, NT, WN, STAGES>(a, b, g_kv, unit, a.n_splits);
+    merge_unit<D, NT, WN, STAGES, BF16>(a, b, g_kv, unit, a.n_splits);
 }
 
 // =====================================================================================
@@ -655,7 +681,7 @@ static_assert(sizeof(ItemDesc) == 48, "descriptor slot size");
 //  * epilogue: combines the consumer warps of a finished item and writes the f16
 //    output (one-partition sequences) or the partition's fp32 partial; the partials
 //    are folded by gqa_paged_merge_kernel (the second pass of paged attention v2).
-template <int D, int NT, int WN, int STAGES, int HG>
+template <int D, int NT, int WN, int STAGES, int HG, bool BF16>
 __global__ void __launch_bounds__(Cfg<D, NT, WN, STAGES>::PTHREADS)
 gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const DecodeArgs a) {
@@ -757,7 +783,7 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       const ItemDesc d = edesc[buf];
       if (d.kind == 2) break;
       const float* sb = reinterpret_cast<const float*>(smem + C::PSCRATCH_OFF + buf * C::PSCRATCH_STRIDE);
-      emit_slice<D, NT, WN, STAGES, HG>(a, sb, d.b, d.g, d.p, d.n_parts == 1, lane, 32);
+      emit_slice<D, NT, WN, STAGES, HG, BF16>(a, sb, d.b, d.g, d.p, d.n_parts == 1, lane, 32);
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(sfree + buf));
     }
@@ -925,7 +951,8 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         const int valid = (int)max((int64_t)0, min((int64_t)16, d.key_end - key0));
         if (valid < 16)
           zero_masked_v<C::HALVES, BOXP>(smem + s * C::STAGE_BYTES + C::KV_BYTES + head_off, ks, valid, lane, br);
-        if (valid > 0) consume_tile<D, NT, BOXP>(st, kbase, vbase, valid, (int)key0, ks, lane, a.scale_log2, br);
+        if (valid > 0)
+          consume_tile<D, NT, BOXP, false, BF16>(st, kbase, vbase, valid, (int)key0, ks, lane, a.scale_log2, br);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(empty + s));
       }
@@ -1011,7 +1038,7 @@ __device__ __forceinline__ void fold_row(const float* m, const float* l, const f
 // partition, fold its partitions' partials (page: _merge_running left to right, then
 // O / l) into the f16 output.  One warp per row; rows of one-partition or empty
 // sequences were written by the first pass.
-template <int D>
+template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
 gqa_paged_merge_kernel(const DecodeArgs a) {
   constexpr int PER = D / 32;
@@ -1028,12 +1055,12 @@ gqa_paged_merge_kernel(const DecodeArgs a) {
   fold_row<D>(a.ws_m, a.ws_l, a.ws_o, n, a.R, r, lane, M, L, acc);
   const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-  for (int i = 0; i < PER; ++i) a.o[r * D + lane * PER + i] = __float2half_rn(acc[i] * inv);
+  for (int i = 0; i < PER; ++i) Elem<BF16>::store(a.o, r * D + lane * PER + i, acc[i] * inv);
 }
 
 // Public merge of n_parts partials laid out [n_parts][rows] and
 // [n_parts][rows][D] (natural-log m).  One warp per row.
-template <int D>
+template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
 gqa_merge_kernel(const float* __restrict__ m, const float* __restrict__ l, const float* __restrict__ op,
                  int n_parts, int64_t rows, __half* o, float* m_out, float* l_out, float* o_out) {
@@ -1046,7 +1073,7 @@ gqa_merge_kernel(const float* __restrict__ m, const float* __restrict__ l, const
   if (o != nullptr) {
     const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) o[r * D + lane * PER + i] = __float2half_rn(acc[i] * inv);
+    for (int i = 0; i < PER; ++i) Elem<BF16>::store(o, r * D + lane * PER + i, acc[i] * inv);
   } else {
     if (lane == 0) {
       m_out[r] = M;

@@ -17,6 +17,9 @@ Generator convention (frozen; regression constants live in
   ``standard_normal``/``random``);
 * normals are drawn as float32 and rounded to float16 (round-to-nearest-even);
 * uniforms in ``[lo, hi)`` are float32 ``lo + (hi-lo)*U`` rounded to float16;
+* bfloat16 workloads round the same float32 draws to bfloat16 (nearest even) instead;
+  numpy has no bfloat16, so they are held as their 16-bit patterns (``uint16``) and
+  decoded exactly with :func:`bf16_to_f32`;
 * integer draws (sequence lengths, permutations) use the stream's
   un-chunked generator ``SeedSequence([seed, stream])``.
 
@@ -51,9 +54,21 @@ def _threads() -> int:
     return max(1, min(os.cpu_count() or 1, 32))
 
 
+def f32_to_bf16(a: np.ndarray) -> np.ndarray:
+    """Round finite float32 values to bfloat16, nearest even; returns the bit patterns."""
+    bits = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    rounded = (bits + np.uint32(0x7FFF) + ((bits >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+    return rounded.astype(np.uint16)
+
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact float32 values of bfloat16 bit patterns."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
 def _draw_2d(seed: int, stream: int, rows: int, cols: int, kind: str,
-             lo: float = -1.0, hi: float = 1.0) -> np.ndarray:
-    out = np.empty((rows, cols), dtype=np.float16)
+             lo: float = -1.0, hi: float = 1.0, elem: str = "f16") -> np.ndarray:
+    out = np.empty((rows, cols), dtype=np.float16 if elem == "f16" else np.uint16)
     n_chunks = (rows + CHUNK_ROWS - 1) // CHUNK_ROWS
 
     def one(c: int) -> None:
@@ -68,7 +83,7 @@ def _draw_2d(seed: int, stream: int, rows: int, cols: int, kind: str,
             a += np.float32(lo)
         else:
             raise ValueError(kind)
-        out[r0:r1] = a.astype(np.float16)
+        out[r0:r1] = a.astype(np.float16) if elem == "f16" else f32_to_bf16(a)
 
     if n_chunks <= 1:
         for c in range(n_chunks):
@@ -79,20 +94,22 @@ def _draw_2d(seed: int, stream: int, rows: int, cols: int, kind: str,
     return out
 
 
-def normal_f16(seed: int, stream: int, shape) -> np.ndarray:
-    """N(0,1) float32 draws rounded to float16, shape ``shape``."""
+def normal_f16(seed: int, stream: int, shape, elem: str = "f16") -> np.ndarray:
+    """N(0,1) float32 draws rounded to float16 (or to bfloat16 bit patterns with
+    ``elem='bf16'``), shape ``shape``."""
     shape = tuple(int(s) for s in shape)
     cols = shape[-1]
     rows = int(np.prod(shape[:-1])) if len(shape) > 1 else 1
-    return _draw_2d(seed, stream, rows, cols, "normal").reshape(shape)
+    return _draw_2d(seed, stream, rows, cols, "normal", elem=elem).reshape(shape)
 
 
-def uniform_f16(seed: int, stream: int, shape, lo: float = -1.0, hi: float = 1.0) -> np.ndarray:
-    """Uniform ``[lo, hi)`` float32 draws rounded to float16, shape ``shape``."""
+def uniform_f16(seed: int, stream: int, shape, lo: float = -1.0, hi: float = 1.0, elem: str = "f16") -> np.ndarray:
+    """Uniform ``[lo, hi)`` float32 draws rounded to float16 (or bfloat16 bit patterns),
+    shape ``shape``."""
     shape = tuple(int(s) for s in shape)
     cols = shape[-1]
     rows = int(np.prod(shape[:-1])) if len(shape) > 1 else 1
-    return _draw_2d(seed, stream, rows, cols, "uniform", lo, hi).reshape(shape)
+    return _draw_2d(seed, stream, rows, cols, "uniform", lo, hi, elem=elem).reshape(shape)
 
 
 # ---------------------------------------------------------------------------
@@ -125,6 +142,7 @@ class Workload:
     partition_size: int = 512
     len_lo: int = 0      # paged: inclusive bounds of the per-sequence length
     len_hi: int = 0
+    elem: str = "f16"    # element type of Q, K, V: "f16" or "bf16" (bit patterns)
 
     @property
     def G(self) -> int:
@@ -166,18 +184,22 @@ def custom(batch: int, T_q: int, S_kv: int, h_q: int, h_kv: int, d_head: int, se
 def make_contiguous(w: Workload) -> dict:
     """Q ``(batch, T_q, h_q*d)``, K/V ``(batch, S_kv, h_kv*d)`` float16 arrays."""
     assert w.kind == "contiguous"
-    q = normal_f16(w.seed, S_Q, (w.batch, w.T_q, w.h_q * w.d_head))
-    k = normal_f16(w.seed, S_K, (w.batch, w.S_kv, w.h_kv * w.d_head))
+    e = w.elem
+    q = normal_f16(w.seed, S_Q, (w.batch, w.T_q, w.h_q * w.d_head), e)
+    k = normal_f16(w.seed, S_K, (w.batch, w.S_kv, w.h_kv * w.d_head), e)
     if w.v_dist == "normal":
-        v = normal_f16(w.seed, S_V, (w.batch, w.S_kv, w.h_kv * w.d_head))
+        v = normal_f16(w.seed, S_V, (w.batch, w.S_kv, w.h_kv * w.d_head), e)
     else:
-        v = uniform_f16(w.seed, S_V, (w.batch, w.S_kv, w.h_kv * w.d_head), -1.0, 1.0)
+        v = uniform_f16(w.seed, S_V, (w.batch, w.S_kv, w.h_kv * w.d_head), -1.0, 1.0, e)
     spike_rows = np.zeros((0,), dtype=np.int64)
     if w.spike_frac > 0.0:
         n_spike = int(round(w.spike_frac * w.S_kv))
         spike_rows = _gen(w.seed, S_SPIKE).permutation(w.S_kv)[:n_spike].astype(np.int64)
-        k[:, spike_rows, :] *= np.float16(w.spike_mult)   # x8 is exact in float16
-    return dict(workload=w, q=q, k=k, v=v, spike_rows=spike_rows,
+        if e == "f16":
+            k[:, spike_rows, :] *= np.float16(w.spike_mult)   # x8 is exact in float16
+        else:
+            k[:, spike_rows, :] = f32_to_bf16(bf16_to_f32(k[:, spike_rows, :]) * np.float32(w.spike_mult))
+    return dict(workload=w, q=q, k=k, v=v, spike_rows=spike_rows, elem=e,
                 batch=w.batch, T_q=w.T_q, S_kv=w.S_kv, h_q=w.h_q, h_kv=w.h_kv,
                 d_head=w.d_head, scale=w.scale)
 
@@ -211,19 +233,21 @@ def make_paged(w: Workload, tail_fill: str = "normal") -> dict:
     kernel must not read them into the result.
     """
     lens, tables, num_blocks = paged_layout(w)
-    q = normal_f16(w.seed, S_Q, (w.batch, w.T_q, w.h_q * w.d_head))
-    kp = normal_f16(w.seed, S_K, (num_blocks, w.block_size, w.h_kv * w.d_head))
-    vp = normal_f16(w.seed, S_V, (num_blocks, w.block_size, w.h_kv * w.d_head))
+    e = w.elem
+    q = normal_f16(w.seed, S_Q, (w.batch, w.T_q, w.h_q * w.d_head), e)
+    kp = normal_f16(w.seed, S_K, (num_blocks, w.block_size, w.h_kv * w.d_head), e)
+    vp = normal_f16(w.seed, S_V, (num_blocks, w.block_size, w.h_kv * w.d_head), e)
     if tail_fill == "nan":
+        nan = np.float16(np.nan) if e == "f16" else np.uint16(0x7FC0)
         for b in range(w.batch):
             L = int(lens[b])
             if L % w.block_size:
                 last = tables[b, L // w.block_size]
-                kp[last, L % w.block_size:, :] = np.float16(np.nan)
-                vp[last, L % w.block_size:, :] = np.float16(np.nan)
+                kp[last, L % w.block_size:, :] = nan
+                vp[last, L % w.block_size:, :] = nan
     elif tail_fill != "normal":
         raise ValueError(tail_fill)
-    return dict(workload=w, q=q, k_pool=kp, v_pool=vp, block_tables=tables, seq_lens=lens,
+    return dict(workload=w, q=q, k_pool=kp, v_pool=vp, block_tables=tables, seq_lens=lens, elem=e,
                 num_seqs=w.batch, T_q=w.T_q, h_q=w.h_q, h_kv=w.h_kv, d_head=w.d_head,
                 scale=w.scale, num_blocks=num_blocks, block_size=w.block_size,
                 partition_size=w.partition_size, max_blocks_per_seq=tables.shape[1],
@@ -251,3 +275,8 @@ def kv_bytes(inp: dict) -> int:
     nblk_used = int(((np.asarray(inp["seq_lens"], dtype=np.int64) + inp["block_size"] - 1)
                      // inp["block_size"]).sum())
     return (2 * tokens * row + 2 * inp["q"].nbytes + nblk_used * 4 + inp["seq_lens"].nbytes)
+
+
+def values(a: np.ndarray, elem: str) -> np.ndarray:
+    """Exact float32 values of an input array (float16 as is, bfloat16 bit patterns decoded)."""
+    return a.astype(np.float32) if elem == "f16" else bf16_to_f32(a)

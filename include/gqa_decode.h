@@ -19,7 +19,8 @@
  * 'paged_attention_v2': a per-partition pass plus a cross-partition merge.
  *
  * Conventions for every call
- *  - f16 buffers hold IEEE binary16 values (passed as uint16_t); float buffers are fp32.
+ *  - 16-bit buffers hold IEEE binary16 values (or bfloat16 with gqa_options.bf16), passed as
+ *    uint16_t; float buffers are fp32.
  *  - All tensors are dense row-major, in device memory of the CURRENT CUDA
  *    device, 16-byte aligned.  The caller owns every buffer; the library never
  *    allocates device memory and never synchronises (except gqa_workspace_check).
@@ -70,10 +71,12 @@ typedef struct {
                             sees only the keys j <= S_kv - T_q + t (the T_q new tokens are the last
                             T_q keys); 0 = every token sees all S_kv keys.  No counterpart on the
                             pages (their kernel is stated for T_q = 1). */
+  int bf16;              /* decode, partial and paged calls: q, k, v (and o) hold bfloat16 values
+                            instead of IEEE binary16; arithmetic stays fp32, o is rounded to bf16 */
 } gqa_options;
 
 /* Default options: n_splits 0, merge_mode 0, timeout_us 0, test_stall_cta -1, paged_head_group 0,
- * causal 0. */
+ * causal 0, bf16 0. */
 gqa_options gqa_default_options(void);
 
 /* Static text for a status code. */

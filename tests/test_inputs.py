@@ -56,3 +56,16 @@ def test_workloads_match_stated_shapes():
     assert W["long"].S_kv == 1 << 20 and W["long"].G == 4
     assert (W["ragged"].T_q, W["ragged"].S_kv, W["ragged"].G) == (4, 131071, 8)
     assert W["paged"].block_size == 16 and W["paged"].partition_size == 512
+
+
+def test_bf16_draws_round_the_same_float32_values():
+    # the bfloat16 workload rounds the very float32 draws the float16 workload rounds
+    f32 = gi._gen(7, 1, 0).standard_normal((3, 5), dtype=np.float32)
+    b = gi.normal_f16(7, 1, (3, 5), elem="bf16")
+    assert b.dtype == np.uint16
+    assert np.array_equal(b, gi.f32_to_bf16(f32))
+    back = gi.bf16_to_f32(b)
+    assert np.all(np.abs(back - f32) <= np.abs(f32) * 2.0 ** -8)
+    # round to nearest even on exact ties
+    ties = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8], dtype=np.float32)
+    assert gi.bf16_to_f32(gi.f32_to_bf16(ties)).tolist() == [1.0, 1.0 + 2.0 ** -6]
