@@ -58,6 +58,8 @@ def parse():
                     help="paged workload: KV heads per work item (1, 2, 4; 0 = library default)")
     ap.add_argument("--n-splits", type=int, default=0)
     ap.add_argument("--merge-mode", type=int, default=0)
+    ap.add_argument("--mma-path", type=int, default=0,
+                    help="contiguous workloads: 0 automatic, 1 mma.sync split kernel, 2 tcgen05 kernel")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -197,7 +199,7 @@ def make_step(pkg, w, x, d, out, ws, args):
     if w.kind == "contiguous":
         def step():
             pkg.gqa_decode(d["q"], d["k"], d["v"], w.h_q, w.h_kv, w.scale, out=out, workspace_tensor=ws,
-                           n_splits=args.n_splits, merge_mode=args.merge_mode)
+                           n_splits=args.n_splits, merge_mode=args.merge_mode, mma_path=args.mma_path)
     else:
         q2 = d["q"].reshape(w.batch, -1)
 
@@ -335,10 +337,12 @@ def main():
     out = out.reshape(w.batch, w.T_q, -1) if w.kind == "contiguous" else out.reshape(w.batch, -1)
     if w.kind == "contiguous":
         nbytes = pkg.gqa_decode_workspace_size(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head, args.n_splits)
-        n_splits = args.n_splits or pkg.gqa_decode_num_splits(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head)
+        n_splits, mma_path, contig_launches = pkg.gqa_decode_plan(
+            w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head, n_splits=args.n_splits, merge_mode=args.merge_mode,
+            mma_path=args.mma_path)
     else:
         nbytes = pkg.gqa_paged_workspace_size(w.batch, w.h_q, w.h_kv, w.d_head, x["max_seq_len"], w.partition_size)
-        n_splits = None
+        n_splits, mma_path, contig_launches = None, 0, 0
     ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
     step = make_step(pkg, w, x, d, out, ws, args)
     flush = None if big else torch.empty(int(2 * l2), dtype=torch.uint8, device=dev)
@@ -440,8 +444,10 @@ def main():
     if rank == 0:
         if w.kind == "paged":   # partition pass, plus the merge pass when a sequence spans partitions
             launches_per_step = 2 if int(x["max_seq_len"]) > w.partition_size else 1
+            kernel = "gqa_paged_kernel"
         else:
-            launches_per_step = 1 if (args.merge_mode == 0 or (n_splits or 1) <= 1) else 2
+            launches_per_step = contig_launches
+            kernel = "gqa_tc_kernel" if mma_path == 2 else "gqa_split_kernel"
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
             "warmup": warm, "ms_per_step": round(ms_step, 6), "us_per_step": round(ms_step * 1e3, 3),
@@ -452,7 +458,7 @@ def main():
                                else f"L2 flushed ({2 * l2 >> 20} MiB write) before every timed step, outside events")),
             "roofline": {"bound": "hbm", "achieved": round(per_launch_gbs, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(per_launch_gbs / peak, 4), "traffic": traffic,
-                         "peak_source": peak_src, "kernel": "gqa_split_kernel",
+                         "peak_source": peak_src, "kernel": kernel,
                          "frac_of_nominal_7900": round(per_launch_gbs / NOMINAL_HBM_GBS, 4)},
             "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": steps * launches_per_step, "l2_hot": l2_hot,
             "clocks": clocks.summary(wall0, wall1),

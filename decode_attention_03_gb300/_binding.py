@@ -37,7 +37,8 @@ class GQAError(RuntimeError):
 class gqa_options(ctypes.Structure):
     _fields_ = [("n_splits", ctypes.c_int), ("merge_mode", ctypes.c_int),
                 ("timeout_us", ctypes.c_uint32), ("test_stall_cta", ctypes.c_int),
-                ("paged_head_group", ctypes.c_int), ("causal", ctypes.c_int), ("bf16", ctypes.c_int)]
+                ("paged_head_group", ctypes.c_int), ("causal", ctypes.c_int), ("bf16", ctypes.c_int),
+                ("mma_path", ctypes.c_int)]
 
 
 def _load():
@@ -57,6 +58,7 @@ _SIGS = {
     "gqa_status_string": ([_i], ctypes.c_char_p),
     "gqa_version": ([], _i),
     "gqa_decode_num_splits": ([_i, _i, _i64, _i, _i, _i], _i),
+    "gqa_decode_plan": ([_i, _i, _i64, _i, _i, _i, _opt, _p, _p, _p], _i),
     "gqa_decode_workspace_size": ([_i, _i, _i64, _i, _i, _i, _i], _sz),
     "gqa_paged_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
     "gqa_workspace_init": ([_p, _sz, _p], _i),
@@ -123,13 +125,14 @@ def _f32(t: torch.Tensor, name: str) -> None:
 
 
 def _opts(n_splits=0, merge_mode=0, timeout_us=0, test_stall_cta=-1, paged_head_group=0, causal=False,
-          bf16=False):
+          bf16=False, mma_path=0):
     o = gqa_options()
     o.n_splits, o.merge_mode, o.timeout_us, o.test_stall_cta = int(n_splits), int(merge_mode), int(timeout_us), \
         int(test_stall_cta)
     o.paged_head_group = int(paged_head_group)
     o.causal = 1 if causal else 0
     o.bf16 = 1 if bf16 else 0
+    o.mma_path = int(mma_path)
     return o
 
 
@@ -155,6 +158,17 @@ def workspace(nbytes: int, device=None, stream=None) -> torch.Tensor:
 
 def gqa_decode_num_splits(batch, T_q, S_kv, h_q, h_kv, d_head) -> int:
     return lib.gqa_decode_num_splits(batch, T_q, S_kv, h_q, h_kv, d_head)
+
+
+def gqa_decode_plan(batch, T_q, S_kv, h_q, h_kv, d_head, *, n_splits=0, merge_mode=0, mma_path=0):
+    """(n_splits, mma_path, launches) of a gqa_decode call with these shapes and options on the current
+    device: mma_path 1 = mma.sync split kernel, 2 = tcgen05 kernel; launches 2 with the merge kernel."""
+    opt = _opts(n_splits, merge_mode, mma_path=mma_path)
+    n, path, launches = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    st = lib.gqa_decode_plan(batch, T_q, S_kv, h_q, h_kv, d_head, ctypes.byref(opt), ctypes.byref(n),
+                             ctypes.byref(path), ctypes.byref(launches))
+    _check(st, "gqa_decode_plan")
+    return n.value, path.value, launches.value
 
 
 def gqa_decode_workspace_size(batch, T_q, S_kv, h_q, h_kv, d_head, n_splits=0) -> int:
@@ -190,10 +204,12 @@ def gqa_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, h_q: int, h_kv
                scale: Optional[float] = None, *, out: Optional[torch.Tensor] = None,
                workspace_tensor: Optional[torch.Tensor] = None, stream=None, n_splits: int = 0,
                merge_mode: int = 0, timeout_us: int = 0, test_stall_cta: int = -1,
-               causal: bool = False) -> torch.Tensor:
+               causal: bool = False, mma_path: int = 0) -> torch.Tensor:
     """O = softmax(scale Q K^T) V for GQA decode; q (B, T_q, h_q*D), k/v (B, S_kv, h_kv*D) float16 or
     bfloat16 (all the same; the output has that dtype too).
-    ``causal``: query token t sees keys j <= S_kv - T_q + t only."""
+    ``causal``: query token t sees keys j <= S_kv - T_q + t only.
+    ``mma_path``: 0 automatic, 1 the mma.sync split kernel (G*T_q <= 64), 2 the tcgen05 kernel
+    (G*T_q <= 128)."""
     B, T_q, S, D = _shape_qkv(q, k, v, h_q, h_kv)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if out is None:
@@ -203,7 +219,8 @@ def gqa_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, h_q: int, h_kv
     if nbytes == 0:
         raise GQAError(GQA_ERR_INVALID_ARG, "gqa_decode_workspace_size")
     ws = workspace(nbytes, q.device, stream) if workspace_tensor is None else workspace_tensor
-    opt = _opts(n_splits, merge_mode, timeout_us, test_stall_cta, causal=causal, bf16=q.dtype == torch.bfloat16)
+    opt = _opts(n_splits, merge_mode, timeout_us, test_stall_cta, causal=causal, bf16=q.dtype == torch.bfloat16,
+                mma_path=mma_path)
     st = lib.gqa_decode_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, T_q, S, h_q, h_kv, D, scale,
                            _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(opt))
     _check(st, "gqa_decode")
@@ -212,7 +229,8 @@ def gqa_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, h_q: int, h_kv
 
 def gqa_decode_partial(q, k, v, h_q: int, h_kv: int, s_begin: int, s_len: int, scale: Optional[float] = None, *,
                        m=None, l=None, o_part=None, workspace_tensor=None, stream=None, n_splits: int = 0,
-                       merge_mode: int = 0, causal: bool = False) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+                       merge_mode: int = 0, causal: bool = False,
+                       mma_path: int = 0) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Partial (m, l, O) over keys [s_begin, s_begin+s_len): m, l (B*T_q*h_q) and O (B*T_q*h_q, D) fp32."""
     B, T_q, S, D = _shape_qkv(q, k, v, h_q, h_kv)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
@@ -226,7 +244,7 @@ def gqa_decode_partial(q, k, v, h_q: int, h_kv: int, s_begin: int, s_len: int, s
     if nbytes == 0:
         raise GQAError(GQA_ERR_INVALID_ARG, "gqa_decode_workspace_size")
     ws = workspace(nbytes, dev, stream) if workspace_tensor is None else workspace_tensor
-    opt = _opts(n_splits, merge_mode, causal=causal, bf16=q.dtype == torch.bfloat16)
+    opt = _opts(n_splits, merge_mode, causal=causal, bf16=q.dtype == torch.bfloat16, mma_path=mma_path)
     st = lib.gqa_decode_partial_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(m), _ptr(l), _ptr(o_part), B, T_q, S,
                                    int(s_begin), int(s_len), h_q, h_kv, D, scale, _ptr(ws), ws.numel(),
                                    _stream(stream), ctypes.byref(opt))

@@ -11,6 +11,7 @@
 
 #include "../../include/gqa_decode.h"
 #include "gqa_instances.cuh"
+#include "gqa_tc.cuh"
 
 namespace gqa {
 namespace {
@@ -20,6 +21,11 @@ constexpr size_t kHeaderBytes = 256;        // status word (+ reserved)
 constexpr int kMinTilesPerSplit = 4;        // a split streams at least 4 x 64 keys
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;
 constexpr int kMaxDevices = 64;
+// Automatic merge choice of the tcgen05 kernel: the last CTA of a unit folds the splits
+// itself only while the unit's partials stay below this size; above it one CTA streaming
+// them is latency-bound (128 rows x 19 splits = 1.26 MB took 42 us in-kernel on GB300
+// against a few us for the separate merge kernel spread over the whole GPU).
+constexpr int64_t kInKernelMergeBytes = 256 * 1024;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -39,7 +45,7 @@ bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 struct DevState {
   bool ready = false;
   int sms = 0;
-  int occ[2][4][5][2] = {};    // [d index][row class][kernel: see kernel_slot][bf16] resident CTAs
+  int occ[2][4][7][2] = {};    // [d index][row class][kernel: see kernel_slot][bf16] resident CTAs
                                // per SM, 0 = not prepared
 };
 std::mutex g_mu;
@@ -50,7 +56,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
-// Kernel selector `kind`: 0 contiguous, 1 contiguous with the causal tail, and for the paged
+// Kernel selector `kind`: 0 contiguous, 1 contiguous with the causal tail, 2 / 3 the same two
+// on the tcgen05 kernel (row class 0 stands for its single configuration), and for the paged
 // kernel 100 + its head group (101, 102, 104).
 typedef cudaError_t (*PrepareFn)(int, int, int*);
 typedef cudaError_t (*LaunchFn)(int, int, dim3, cudaStream_t, const CUtensorMap&, const CUtensorMap&,
@@ -65,18 +72,29 @@ const LaunchFn kLaunch[2][2][2] = {{{contig_d64_launch, contig_d64_bf16_launch},
                                    {{paged_d64_launch, paged_d64_bf16_launch},
                                     {paged_d128_launch, paged_d128_bf16_launch}}};
 
+const PrepareFn kTcPrepare[2] = {tc_d64_prepare, tc_d128_prepare};
+typedef cudaError_t (*TcLaunchFn)(int, int, dim3, cudaStream_t, const CUtensorMap&, const CUtensorMap&,
+                                  const DecodeArgs&);
+const TcLaunchFn kTcLaunch[2] = {tc_d64_launch, tc_d128_launch};
+
 cudaError_t prepare_unit(int di, int cls, int kind, int bf16, int* occ) {
+  if (kind == 2 || kind == 3) return kTcPrepare[di](kind - 2, bf16, occ);
   const int paged = kind >= 100;
   return kPrepare[paged][di][bf16](cls, paged ? kind - 100 : kind, occ);
 }
 
 cudaError_t launch_unit(int di, int cls, int kind, int bf16, dim3 grid, cudaStream_t st, const CUtensorMap& tk,
                         const CUtensorMap& tv, const DecodeArgs& a) {
+  if (kind == 2 || kind == 3) return kTcLaunch[di](kind - 2, bf16, grid, st, tk, tv, a);
   const int paged = kind >= 100;
   return kLaunch[paged][di][bf16](cls, paged ? kind - 100 : kind, grid, st, tk, tv, a);
 }
 
-int kernel_slot(int kind) { return kind < 100 ? kind : (kind == 101 ? 2 : (kind == 102 ? 3 : 4)); }
+int kernel_slot(int kind) {
+  if (kind < 2) return kind;
+  if (kind < 100) return kind + 3;   // tcgen05: 5, 6
+  return kind == 101 ? 2 : (kind == 102 ? 3 : 4);
+}
 
 // SM count and resident CTAs per SM of one kernel configuration on the current device
 gqa_status device_info(int di, int cls, int kind, int bf16, int* sms, int* occ) {
@@ -176,18 +194,21 @@ gqa_options defaults() {
   o.paged_head_group = 0;
   o.causal = 0;
   o.bf16 = 0;
+  o.mma_path = 0;
   return o;
 }
 
 struct ContigPlan {
   int di, cls, rows, n_splits;
+  bool tc;                     // the tcgen05 kernel (else the mma.sync split kernel)
   int64_t units, tiles, R;
   Layout lay;
 };
 
 // validation shared by the size query and the calls
+// mma_path: 0 auto (tcgen05 above 64 query rows per KV head), 1 mma.sync, 2 tcgen05
 gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_len, int h_q, int h_kv, int D,
-                       int forced_splits, bool need_device, ContigPlan* p) {
+                       int forced_splits, bool need_device, ContigPlan* p, int mma_path = 0) {
   if (B < 0 || T_q < 1 || h_q < 1 || h_kv < 1 || S_kv < 0 || s_begin < 0 || s_len < 0) return GQA_ERR_INVALID_ARG;
   if (s_begin + s_len > S_kv) return GQA_ERR_INVALID_ARG;
   if (h_q % h_kv != 0 || forced_splits < 0) return GQA_ERR_INVALID_ARG;
@@ -196,8 +217,12 @@ gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_
   p->di = d_index(D);
   p->rows = (h_q / h_kv) * T_q;
   if (p->di < 0) return GQA_ERR_UNSUPPORTED;
-  if ((int64_t)(h_q / h_kv) * T_q > 64) return GQA_ERR_UNSUPPORTED;
-  p->cls = row_class(p->rows);
+  if (mma_path < 0 || mma_path > 2) return GQA_ERR_INVALID_ARG;
+  const int64_t rows = (int64_t)(h_q / h_kv) * T_q;
+  if (rows > kTcRows) return GQA_ERR_UNSUPPORTED;
+  p->tc = mma_path == 2 || (mma_path == 0 && rows > 64);
+  if (!p->tc && rows > 64) return GQA_ERR_UNSUPPORTED;
+  p->cls = p->tc ? 0 : row_class(p->rows);
   p->units = (int64_t)B * h_kv;
   p->tiles = (s_len + kTile - 1) / kTile;
   p->R = (int64_t)B * T_q * h_q;
@@ -208,7 +233,7 @@ gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_
     p->n_splits = (int)n;
   } else if (need_device) {
     int sms = 0, occ = 0;
-    gqa_status s = device_info(p->di, p->cls, 0, 0, &sms, &occ);
+    gqa_status s = device_info(p->di, p->cls, p->tc ? 2 : 0, 0, &sms, &occ);
     if (s != GQA_OK) return s;
     p->n_splits = heuristic_splits(p->units, p->tiles, sms, occ);
   } else {
@@ -232,17 +257,25 @@ gqa_status merge_launch(const float* m, const float* l, const float* op, int n_p
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
+// merge_mode 0 (automatic): in-kernel for the mma.sync kernel, and for the tcgen05 kernel while a
+// unit's partials are at most kInKernelMergeBytes; 1 separate kernel; 2 in-kernel
+bool merge_in_kernel(const ContigPlan& p, int D, int merge_mode) {
+  if (merge_mode == 1) return false;
+  if (merge_mode == 2 || !p.tc) return true;
+  return (int64_t)p.n_splits * p.rows * (D + 2) * 4 <= kInKernelMergeBytes;
+}
+
 gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* m_out,
                        float* l_out, float* op_out, int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_len,
                        int h_q, int h_kv, int D, float scale, void* ws, size_t ws_bytes, void* stream,
                        const gqa_options* opt_in, bool partial) {
   const gqa_options opt = opt_in ? *opt_in : defaults();
-  if (opt.merge_mode < 0 || opt.merge_mode > 1) return GQA_ERR_INVALID_ARG;
+  if (opt.merge_mode < 0 || opt.merge_mode > 2) return GQA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
   if (!partial && S_kv < 1) return GQA_ERR_INVALID_ARG;
   ContigPlan p;
   // shape checks first: they need no device
-  gqa_status s = plan_contig(B, T_q, S_kv, s_begin, s_len, h_q, h_kv, D, 1, false, &p);
+  gqa_status s = plan_contig(B, T_q, S_kv, s_begin, s_len, h_q, h_kv, D, 1, false, &p, opt.mma_path);
   if (s != GQA_OK) return s;
   if (B == 0) return GQA_OK;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(ws)) return GQA_ERR_INVALID_ARG;
@@ -251,19 +284,20 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
   } else if (!aligned16(o)) {
     return GQA_ERR_INVALID_ARG;
   }
-  s = plan_contig(B, T_q, S_kv, s_begin, s_len, h_q, h_kv, D, opt.n_splits, true, &p);
+  s = plan_contig(B, T_q, S_kv, s_begin, s_len, h_q, h_kv, D, opt.n_splits, true, &p, opt.mma_path);
   if (s != GQA_OK) return s;
   if (ws_bytes < p.lay.total) return GQA_ERR_WORKSPACE;
   int sms = 0, occ = 0;
-  const int kind = opt.causal ? 1 : 0;
+  const int kind = (p.tc ? 2 : 0) + (opt.causal ? 1 : 0);
   const int bf16 = opt.bf16 ? 1 : 0;
   s = device_info(p.di, p.cls, kind, bf16, &sms, &occ);
   if (s != GQA_OK) return s;
 
   CUtensorMap tk, tv;
   const uint64_t cols = (uint64_t)h_kv * D, nrows = (uint64_t)B * (uint64_t)S_kv;
-  if ((s = encode_map(&tk, k, cols, nrows, kTile, (uint32_t)D / 64, bf16)) != GQA_OK) return s;
-  if ((s = encode_map(&tv, v, cols, nrows, kTile, (uint32_t)D / 64, bf16)) != GQA_OK) return s;
+  const uint32_t box_rows = p.tc ? kTcKeys : kTile;   // keys per pipeline stage
+  if ((s = encode_map(&tk, k, cols, nrows, box_rows, (uint32_t)D / 64, bf16)) != GQA_OK) return s;
+  if ((s = encode_map(&tv, v, cols, nrows, box_rows, (uint32_t)D / 64, bf16)) != GQA_OK) return s;
 
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   DecodeArgs a;
@@ -291,7 +325,7 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
   a.s_begin = s_begin;
   a.s_len = s_len;
   a.n_splits = p.n_splits;
-  a.merge_in_kernel = opt.merge_mode == 0 ? 1 : 0;
+  a.merge_in_kernel = merge_in_kernel(p, D, opt.merge_mode) ? 1 : 0;
   a.causal = opt.causal ? 1 : 0;
   a.scale_log2 = scale * kLog2e;
   a.timeout_ns = opt.timeout_us ? (uint64_t)opt.timeout_us * 1000ull : kDefaultTimeoutNs;
@@ -438,7 +472,7 @@ const char* gqa_status_string(int status) {
   switch (status) {
     case GQA_OK: return "ok";
     case GQA_ERR_INVALID_ARG: return "invalid argument";
-    case GQA_ERR_UNSUPPORTED: return "unsupported shape (d_head must be 64 or 128, G*T_q <= 64)";
+    case GQA_ERR_UNSUPPORTED: return "unsupported shape (d_head must be 64 or 128, G*T_q <= 128; paged G <= 64)";
     case GQA_ERR_WORKSPACE: return "workspace too small";
     case GQA_ERR_CUDA: return "CUDA error";
     case GQA_ERR_TIMEOUT: return "a device wait timed out";
@@ -456,6 +490,23 @@ int gqa_decode_num_splits(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, i
     return p.n_splits;
   } catch (...) {
     return -1;
+  }
+}
+
+gqa_status gqa_decode_plan(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head, const gqa_options* opt,
+                           int* n_splits, int* mma_path, int* launches) {
+  try {
+    const gqa_options o = opt ? *opt : defaults();
+    if (S_kv < 1 || batch < 1 || o.merge_mode < 0 || o.merge_mode > 2) return GQA_ERR_INVALID_ARG;
+    ContigPlan p;
+    gqa_status s = plan_contig(batch, T_q, S_kv, 0, S_kv, h_q, h_kv, d_head, o.n_splits, true, &p, o.mma_path);
+    if (s != GQA_OK) return s;
+    if (n_splits) *n_splits = p.n_splits;
+    if (mma_path) *mma_path = p.tc ? 2 : 1;
+    if (launches) *launches = (p.n_splits > 1 && !merge_in_kernel(p, d_head, o.merge_mode)) ? 2 : 1;
+    return GQA_OK;
+  } catch (...) {
+    return GQA_ERR_CUDA;
   }
 }
 

@@ -457,15 +457,13 @@ __device__ __forceinline__ bool last_to_arrive(const DecodeArgs& a, int unit, in
   return last;
 }
 
-// Fold the n partials of unit (b, g) (page: _merge_running applied left to right) and
-// write the output (O / l) or the merged partial; resets the unit's counter.  Each
-// thread folds IPT items (4 consecutive d of one row) over chunks of partials whose
-// loads are all issued before the folds.
-template <int D, int NT, int WN, int STAGES, bool BF16 = false>
-__device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int g, int unit, int n) {
-  using C = Cfg<D, NT, WN, STAGES>;
+// Fold the n partials of unit (b, g) (page: _merge_running applied left to right) for the
+// items item0 + threadIdx.x + i * NTH (i < IPT; an item is 4 consecutive d of one query
+// row) and write the output (O / l) or the merged partial.  Partials are read in chunks
+// whose loads are all issued before the folds.
+template <int D, int NTH, int IPT, bool BF16>
+__device__ __forceinline__ void merge_pass(const DecodeArgs& a, int b, int g, int item0, int n) {
   constexpr int DQ = D / 4;
-  constexpr int IPT = (C::WROWS * WN * DQ + C::CTHREADS - 1) / C::CTHREADS;
   const int n_items = a.rows * DQ;
   float M[IPT], L[IPT];
   float4 O[IPT];
@@ -473,7 +471,7 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int g, in
   int c4_i[IPT];
 #pragma unroll
   for (int i = 0; i < IPT; ++i) {
-    const int item = threadIdx.x + i * C::CTHREADS;
+    const int item = item0 + threadIdx.x + i * NTH;
     const int r = item < n_items ? item / DQ : 0;
     c4_i[i] = item < n_items ? item - r * DQ : 0;
     orow_i[i] = out_row(a, b, g, r);
@@ -517,7 +515,7 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int g, in
   }
 #pragma unroll
   for (int i = 0; i < IPT; ++i) {
-    if (threadIdx.x + i * C::CTHREADS >= n_items) continue;
+    if (item0 + threadIdx.x + i * NTH >= n_items) continue;
     const int64_t orow = orow_i[i];
     if (a.o != nullptr) {
       const float inv = L[i] > 0.f ? 1.f / L[i] : 0.f;
@@ -531,6 +529,14 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int g, in
       reinterpret_cast<float4*>(a.o_part_out + orow * D)[c4_i[i]] = O[i];
     }
   }
+}
+
+// The whole unit in one pass (each consumer thread IPT items); resets the unit's counter.
+template <int D, int NT, int WN, int STAGES, bool BF16 = false>
+__device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int g, int unit, int n) {
+  using C = Cfg<D, NT, WN, STAGES>;
+  constexpr int IPT = (C::WROWS * WN * (D / 4) + C::CTHREADS - 1) / C::CTHREADS;
+  merge_pass<D, C::CTHREADS, IPT, BF16>(a, b, g, 0, n);
   if (threadIdx.x == 0) atomicExch(a.counters + unit, 0u);
 }
 

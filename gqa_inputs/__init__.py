@@ -170,6 +170,11 @@ WORKLOADS: Dict[str, Workload] = {
     # V uniform in [-1, 1); seed 4
     "ragged": Workload("ragged", "contiguous", 1, 4, 131071, 64, 8, 128, seed=4,
                        v_dist="uniform", spike_frac=0.01, spike_mult=8.0),
+    # speculative verification of 16 draft tokens (G*T_q = 128 query rows per KV head, the
+    # tcgen05 path): T_q=16, S_kv=262143, h_q=64, h_kv=8; the ragged stress's value
+    # distributions (1% of key rows x8, V uniform in [-1, 1)); seed 5
+    "verify16": Workload("verify16", "contiguous", 1, 16, 262143, 64, 8, 128, seed=5,
+                         v_dist="uniform", spike_frac=0.01, spike_mult=8.0),
 }
 
 

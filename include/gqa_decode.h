@@ -30,8 +30,13 @@
  *  - Launch failures return GQA_ERR_CUDA.  Faults detected on the device (a
  *    bounded wait that gave up, a block id outside the pool) are recorded in
  *    the workspace's status word; gqa_workspace_check reads it.
- *  - Supported: h_q % h_kv == 0, G * T_q <= 64, d_head in {64, 128}
- *    (GQA_ERR_UNSUPPORTED otherwise); no C++ exception crosses this ABI.
+ *  - Supported: h_q % h_kv == 0, d_head in {64, 128}, G * T_q <= 128 for contiguous calls
+ *    and G <= 64 for paged calls (GQA_ERR_UNSUPPORTED otherwise); no C++ exception crosses
+ *    this ABI.
+ *  - Two tensor-core paths compute the same result: the warp-level mma.sync split kernel
+ *    (G * T_q <= 64) and the tcgen05 kernel (single-thread MMAs with fp32 accumulators in
+ *    tensor memory, M = 128 query rows; contiguous calls, G * T_q <= 128), chosen by
+ *    gqa_options.mma_path.
  *  - Scores, softmax statistics, partials and accumulation are fp32; the output
  *    O is rounded to f16 (nearest even).
  */
@@ -57,7 +62,9 @@ typedef enum {
 /* Optional knobs for tests and benchmarks (NULL = defaults everywhere). */
 typedef struct {
   int n_splits;          /* contiguous calls: splits per (sequence, KV head); 0 = heuristic */
-  int merge_mode;        /* 0 = last-arriving CTA merges in the same kernel; 1 = separate merge kernel */
+  int merge_mode;        /* how a unit's splits are folded: 0 = automatic (the last-arriving CTA of the
+                            unit in the same kernel, except for the tcgen05 kernel when a unit's
+                            partials exceed 256 KB), 1 = separate merge kernel, 2 = last-arriving CTA */
   uint32_t timeout_us;   /* limit of every device wait; 0 = 1,000,000 us */
   int test_stall_cta;    /* test hook, -1 = off.  Contiguous calls: linear id (x + X*(y + Y*z)) of
                             one CTA whose producer never loads its second tile; paged calls: the
@@ -73,10 +80,13 @@ typedef struct {
                             pages (their kernel is stated for T_q = 1). */
   int bf16;              /* decode, partial and paged calls: q, k, v (and o) hold bfloat16 values
                             instead of IEEE binary16; arithmetic stays fp32, o is rounded to bf16 */
+  int mma_path;          /* contiguous calls: 0 = automatic (tcgen05 when G * T_q > 64, else mma.sync),
+                            1 = mma.sync split kernel (G * T_q <= 64), 2 = tcgen05 kernel
+                            (G * T_q <= 128).  The workspace size query covers either path. */
 } gqa_options;
 
 /* Default options: n_splits 0, merge_mode 0, timeout_us 0, test_stall_cta -1, paged_head_group 0,
- * causal 0, bf16 0. */
+ * causal 0, bf16 0, mma_path 0. */
 gqa_options gqa_default_options(void);
 
 /* Static text for a status code. */
@@ -88,6 +98,12 @@ int gqa_version(void);
 /* Splits per (sequence, KV head) the heuristic picks on the current device for a contiguous
  * call sweeping S_kv keys; <= 0 on invalid arguments or when no device is usable. */
 int gqa_decode_num_splits(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head);
+
+/* What a gqa_decode_ex call with these shapes and options (NULL = defaults) launches on the current
+ * device: splits per (sequence, KV head), the MMA path (1 mma.sync, 2 tcgen05) and the number of
+ * kernel launches (1, or 2 with the separate merge kernel).  Output pointers may be NULL. */
+gqa_status gqa_decode_plan(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head, const gqa_options* opt,
+                           int* n_splits, int* mma_path, int* launches);
 
 /* Workspace bytes for gqa_decode / gqa_decode_partial on the current device, sweeping S_kv
  * keys (for a partial call pass s_len).  n_splits = 0 sizes for the heuristic; a positive

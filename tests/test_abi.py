@@ -70,8 +70,8 @@ def test_validation_codes_without_gpu(binding):
 
     assert dec(hq=6, hkv=4) == binding.GQA_ERR_INVALID_ARG          # h_q % h_kv != 0
     assert dec(d=96) == binding.GQA_ERR_UNSUPPORTED                 # d_head not in {64, 128}
-    assert dec(hq=65, hkv=1) == binding.GQA_ERR_UNSUPPORTED          # G*T_q > 64
-    assert dec(hq=16, hkv=1, T=5) == binding.GQA_ERR_UNSUPPORTED     # G*T_q = 80
+    assert dec(hq=129, hkv=1) == binding.GQA_ERR_UNSUPPORTED         # G*T_q > 128
+    assert dec(hq=16, hkv=1, T=9) == binding.GQA_ERR_UNSUPPORTED     # G*T_q = 144
     assert dec(S=0) == binding.GQA_ERR_INVALID_ARG                   # no keys
     assert dec(B=-1) == binding.GQA_ERR_INVALID_ARG
     assert dec(T=0) == binding.GQA_ERR_INVALID_ARG
@@ -80,6 +80,15 @@ def test_validation_codes_without_gpu(binding):
     assert dec(B=0) == binding.GQA_OK                                # empty batch: no-op
     assert dec(B=2, S=(1 << 30)) == binding.GQA_ERR_INVALID_ARG      # batch*S_kv >= 2^31
     assert lib.gqa_decode(p, p, p, p, 1, 1, 16, 8, 2, 64, float("nan"), p, 4096, st) == binding.GQA_ERR_INVALID_ARG
+    # the mma.sync path stops at 64 query rows per KV head; the tcgen05 path at 128
+    def dec_path(path, T, hq=16, hkv=1):
+        opt = binding.gqa_options(0, 0, 0, -1, 0, 0, 0, path)
+        return lib.gqa_decode_ex(p, p, p, p, 1, T, 16, hq, hkv, 64, s, p, 1 << 12, st, ctypes.byref(opt))
+
+    assert dec_path(1, 5) == binding.GQA_ERR_UNSUPPORTED             # G*T_q = 80 on mma.sync
+    assert dec_path(2, 9) == binding.GQA_ERR_UNSUPPORTED             # G*T_q = 144
+    assert dec_path(3, 1) == binding.GQA_ERR_INVALID_ARG             # no such path
+    assert dec_path(-1, 1) == binding.GQA_ERR_INVALID_ARG
     # workspace too small (forced split count: sized without a device)
     opt = binding.gqa_options(8, 0, 0, -1, 0, 0)
     need = lib.gqa_decode_workspace_size(1, 1, 4096, 8, 2, 64, 8)
