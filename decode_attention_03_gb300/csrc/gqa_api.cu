@@ -26,6 +26,7 @@ constexpr int kMaxDevices = 64;
 // them is latency-bound (128 rows x 19 splits = 1.26 MB took 42 us in-kernel on GB300
 // against a few us for the separate merge kernel spread over the whole GPU).
 constexpr int64_t kInKernelMergeBytes = 256 * 1024;
+constexpr int kTcMinRows = 16;              // automatic MMA path: tcgen05 from this many rows per KV head
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -220,7 +221,10 @@ gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_
   if (mma_path < 0 || mma_path > 2) return GQA_ERR_INVALID_ARG;
   const int64_t rows = (int64_t)(h_q / h_kv) * T_q;
   if (rows > kTcRows) return GQA_ERR_UNSUPPORTED;
-  p->tc = mma_path == 2 || (mma_path == 0 && rows > 64);
+  // automatic: the tcgen05 kernel from kTcMinRows rows (measured on GB300 at 2^18 keys, 8 KV
+  // heads, d_head 128: 4-8 rows 171-173 us on mma.sync vs 175 us; 16 rows 177-179 vs 175; 32 rows
+  // 193-195 vs 177; 64 rows 451 vs 179)
+  p->tc = mma_path == 2 || (mma_path == 0 && rows >= kTcMinRows);
   if (!p->tc && rows > 64) return GQA_ERR_UNSUPPORTED;
   p->cls = p->tc ? 0 : row_class(p->rows);
   p->units = (int64_t)B * h_kv;
@@ -243,18 +247,35 @@ gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_
   return GQA_OK;
 }
 
+// Launch with programmatic stream serialisation: the kernel may begin launching while the
+// previous kernel in the stream finishes (it waits in griddepcontrol.wait before reading).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 gqa_status merge_launch(const float* m, const float* l, const float* op, int n_parts, int64_t rows, int D,
                         __half* o, float* mo, float* lo, float* oo, cudaStream_t st, int bf16 = 0) {
   if (rows == 0) return GQA_OK;
-  const int warps = 8;
-  const int64_t blocks = (rows + warps - 1) / warps;
+  const int64_t blocks = (rows + kMergeRows - 1) / kMergeRows;
   if (blocks > 2147483647LL) return GQA_ERR_INVALID_ARG;
-  const unsigned g = (unsigned)blocks;
-  if (D == 64 && !bf16) gqa_merge_kernel<64, false><<<g, warps * 32, 0, st>>>(m, l, op, n_parts, rows, o, mo, lo, oo);
-  if (D == 64 && bf16) gqa_merge_kernel<64, true><<<g, warps * 32, 0, st>>>(m, l, op, n_parts, rows, o, mo, lo, oo);
-  if (D == 128 && !bf16) gqa_merge_kernel<128, false><<<g, warps * 32, 0, st>>>(m, l, op, n_parts, rows, o, mo, lo, oo);
-  if (D == 128 && bf16) gqa_merge_kernel<128, true><<<g, warps * 32, 0, st>>>(m, l, op, n_parts, rows, o, mo, lo, oo);
-  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  const unsigned g = (unsigned)blocks, t = kMergeWarps * kMergeRows * 32;
+  cudaError_t e = cudaErrorInvalidValue;
+  if (D == 64 && !bf16) e = launch_pdl(gqa_merge_kernel<64, false>, g, t, st, m, l, op, n_parts, rows, o, mo, lo, oo);
+  if (D == 64 && bf16) e = launch_pdl(gqa_merge_kernel<64, true>, g, t, st, m, l, op, n_parts, rows, o, mo, lo, oo);
+  if (D == 128 && !bf16) e = launch_pdl(gqa_merge_kernel<128, false>, g, t, st, m, l, op, n_parts, rows, o, mo, lo, oo);
+  if (D == 128 && bf16) e = launch_pdl(gqa_merge_kernel<128, true>, g, t, st, m, l, op, n_parts, rows, o, mo, lo, oo);
+  return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
 // merge_mode 0 (automatic): in-kernel for the mma.sync kernel, and for the tcgen05 kernel while a
@@ -448,12 +469,13 @@ gqa_status paged_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t*
       return GQA_ERR_CUDA;
     if (p.max_parts > 1) {
       // second pass: fold the partitions of every multi-partition sequence
-      const unsigned blocks = (unsigned)((a.R + 7) / 8);
-      if (D == 64 && !bf16) gqa_paged_merge_kernel<64, false><<<blocks, 256, 0, st>>>(a);
-      if (D == 64 && bf16) gqa_paged_merge_kernel<64, true><<<blocks, 256, 0, st>>>(a);
-      if (D == 128 && !bf16) gqa_paged_merge_kernel<128, false><<<blocks, 256, 0, st>>>(a);
-      if (D == 128 && bf16) gqa_paged_merge_kernel<128, true><<<blocks, 256, 0, st>>>(a);
-      if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+      const unsigned blocks = (unsigned)((a.R + kMergeRows - 1) / kMergeRows), t = kMergeWarps * kMergeRows * 32;
+      cudaError_t e = cudaErrorInvalidValue;
+      if (D == 64 && !bf16) e = launch_pdl(gqa_paged_merge_kernel<64, false>, blocks, t, st, a);
+      if (D == 64 && bf16) e = launch_pdl(gqa_paged_merge_kernel<64, true>, blocks, t, st, a);
+      if (D == 128 && !bf16) e = launch_pdl(gqa_paged_merge_kernel<128, false>, blocks, t, st, a);
+      if (D == 128 && bf16) e = launch_pdl(gqa_paged_merge_kernel<128, true>, blocks, t, st, a);
+      if (e != cudaSuccess) return GQA_ERR_CUDA;
     }
   }
   return GQA_OK;

@@ -393,6 +393,7 @@ gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     }
 
     // ------------------------------------------------------------ epilogue
+    if (threadIdx.x == 0) ptx::grid_launch_dependents();   // a separate merge kernel may start launching
     // a wait that gave up anywhere -> leave the output alone
     const bool aborted = ptx::named_bar_or(1, C::SOFTMAX_THREADS, flags[0] != 0);
     const int n_mine = n_tiles > wg ? (n_tiles - wg + 1) / 2 : 0;   // tiles of this warpgroup

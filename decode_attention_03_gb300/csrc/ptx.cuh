@@ -184,6 +184,14 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// wait until the grids this one depends on have completed and their writes are visible
+// (a no-op without such a dependency)
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// let a dependent grid launched with programmatic stream serialisation begin launching
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- tcgen05 (5th-generation tensor cores)
 // Tensor memory (TMEM) is allocated by one whole warp; the allocated base address
 // (lane 0, first column) is written to shared memory.  ncols: a power of two >= 32.

@@ -80,7 +80,7 @@ typedef struct {
                             pages (their kernel is stated for T_q = 1). */
   int bf16;              /* decode, partial and paged calls: q, k, v (and o) hold bfloat16 values
                             instead of IEEE binary16; arithmetic stays fp32, o is rounded to bf16 */
-  int mma_path;          /* contiguous calls: 0 = automatic (tcgen05 when G * T_q > 64, else mma.sync),
+  int mma_path;          /* contiguous calls: 0 = automatic (tcgen05 when G * T_q >= 16, else mma.sync),
                             1 = mma.sync split kernel (G * T_q <= 64), 2 = tcgen05 kernel
                             (G * T_q <= 128).  The workspace size query covers either path. */
 } gqa_options;

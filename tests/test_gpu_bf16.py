@@ -64,13 +64,14 @@ def contig(B, T, S, hq, hkv, D, seed, **kw):
 @pytest.mark.parametrize("B,T,S,hq,hkv,D", [(1, 1, 4096, 8, 2, 64), (2, 1, 20000, 32, 8, 128), (1, 4, 9000, 64, 8, 128),
                                             (2, 2, 777, 16, 2, 128), (3, 1, 65, 8, 8, 64)])
 @pytest.mark.parametrize("n_splits", [0, 1, 5])
-def test_bf16_decode(gqa, B, T, S, hq, hkv, D, n_splits):
+@pytest.mark.parametrize("path", [1, 2])
+def test_bf16_decode(gqa, B, T, S, hq, hkv, D, n_splits, path):
     x = contig(B, T, S, hq, hkv, D, 2000 + S + T, v_dist="uniform", spike_frac=0.01, spike_mult=8.0)
     ref = oracle.decode(val(x["q"]), val(x["k"]), val(x["v"]), hq, hkv, D, x["scale"])
-    o = gqa.gqa_decode(dev(x["q"]), dev(x["k"]), dev(x["v"]), hq, hkv, x["scale"], n_splits=n_splits)
+    o = gqa.gqa_decode(dev(x["q"]), dev(x["k"]), dev(x["v"]), hq, hkv, x["scale"], n_splits=n_splits, mma_path=path)
     torch.cuda.synchronize()
     assert o.dtype == torch.bfloat16
-    assert_close(o, ref, f"bf16 B={B} T={T} S={S} hq={hq} hkv={hkv} D={D} splits={n_splits}")
+    assert_close(o, ref, f"bf16 B={B} T={T} S={S} hq={hq} hkv={hkv} D={D} splits={n_splits} path={path}")
 
 
 def test_bf16_causal_and_merge_mode(gqa):

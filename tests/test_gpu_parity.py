@@ -94,6 +94,7 @@ def test_workload_ragged(gqa):
     # spiked keys drive logits to tens: the online rescale and the masked tail tile are exercised
     assert_close(run_contig(gqa, x), ref, "ragged")
     assert_close(run_contig(gqa, x, n_splits=1), ref, "ragged, one split")
+    assert_close(run_contig(gqa, x, mma_path=1), ref, "ragged on the mma.sync kernel")
 
 
 def run_paged(gqa, p, **kw):
@@ -147,11 +148,13 @@ def test_ragged_lengths(gqa, S, D):
 @pytest.mark.parametrize("hq,hkv,T", [(8, 8, 1), (32, 8, 1), (24, 2, 1), (16, 2, 2), (32, 4, 3), (64, 8, 4),
                                       (64, 4, 3), (64, 2, 2), (16, 16, 4)])
 @pytest.mark.parametrize("D", [64, 128])
-def test_row_classes(gqa, hq, hkv, T, D):
+@pytest.mark.parametrize("path", [1, 2])
+def test_row_classes(gqa, hq, hkv, T, D, path):
+    # every row class of the mma.sync kernel (path 1) and the same units on the tcgen05 kernel
     x = gi.make_contiguous(gi.custom(2, T, 777, hq, hkv, D, 300 + hq + T))
     ref = ref_contig(x)
-    assert_close(run_contig(gqa, x), ref, f"hq={hq} hkv={hkv} T={T} D={D}")
-    assert_close(run_contig(gqa, x, n_splits=3), ref, f"hq={hq} hkv={hkv} T={T} D={D} 3 splits")
+    assert_close(run_contig(gqa, x, mma_path=path), ref, f"hq={hq} hkv={hkv} T={T} D={D} path={path}")
+    assert_close(run_contig(gqa, x, n_splits=3, mma_path=path), ref, f"hq={hq} hkv={hkv} T={T} D={D} 3 splits")
 
 
 def test_constant_scores_and_shift(gqa):
@@ -335,11 +338,12 @@ def test_paged_timeout_is_reported_not_hung(gqa):
 @pytest.mark.parametrize("hq,hkv,T,S,D", [(32, 8, 4, 5000, 128), (64, 8, 4, 20000, 128), (16, 16, 3, 777, 64),
                                           (8, 2, 2, 64, 128), (32, 4, 8, 3000, 128), (16, 2, 4, 5, 64)])
 @pytest.mark.parametrize("n_splits", [0, 1, 7])
-def test_causal_tail(gqa, hq, hkv, T, S, D, n_splits):
+@pytest.mark.parametrize("path", [1, 2])
+def test_causal_tail(gqa, hq, hkv, T, S, D, n_splits, path):
     x = gi.make_contiguous(gi.custom(2, T, S, hq, hkv, D, 1300 + S + T))
     ref = oracle.decode(x["q"], x["k"], x["v"], hq, hkv, D, x["scale"], causal=True)
-    o = run_contig(gqa, x, causal=True, n_splits=n_splits)
-    assert_close(o, ref, f"causal hq={hq} hkv={hkv} T={T} S={S} D={D} splits={n_splits}")
+    o = run_contig(gqa, x, causal=True, n_splits=n_splits, mma_path=path)
+    assert_close(o, ref, f"causal hq={hq} hkv={hkv} T={T} S={S} D={D} splits={n_splits} path={path}")
 
 
 def test_causal_partial_with_empty_rows(gqa):

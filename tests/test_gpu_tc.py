@@ -175,8 +175,11 @@ def test_plan_query(gqa):
     n, path, launches = gqa.gqa_decode_plan(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head)
     assert path == 2 and n > 1 and launches == 2          # 128 rows: tcgen05, partials too big to fold in-kernel
     assert gqa.gqa_decode_plan(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head, merge_mode=2)[2] == 1
-    w = gi.WORKLOADS["ragged"]
+    w = gi.WORKLOADS["ragged"]                          # 32 rows: tcgen05 automatically
+    n, path, launches = gqa.gqa_decode_plan(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head)
+    assert path == 2
+    assert gqa.gqa_decode_plan(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head, mma_path=1) == (n, 1, 1)
+    w = gi.WORKLOADS["llama8b"]                         # 4 rows: mma.sync, in-kernel merge
     n, path, launches = gqa.gqa_decode_plan(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head)
     assert path == 1 and launches == 1
-    assert gqa.gqa_decode_plan(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head, mma_path=2)[1] == 2
     assert gqa.gqa_decode_plan(1, 1, 100, 8, 2, 64, n_splits=1) == (1, 1, 1)
