@@ -98,23 +98,36 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+# device-code files that define each timed kernel (its template instantiations, the shared
+# kernel helpers and the PTX wrappers); a traffic record is valid while these are unchanged
+KERNEL_SOURCES = {
+    "gqa_split_kernel": ["gqa_kernels.cuh", "gqa_instances.cuh", "ptx.cuh", "gqa_contig_*.cu"],
+    "gqa_paged_kernel": ["gqa_kernels.cuh", "gqa_instances.cuh", "ptx.cuh", "gqa_paged_*.cu"],
+    "gqa_tc_kernel": ["gqa_kernels.cuh", "gqa_tc.cuh", "ptx.cuh", "gqa_tc_*.cu"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "decode_attention_03_gb300", "csrc", "*"))):
+    files = set()
+    for pat in KERNEL_SOURCES[kernel]:
+        files.update(glob.glob(os.path.join(ROOT, "decode_attention_03_gb300", "csrc", pat)))
+    for p in sorted(files):
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current source of
+    the kernel that dominates the step."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d.get(workload)
-        if e and e.get("source_hash") == kernel_source_hash():
+        if e and e.get("kernel") == kernel and e.get("source_hash") == kernel_source_hash(kernel):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -429,7 +442,6 @@ def main():
     value = job_throughput(bytes_step, steps, world, t_max)
     per_launch_gbs = bytes_step / (ms_step * 1e-3) / 1e9
     peak, peak_src = measured_peak()
-    traffic = recorded_traffic(w.name)
 
     # ---- end to end: pinned host inputs -> device, decode, output -> host, every step
     e2e = None
@@ -448,6 +460,7 @@ def main():
         else:
             launches_per_step = contig_launches
             kernel = "gqa_tc_kernel" if mma_path == 2 else "gqa_split_kernel"
+        traffic = recorded_traffic(w.name, kernel)
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
             "warmup": warm, "ms_per_step": round(ms_step, 6), "us_per_step": round(ms_step * 1e3, 3),
