@@ -56,6 +56,8 @@ def parse():
                     help="paged workload: override the KV block size")
     ap.add_argument("--head-group", type=int, default=0,
                     help="paged workload: KV heads per work item (1, 2, 4; 0 = library default)")
+    ap.add_argument("--partition-size", type=int, default=-1,
+                    help="paged workloads: override the partition size (0 = automatic v1 / v2)")
     ap.add_argument("--n-splits", type=int, default=0)
     ap.add_argument("--merge-mode", type=int, default=0)
     ap.add_argument("--mma-path", type=int, default=0,
@@ -192,9 +194,11 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------------------------
-def load_inputs(name: str, s_kv: int = 0, block_size: int = 0):
+def load_inputs(name: str, s_kv: int = 0, block_size: int = 0, partition_size: int = -1):
     import dataclasses
     w = gi.WORKLOADS[name]
+    if partition_size >= 0 and w.kind == "paged" and partition_size != w.partition_size:
+        w = dataclasses.replace(w, name=f"{w.name}[partition={partition_size}]", partition_size=int(partition_size))
     if s_kv and w.kind == "contiguous" and s_kv != w.S_kv:
         w = dataclasses.replace(w, name=f"{w.name}[S_kv={s_kv}]", S_kv=int(s_kv))
     if block_size and w.kind == "paged" and block_size != w.block_size:
@@ -215,11 +219,12 @@ def make_step(pkg, w, x, d, out, ws, args):
                            n_splits=args.n_splits, merge_mode=args.merge_mode, mma_path=args.mma_path)
     else:
         q2 = d["q"].reshape(w.batch, -1)
+        fn = pkg.gqa_decode_paged_vllm if w.layout == "vllm" else pkg.gqa_decode_paged
 
         def step():
-            pkg.gqa_decode_paged(q2, d["k_pool"], d["v_pool"], d["block_tables"], d["seq_lens"], w.h_q, w.h_kv,
-                                 w.scale, max_seq_len=x["max_seq_len"], partition_size=w.partition_size,
-                                 out=out, workspace_tensor=ws, head_group=args.head_group)
+            fn(q2, d["k_pool"], d["v_pool"], d["block_tables"], d["seq_lens"], w.h_q, w.h_kv,
+               w.scale, max_seq_len=x["max_seq_len"], partition_size=w.partition_size,
+               out=out, workspace_tensor=ws, head_group=args.head_group)
     return step
 
 
@@ -281,7 +286,7 @@ def run_reference(args, rank, world):
     """The oracle as the reference arm: host cores, bounded samples, the same metric."""
     if rank != 0:
         return 0
-    w, x = load_inputs(args.workload, args.s_kv, args.block_size)
+    w, x = load_inputs(args.workload, args.s_kv, args.block_size, args.partition_size)
     steps = args.steps if args.steps is not None else 5
     warm = args.warmup if args.warmup is not None else 1
     per_step = max(0.2, min(10.0, 150.0 / max(1, steps + warm)))
@@ -340,7 +345,7 @@ def main():
     _b.build()
     import decode_attention_03_gb300 as pkg
 
-    w, x = load_inputs(args.workload, args.s_kv, args.block_size)
+    w, x = load_inputs(args.workload, args.s_kv, args.block_size, args.partition_size)
     d = to_device(x, dev)
     bytes_step = gi.kv_bytes(x)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -455,7 +460,10 @@ def main():
 
     if rank == 0:
         if w.kind == "paged":   # partition pass, plus the merge pass when a sequence spans partitions
-            launches_per_step = 2 if int(x["max_seq_len"]) > w.partition_size else 1
+            part, hg, launches_per_step = pkg.gqa_paged_plan(w.batch, w.h_q, w.h_kv, w.d_head, int(x["max_seq_len"]),
+                                                             w.partition_size, block_size=w.block_size,
+                                                             vllm_layout=w.layout == "vllm",
+                                                             head_group=args.head_group)
             kernel = "gqa_paged_kernel"
         else:
             launches_per_step = contig_launches

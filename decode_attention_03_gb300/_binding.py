@@ -59,6 +59,7 @@ _SIGS = {
     "gqa_version": ([], _i),
     "gqa_decode_num_splits": ([_i, _i, _i64, _i, _i, _i], _i),
     "gqa_decode_plan": ([_i, _i, _i64, _i, _i, _i, _opt, _p, _p, _p], _i),
+    "gqa_paged_plan": ([_i, _i, _i, _i, _i, _i, _i, _i, _opt, _p, _p, _p], _i),
     "gqa_decode_workspace_size": ([_i, _i, _i64, _i, _i, _i, _i], _sz),
     "gqa_paged_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
     "gqa_workspace_init": ([_p, _sz, _p], _i),
@@ -74,6 +75,9 @@ _SIGS = {
     "gqa_decode_paged_ex": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p, _opt],
                             _i),
     "gqa_decode_noalloc": ([_p, _p, _p, _p, _i, _i, _i64, _i, _i, _i, _f, _p], _i),
+    "gqa_decode_paged_vllm": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p], _i),
+    "gqa_decode_paged_vllm_ex": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p,
+                                  _opt], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -158,6 +162,19 @@ def workspace(nbytes: int, device=None, stream=None) -> torch.Tensor:
 
 def gqa_decode_num_splits(batch, T_q, S_kv, h_q, h_kv, d_head) -> int:
     return lib.gqa_decode_num_splits(batch, T_q, S_kv, h_q, h_kv, d_head)
+
+
+def gqa_paged_plan(num_seqs, h_q, h_kv, d_head, max_seq_len, partition_size=0, *, block_size=16,
+                   vllm_layout=False, head_group=0):
+    """(partition_size, head_group, launches) a paged call with these shapes makes on the current device
+    (partition_size 0 resolved to the automatic choice)."""
+    opt = _opts(0, 0, paged_head_group=head_group)
+    part, hg, launches = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    st = lib.gqa_paged_plan(num_seqs, h_q, h_kv, d_head, int(block_size), int(max_seq_len), int(partition_size),
+                            1 if vllm_layout else 0, ctypes.byref(opt), ctypes.byref(part), ctypes.byref(hg),
+                            ctypes.byref(launches))
+    _check(st, "gqa_paged_plan")
+    return part.value, hg.value, launches.value
 
 
 def gqa_decode_plan(batch, T_q, S_kv, h_q, h_kv, d_head, *, n_splits=0, merge_mode=0, mma_path=0):
@@ -306,6 +323,43 @@ def gqa_decode_paged(q, k_pool, v_pool, block_tables, seq_lens, h_q: int, h_kv: 
                                  h_q, h_kv, D, scale, int(max_seq_len), _ptr(ws), ws.numel(), _stream(stream),
                                  ctypes.byref(opt))
     _check(st, "gqa_decode_paged")
+    return out
+
+
+def gqa_decode_paged_vllm(q, k_cache, v_cache, block_tables, seq_lens, h_q: int, h_kv: int,
+                          scale: Optional[float] = None, *, max_seq_len: int, partition_size: int = 0, out=None,
+                          workspace_tensor=None, stream=None, timeout_us: int = 0, test_stall_cta: int = -1,
+                          head_group: int = 0) -> torch.Tensor:
+    """Paged decode over vLLM's cache layout, read in place: q (N, h_q*D); k_cache
+    (num_blocks, h_kv, D/8, block_size, 8), v_cache (num_blocks, h_kv, D, block_size), float16 or
+    bfloat16; tables (N, max_blocks) int32.  partition_size 0: automatic (512-token partitions);
+    partition_size >= max_seq_len: single pass (one launch)."""
+    _h16(q, "q"), _h16(k_cache, "k_cache", q.dtype), _h16(v_cache, "v_cache", q.dtype)
+    if not (block_tables.is_cuda and block_tables.dtype == torch.int32 and block_tables.is_contiguous()):
+        raise ValueError("block_tables must be a contiguous int32 CUDA tensor")
+    if not (seq_lens.is_cuda and seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()):
+        raise ValueError("seq_lens must be a contiguous int32 CUDA tensor")
+    q2 = q.reshape(q.shape[0], -1)
+    N, qc = q2.shape
+    if k_cache.dim() != 5 or k_cache.shape[4] != 8 or v_cache.dim() != 4:
+        raise ValueError("k_cache must be (num_blocks, h_kv, D/8, block_size, 8), v_cache (num_blocks, h_kv, D, block_size)")
+    num_blocks, hk, d8, block_size, _ = k_cache.shape
+    D = d8 * 8
+    if hk != h_kv or qc != h_q * D or tuple(v_cache.shape) != (num_blocks, h_kv, D, block_size):
+        raise ValueError("inconsistent head sizes")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    out = torch.empty_like(q2) if out is None else out
+    _h16(out, "out", q.dtype)
+    nbytes = gqa_paged_workspace_size(N, h_q, h_kv, D, max_seq_len, partition_size)
+    if nbytes == 0:
+        raise GQAError(GQA_ERR_INVALID_ARG, "gqa_paged_workspace_size")
+    ws = workspace(nbytes, q.device, stream) if workspace_tensor is None else workspace_tensor
+    opt = _opts(0, 0, timeout_us, test_stall_cta, head_group, bf16=q.dtype == torch.bfloat16)
+    st = lib.gqa_decode_paged_vllm_ex(_ptr(q2), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(seq_lens),
+                                      _ptr(out), N, block_tables.shape[1], num_blocks, block_size, partition_size,
+                                      h_q, h_kv, D, scale, int(max_seq_len), _ptr(ws), ws.numel(), _stream(stream),
+                                      ctypes.byref(opt))
+    _check(st, "gqa_decode_paged_vllm")
     return out
 
 

@@ -27,6 +27,16 @@ constexpr int kMaxDevices = 64;
 // against a few us for the separate merge kernel spread over the whole GPU).
 constexpr int64_t kInKernelMergeBytes = 256 * 1024;
 constexpr int kTcMinRows = 16;              // automatic MMA path: tcgen05 from this many rows per KV head
+// Paged partitions chosen automatically (partition_size 0).  Page "muh_kernel_map.py" picks v1 --
+// one pass over each whole sequence, no merge pass -- for seq_len <= 8192 and v2 with 512-token
+// partitions above.  On GB300 the persistent kernel with 512-token partitions (and the merge pass
+// launched as a programmatic dependent) measured at least as fast as v1 on every batch tried
+// (vLLM layout, block 16, h_q 32, h_kv 8, d 128; us, v1 / v2-512: 384 seqs of 128-2048 keys
+// 398 / 354; 1024 seqs 797 / 787; 2048 seqs 1618 / 1616; 512 seqs of 2048-8192 keys 1886 / 1637;
+// 1024 seqs of 1024-8192 keys 3112 / 2945): a v1 item is a whole sequence, and whichever SMs take
+// the longest ones finish last.  So the automatic choice is v2; v1 is a partition_size of at
+// least max_seq_len.
+constexpr int kV2Partition = 512;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -46,7 +56,7 @@ bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 struct DevState {
   bool ready = false;
   int sms = 0;
-  int occ[2][4][7][2] = {};    // [d index][row class][kernel: see kernel_slot][bf16] resident CTAs
+  int occ[2][4][10][2] = {};   // [d index][row class][kernel: see kernel_slot][bf16] resident CTAs
                                // per SM, 0 = not prepared
 };
 std::mutex g_mu;
@@ -59,19 +69,24 @@ EncodeTiledFn g_encode = nullptr;
 
 // Kernel selector `kind`: 0 contiguous, 1 contiguous with the causal tail, 2 / 3 the same two
 // on the tcgen05 kernel (row class 0 stands for its single configuration), and for the paged
-// kernel 100 + its head group (101, 102, 104).
+// kernel 100 + its head group (101, 102, 104) over the row-layout pool, 200 + its head group over
+// the vLLM cache layout.
 typedef cudaError_t (*PrepareFn)(int, int, int*);
 typedef cudaError_t (*LaunchFn)(int, int, dim3, cudaStream_t, const CUtensorMap&, const CUtensorMap&,
                                 const DecodeArgs&);
-// [paged][d index][bf16]
-const PrepareFn kPrepare[2][2][2] = {{{contig_d64_prepare, contig_d64_bf16_prepare},
+// [contiguous / paged / paged over the vLLM layout][d index][bf16]
+const PrepareFn kPrepare[3][2][2] = {{{contig_d64_prepare, contig_d64_bf16_prepare},
                                       {contig_d128_prepare, contig_d128_bf16_prepare}},
                                      {{paged_d64_prepare, paged_d64_bf16_prepare},
-                                      {paged_d128_prepare, paged_d128_bf16_prepare}}};
-const LaunchFn kLaunch[2][2][2] = {{{contig_d64_launch, contig_d64_bf16_launch},
+                                      {paged_d128_prepare, paged_d128_bf16_prepare}},
+                                     {{paged_vllm_d64_prepare, paged_vllm_d64_bf16_prepare},
+                                      {paged_vllm_d128_prepare, paged_vllm_d128_bf16_prepare}}};
+const LaunchFn kLaunch[3][2][2] = {{{contig_d64_launch, contig_d64_bf16_launch},
                                     {contig_d128_launch, contig_d128_bf16_launch}},
                                    {{paged_d64_launch, paged_d64_bf16_launch},
-                                    {paged_d128_launch, paged_d128_bf16_launch}}};
+                                    {paged_d128_launch, paged_d128_bf16_launch}},
+                                   {{paged_vllm_d64_launch, paged_vllm_d64_bf16_launch},
+                                    {paged_vllm_d128_launch, paged_vllm_d128_bf16_launch}}};
 
 const PrepareFn kTcPrepare[2] = {tc_d64_prepare, tc_d128_prepare};
 typedef cudaError_t (*TcLaunchFn)(int, int, dim3, cudaStream_t, const CUtensorMap&, const CUtensorMap&,
@@ -80,21 +95,22 @@ const TcLaunchFn kTcLaunch[2] = {tc_d64_launch, tc_d128_launch};
 
 cudaError_t prepare_unit(int di, int cls, int kind, int bf16, int* occ) {
   if (kind == 2 || kind == 3) return kTcPrepare[di](kind - 2, bf16, occ);
-  const int paged = kind >= 100;
-  return kPrepare[paged][di][bf16](cls, paged ? kind - 100 : kind, occ);
+  const int family = kind / 100;   // 0 contiguous, 1 paged, 2 paged over the vLLM layout
+  return kPrepare[family][di][bf16](cls, kind - 100 * family, occ);
 }
 
 cudaError_t launch_unit(int di, int cls, int kind, int bf16, dim3 grid, cudaStream_t st, const CUtensorMap& tk,
                         const CUtensorMap& tv, const DecodeArgs& a) {
   if (kind == 2 || kind == 3) return kTcLaunch[di](kind - 2, bf16, grid, st, tk, tv, a);
-  const int paged = kind >= 100;
-  return kLaunch[paged][di][bf16](cls, paged ? kind - 100 : kind, grid, st, tk, tv, a);
+  const int family = kind / 100;   // 0 contiguous, 1 paged, 2 paged over the vLLM layout
+  return kLaunch[family][di][bf16](cls, kind - 100 * family, grid, st, tk, tv, a);
 }
 
 int kernel_slot(int kind) {
   if (kind < 2) return kind;
   if (kind < 100) return kind + 3;   // tcgen05: 5, 6
-  return kind == 101 ? 2 : (kind == 102 ? 3 : 4);
+  const int hg_slot = (kind % 100) == 1 ? 0 : ((kind % 100) == 2 ? 1 : 2);
+  return (kind < 200 ? 2 : 7) + hg_slot;   // paged: 2-4, vLLM layout: 7-9
 }
 
 // SM count and resident CTAs per SM of one kernel configuration on the current device
@@ -141,6 +157,43 @@ gqa_status encode_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_
                         const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GQA_OK : GQA_ERR_CUDA;
+}
+
+// vLLM caches, one TMA box per (block, group of hg KV heads) -- a contiguous stretch of both
+// caches -- moved in 128-byte rows:
+//  * key cache [num_blocks, h_kv, D/8, block_size, 8] as the 4-D tensor (64 elements = 8 keys of
+//    one 8-column chunk, block_size/8 key groups, D/8 chunks, num_blocks*h_kv heads); the box
+//    {64, block/8, D/8, hg} lands as [chunks][keys][16 B], no swizzle;
+//  * value cache [num_blocks, h_kv, D, block_size] as the 3-D tensor (64 elements, D*block/64
+//    rows, num_blocks*h_kv heads); the box {64, D*block/64, hg} lands as [D rows][block keys]
+//    with the 128-byte swizzle.
+gqa_status encode_vllm_k(CUtensorMap* map, const void* base, uint64_t num_blocks, int h_kv, int D, int block_size,
+                         uint32_t hg, int bf16) {
+  cuuint64_t dims[4] = {64, (cuuint64_t)block_size / 8, (cuuint64_t)D / 8, num_blocks * (uint64_t)h_kv};
+  cuuint64_t strides[3] = {128, (cuuint64_t)block_size * 16, (cuuint64_t)D * block_size * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)block_size / 8, (cuuint32_t)D / 8, hg};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  if (dims[3] == 0) dims[3] = 1;
+  CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GQA_OK : GQA_ERR_CUDA;
+}
+
+gqa_status encode_vllm_v(CUtensorMap* map, const void* base, uint64_t num_blocks, int h_kv, int D, int block_size,
+                         uint32_t hg, int bf16) {
+  const uint64_t rows = (uint64_t)D * block_size / 64;
+  cuuint64_t dims[3] = {64, rows, num_blocks * (uint64_t)h_kv};
+  cuuint64_t strides[2] = {128, (cuuint64_t)D * block_size * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, hg};
+  cuuint32_t estr[3] = {1, 1, 1};
+  if (dims[2] == 0) dims[2] = 1;
+  CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GQA_OK : GQA_ERR_CUDA;
 }
 
@@ -367,8 +420,10 @@ struct PagedPlan {
   Layout lay;
 };
 
+// partition_size 0: automatic (kV2Partition)
 gqa_status plan_paged(int N, int h_q, int h_kv, int D, int max_seq_len, int partition_size, PagedPlan* p) {
-  if (N < 0 || h_q < 1 || h_kv < 1 || max_seq_len < 0 || partition_size <= 0) return GQA_ERR_INVALID_ARG;
+  if (partition_size == 0) partition_size = kV2Partition;
+  if (N < 0 || h_q < 1 || h_kv < 1 || max_seq_len < 0 || partition_size < 0) return GQA_ERR_INVALID_ARG;
   if (h_q % h_kv != 0 || N > 65535 || h_kv > 65535) return GQA_ERR_INVALID_ARG;
   if (partition_size % kTile != 0) return GQA_ERR_INVALID_ARG;
   p->di = d_index(D);
@@ -387,10 +442,34 @@ gqa_status plan_paged(int N, int h_q, int h_kv, int D, int max_seq_len, int part
   return GQA_OK;
 }
 
+// Head group and partition size of a paged call, and the SMs / resident CTAs of its kernel.
+//  * head group: one item (and one TMA box) covers hg KV heads; larger boxes move the small
+//    16-token blocks at full bandwidth.  Needs a single query column (G <= 16).
+//  * partition_size 0: automatic (kV2Partition); `p` was planned with it.
+gqa_status choose_paged(PagedPlan& p, int N, int h_q, int h_kv, int D, int max_seq_len, int block_size,
+                        const gqa_options& opt, bool vllm, int* partition_size, int* hg_out, int* sms, int* occ) {
+  // over the vLLM layout a TMA box holds whole blocks, so a tile (64 / hg keys) spans at least one
+  const int hg_max = vllm ? std::min(4, 64 / block_size) : 4;
+  int hg = opt.paged_head_group;
+  if (hg == 0) {
+    hg = p.cls <= 1 ? (h_kv % 4 == 0 ? 4 : (h_kv % 2 == 0 ? 2 : 1)) : 1;
+    while (hg > hg_max) hg /= 2;
+    while (h_kv % hg != 0) hg /= 2;
+  }
+  if (!(hg == 1 || hg == 2 || hg == 4) || h_kv % hg != 0 || (hg > 1 && p.cls > 1) || hg > hg_max)
+    return GQA_ERR_INVALID_ARG;
+  gqa_status s = device_info(p.di, p.cls, (vllm ? 200 : 100) + hg, opt.bf16 ? 1 : 0, sms, occ);
+  if (s != GQA_OK) return s;
+  if (*partition_size == 0) *partition_size = kV2Partition;
+  *hg_out = hg;
+  return GQA_OK;
+}
+
+// vllm: k_pool / v_pool are the vLLM caches ([blocks, h_kv, D/8, block, 8] and [blocks, h_kv, D, block])
 gqa_status paged_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool, const int32_t* tables,
                       const int32_t* lens, uint16_t* o, int N, int max_blocks, int num_blocks, int block_size,
                       int partition_size, int h_q, int h_kv, int D, float scale, int max_seq_len, void* ws,
-                      size_t ws_bytes, void* stream, const gqa_options* opt_in) {
+                      size_t ws_bytes, void* stream, const gqa_options* opt_in, bool vllm) {
   const gqa_options opt = opt_in ? *opt_in : defaults();
   if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
   PagedPlan p;
@@ -399,6 +478,7 @@ gqa_status paged_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t*
   if (!(block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64)) return GQA_ERR_INVALID_ARG;
   // at most kMaxBoxesPerPart TMA boxes per partition; a box holds min(block_size, 16..64) rows
   if (partition_size / std::min(block_size, 16) > kMaxBoxesPerPart) return GQA_ERR_INVALID_ARG;
+  if (vllm && (int64_t)num_blocks * h_kv * (D / 8) >= (int64_t(1) << 31)) return GQA_ERR_INVALID_ARG;
   if (max_blocks < 1 || num_blocks < 0) return GQA_ERR_INVALID_ARG;
   if ((int64_t)max_blocks * block_size >= (int64_t(1) << 31)) return GQA_ERR_INVALID_ARG;
   if ((int64_t)num_blocks * block_size >= (int64_t(1) << 31)) return GQA_ERR_INVALID_ARG;
@@ -408,22 +488,24 @@ gqa_status paged_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t*
       (reinterpret_cast<uintptr_t>(lens) & 3u))
     return GQA_ERR_INVALID_ARG;
   if (ws_bytes < p.lay.total) return GQA_ERR_WORKSPACE;
-  // head group: one item (and one TMA box) covers hg KV heads; larger boxes move the
-  // small 16-token blocks at full bandwidth.  Needs a single query column (G <= 16).
-  int hg = opt.paged_head_group;
-  if (hg == 0) hg = p.cls <= 1 ? (h_kv % 4 == 0 ? 4 : (h_kv % 2 == 0 ? 2 : 1)) : 1;
-  if (!(hg == 1 || hg == 2 || hg == 4) || h_kv % hg != 0 || (hg > 1 && p.cls > 1)) return GQA_ERR_INVALID_ARG;
-  int sms = 0, occ = 0;
+  int hg = 0, sms = 0, occ = 0;
   const int bf16 = opt.bf16 ? 1 : 0;
-  s = device_info(p.di, p.cls, 100 + hg, bf16, &sms, &occ);
-  if (s != GQA_OK) return s;
+  if ((s = choose_paged(p, N, h_q, h_kv, D, max_seq_len, block_size, opt, vllm, &partition_size, &hg, &sms,
+                        &occ)) != GQA_OK)
+    return s;
+  const int kind = (vllm ? 200 : 100) + hg;
 
   CUtensorMap tk, tv;
-  const uint64_t cols = (uint64_t)h_kv * D, nrows = (uint64_t)num_blocks * block_size;
   const uint32_t box_rows = (uint32_t)std::min(block_size, 16 * (4 / hg));   // min(block, keys per tile)
-  const uint32_t planes = (uint32_t)(hg * D / 64);
-  if ((s = encode_map(&tk, k_pool, cols, nrows, box_rows, planes, bf16)) != GQA_OK) return s;
-  if ((s = encode_map(&tv, v_pool, cols, nrows, box_rows, planes, bf16)) != GQA_OK) return s;
+  if (vllm) {
+    if ((s = encode_vllm_k(&tk, k_pool, (uint64_t)num_blocks, h_kv, D, block_size, hg, bf16)) != GQA_OK) return s;
+    if ((s = encode_vllm_v(&tv, v_pool, (uint64_t)num_blocks, h_kv, D, block_size, hg, bf16)) != GQA_OK) return s;
+  } else {
+    const uint64_t cols = (uint64_t)h_kv * D, nrows = (uint64_t)num_blocks * block_size;
+    const uint32_t planes = (uint32_t)(hg * D / 64);
+    if ((s = encode_map(&tk, k_pool, cols, nrows, box_rows, planes, bf16)) != GQA_OK) return s;
+    if ((s = encode_map(&tv, v_pool, cols, nrows, box_rows, planes, bf16)) != GQA_OK) return s;
+  }
 
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   DecodeArgs a;
@@ -465,7 +547,7 @@ gqa_status paged_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t*
     a.R = (int64_t)n * h_q;
     a.total_items = (int64_t)n * p.max_parts * (h_kv / hg);   // upper bound; the kernel counts the real ones
     const int64_t ctas = std::min<int64_t>((int64_t)sms * occ, a.total_items);
-    if (launch_unit(p.di, p.cls, 100 + hg, bf16, dim3((unsigned)ctas, 1, 1), st, tk, tv, a) != cudaSuccess)
+    if (launch_unit(p.di, p.cls, kind, bf16, dim3((unsigned)ctas, 1, 1), st, tk, tv, a) != cudaSuccess)
       return GQA_ERR_CUDA;
     if (p.max_parts > 1) {
       // second pass: fold the partitions of every multi-partition sequence
@@ -539,6 +621,30 @@ size_t gqa_decode_workspace_size(int batch, int T_q, int64_t S_kv, int h_q, int 
     return p.lay.total;
   } catch (...) {
     return 0;
+  }
+}
+
+gqa_status gqa_paged_plan(int num_seqs, int h_q, int h_kv, int d_head, int block_size, int max_seq_len,
+                          int partition_size, int vllm_layout, const gqa_options* opt, int* partition_out,
+                          int* head_group_out, int* launches_out) {
+  try {
+    const gqa_options o = opt ? *opt : defaults();
+    PagedPlan p;
+    gqa_status s = plan_paged(num_seqs, h_q, h_kv, d_head, max_seq_len, partition_size, &p);
+    if (s != GQA_OK) return s;
+    if (num_seqs < 1) return GQA_ERR_INVALID_ARG;
+    int part = partition_size, hg = 0, sms = 0, occ = 0;
+    if (!(block_size == 8 || block_size == 16 || block_size == 32 || block_size == 64)) return GQA_ERR_INVALID_ARG;
+    if ((s = choose_paged(p, num_seqs, h_q, h_kv, d_head, max_seq_len, block_size, o, vllm_layout != 0, &part, &hg,
+                          &sms, &occ)) != GQA_OK)
+      return s;
+    const int chunks = (num_seqs + kPagedSeqs - 1) / kPagedSeqs;
+    if (partition_out) *partition_out = part;
+    if (head_group_out) *head_group_out = hg;
+    if (launches_out) *launches_out = chunks * (p.max_parts > 1 ? 2 : 1);
+    return GQA_OK;
+  } catch (...) {
+    return GQA_ERR_CUDA;
   }
 }
 
@@ -633,7 +739,7 @@ gqa_status gqa_decode_paged_ex(const uint16_t* q, const uint16_t* k_pool, const 
   try {
     return paged_impl(q, k_pool, v_pool, block_tables, seq_lens, o, num_seqs, max_blocks_per_seq, num_blocks,
                       block_size, partition_size, h_q, h_kv, d_head, scale, max_seq_len, workspace, ws_bytes, stream,
-                      opt);
+                      opt, false);
   } catch (...) {
     return GQA_ERR_CUDA;
   }
@@ -647,6 +753,30 @@ gqa_status gqa_decode_paged(const uint16_t* q, const uint16_t* k_pool, const uin
   return gqa_decode_paged_ex(q, k_pool, v_pool, block_tables, seq_lens, o, num_seqs, max_blocks_per_seq, num_blocks,
                              block_size, partition_size, h_q, h_kv, d_head, scale, max_seq_len, workspace, ws_bytes,
                              stream, nullptr);
+}
+
+gqa_status gqa_decode_paged_vllm_ex(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                    const int32_t* block_tables, const int32_t* seq_lens, uint16_t* o, int num_seqs,
+                                    int max_blocks_per_seq, int num_blocks, int block_size, int partition_size,
+                                    int h_q, int h_kv, int d_head, float scale, int max_seq_len, void* workspace,
+                                    size_t ws_bytes, void* stream, const gqa_options* opt) {
+  try {
+    return paged_impl(q, k_cache, v_cache, block_tables, seq_lens, o, num_seqs, max_blocks_per_seq, num_blocks,
+                      block_size, partition_size, h_q, h_kv, d_head, scale, max_seq_len, workspace, ws_bytes, stream,
+                      opt, true);
+  } catch (...) {
+    return GQA_ERR_CUDA;
+  }
+}
+
+gqa_status gqa_decode_paged_vllm(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                 const int32_t* block_tables, const int32_t* seq_lens, uint16_t* o, int num_seqs,
+                                 int max_blocks_per_seq, int num_blocks, int block_size, int partition_size, int h_q,
+                                 int h_kv, int d_head, float scale, int max_seq_len, void* workspace,
+                                 size_t ws_bytes, void* stream) {
+  return gqa_decode_paged_vllm_ex(q, k_cache, v_cache, block_tables, seq_lens, o, num_seqs, max_blocks_per_seq,
+                                  num_blocks, block_size, partition_size, h_q, h_kv, d_head, scale, max_seq_len,
+                                  workspace, ws_bytes, stream, nullptr);
 }
 
 }  // extern "C"

@@ -55,7 +55,7 @@ struct Inst {
   }
 };
 
-template <int D, int CLS, int HG, bool BF16>
+template <int D, int CLS, int HG, bool BF16, bool VLLM>
 struct PagedInst {
   static constexpr int NT = cls_nt(CLS);
   static constexpr int WN = cls_wn(CLS);
@@ -64,21 +64,21 @@ struct PagedInst {
   static_assert(C::PSMEM_BYTES <= 227 * 1024, "shared memory budget");
 
   static cudaError_t prepare(int* occupancy) {
-    auto fn = gqa_paged_kernel<D, NT, WN, STAGES, HG, BF16>;
+    auto fn = gqa_paged_kernel<D, NT, WN, STAGES, HG, BF16, VLLM>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::PSMEM_BYTES);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, fn, C::PTHREADS, C::PSMEM_BYTES);
   }
   static cudaError_t launch(dim3 grid, cudaStream_t st, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a) {
-    gqa_paged_kernel<D, NT, WN, STAGES, HG, BF16><<<grid, C::PTHREADS, C::PSMEM_BYTES, st>>>(tk, tv, a);
+    gqa_paged_kernel<D, NT, WN, STAGES, HG, BF16, VLLM><<<grid, C::PTHREADS, C::PSMEM_BYTES, st>>>(tk, tv, a);
     return cudaGetLastError();
   }
 };
 
 // One unit (translation unit) per (kernel kind, d_head, element type).  Contiguous units:
-// cls in [0, 4), variant = causal (0 / 1).  Paged units: cls in [0, 4), variant = head
-// group in {1, 2, 4} (2 and 4 only for cls 0 and 1).
+// cls in [0, 4), variant = causal (0 / 1).  Paged units (row-layout pool or vLLM cache
+// layout): cls in [0, 4), variant = head group in {1, 2, 4} (2 and 4 only for cls 0 and 1).
 #define GQA_DECLARE_UNIT(NAME)                                                                   \
   cudaError_t NAME##_prepare(int cls, int variant, int* occupancy);                              \
   cudaError_t NAME##_launch(int cls, int variant, dim3 grid, cudaStream_t st, const CUtensorMap& tk, \
@@ -100,24 +100,24 @@ struct PagedInst {
     GQA_CONTIG_CASES(D, BF, launch(grid, st, tk, tv, a))                                         \
   }
 
-#define GQA_PAGED_CASES(D, BF, CALL)                                                             \
-  if (cls == 0 && variant == 1) return PagedInst<D, 0, 1, BF>::CALL;                             \
-  if (cls == 0 && variant == 2) return PagedInst<D, 0, 2, BF>::CALL;                             \
-  if (cls == 0 && variant == 4) return PagedInst<D, 0, 4, BF>::CALL;                             \
-  if (cls == 1 && variant == 1) return PagedInst<D, 1, 1, BF>::CALL;                             \
-  if (cls == 1 && variant == 2) return PagedInst<D, 1, 2, BF>::CALL;                             \
-  if (cls == 1 && variant == 4) return PagedInst<D, 1, 4, BF>::CALL;                             \
-  if (cls == 2 && variant == 1) return PagedInst<D, 2, 1, BF>::CALL;                             \
-  if (cls == 3 && variant == 1) return PagedInst<D, 3, 1, BF>::CALL;                             \
+#define GQA_PAGED_CASES(D, BF, VL, CALL)                                                         \
+  if (cls == 0 && variant == 1) return PagedInst<D, 0, 1, BF, VL>::CALL;                         \
+  if (cls == 0 && variant == 2) return PagedInst<D, 0, 2, BF, VL>::CALL;                         \
+  if (cls == 0 && variant == 4) return PagedInst<D, 0, 4, BF, VL>::CALL;                         \
+  if (cls == 1 && variant == 1) return PagedInst<D, 1, 1, BF, VL>::CALL;                         \
+  if (cls == 1 && variant == 2) return PagedInst<D, 1, 2, BF, VL>::CALL;                         \
+  if (cls == 1 && variant == 4) return PagedInst<D, 1, 4, BF, VL>::CALL;                         \
+  if (cls == 2 && variant == 1) return PagedInst<D, 2, 1, BF, VL>::CALL;                         \
+  if (cls == 3 && variant == 1) return PagedInst<D, 3, 1, BF, VL>::CALL;                         \
   return cudaErrorInvalidValue;
 
-#define GQA_DEFINE_PAGED_UNIT(NAME, D, BF)                                                       \
+#define GQA_DEFINE_PAGED_UNIT(NAME, D, BF, VL)                                                   \
   cudaError_t NAME##_prepare(int cls, int variant, int* occupancy) {                             \
-    GQA_PAGED_CASES(D, BF, prepare(occupancy))                                                   \
+    GQA_PAGED_CASES(D, BF, VL, prepare(occupancy))                                               \
   }                                                                                              \
   cudaError_t NAME##_launch(int cls, int variant, dim3 grid, cudaStream_t st, const CUtensorMap& tk, \
                             const CUtensorMap& tv, const DecodeArgs& a) {                        \
-    GQA_PAGED_CASES(D, BF, launch(grid, st, tk, tv, a))                                          \
+    GQA_PAGED_CASES(D, BF, VL, launch(grid, st, tk, tv, a))                                      \
   }
 
 GQA_DECLARE_UNIT(contig_d64)
@@ -128,5 +128,9 @@ GQA_DECLARE_UNIT(contig_d64_bf16)
 GQA_DECLARE_UNIT(contig_d128_bf16)
 GQA_DECLARE_UNIT(paged_d64_bf16)
 GQA_DECLARE_UNIT(paged_d128_bf16)
+GQA_DECLARE_UNIT(paged_vllm_d64)
+GQA_DECLARE_UNIT(paged_vllm_d128)
+GQA_DECLARE_UNIT(paged_vllm_d64_bf16)
+GQA_DECLARE_UNIT(paged_vllm_d128_bf16)
 
 }  // namespace gqa

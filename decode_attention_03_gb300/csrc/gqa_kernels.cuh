@@ -50,7 +50,7 @@ constexpr uint32_t kDevTimeout = 1u;
 constexpr uint32_t kDevBadInput = 2u;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMaxBoxesPerPart = 256;   // paged: TMA boxes (blocks or block slices) of one partition
+constexpr int kMaxBoxesPerPart = 1024;  // paged: TMA boxes (blocks or block slices) of one partition
 constexpr int kItemSlots = 4;      // paged kernel: descriptors in flight between scheduler and workers
 constexpr int kPagedSeqs = 1024;   // paged kernel: sequences per launch (the host splits larger batches)
 
@@ -244,9 +244,39 @@ __device__ __forceinline__ void zero_masked_v(uint8_t* vhead, int ks, int valid,
   __syncwarp();
 }
 
+// vLLM cache layout (page "muh_kernel_map.py", paged_attention_v1 key_cache
+// [num_blocks, num_kv_heads, head_dim/x, block_size, x], x = 8 16-bit elements; value cache
+// [num_blocks, num_kv_heads, head_dim, block_size]).  A TMA box holds one whole block
+// (rb = block_size keys) of HG heads -- a contiguous stretch of each cache -- and lands as:
+//  * K: [HG*D/8 chunks][rb keys][16 bytes] -- chunk-major, no swizzle: the 8 keys of an
+//    ldmatrix row group are 128 consecutive bytes;
+//  * V: [HG*D rows][rb keys] (V transposed), moved as 128-byte rows with the 128-byte
+//    swizzle, so that the 8 d rows an ldmatrix reads hit distinct banks for every block size.
+// Byte offset of element (d row, key kb) of a V box, swizzle applied:
+__device__ __forceinline__ int vllm_v_offset(int drow, int kb, int rb) {
+  const int off = (drow * rb + kb) * 2;
+  return off ^ (((off >> 7) & 7) << 4);
+}
+
+// Keys of this warp's slice past the range, vLLM layout: zero their V columns (every d row of
+// the warp's head) so that 0 * (stale or NaN) cannot reach O.  `vhead` points at the first
+// row of this warp's head in the tile's first box; boxes of rb keys are box_bytes apart.
+template <int D>
+__device__ __forceinline__ void zero_masked_v_vllm(uint8_t* vhead, int ks, int valid, int lane, int rb,
+                                                   int box_bytes) {
+  const int nmask = 16 - valid;
+  for (int i = lane; i < D * nmask; i += 32) {
+    const int drow = i / nmask;
+    const int key = ks * 16 + valid + (i - drow * nmask);
+    *reinterpret_cast<uint16_t*>(vhead + (key / rb) * box_bytes + vllm_v_offset(drow, key % rb, rb)) = 0;
+  }
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+}
+
 // One tile: this warp's 16 keys against its 8*NT query rows; kbase / vbase point at
-// the first plane of the warp's head.
-template <int D, int NT, int BOXP, bool CAUSAL = false, bool BF16 = false>
+// the first plane (row layout) or first chunk / d row (VLLM) of the warp's head.
+template <int D, int NT, int BOXP, bool CAUSAL = false, bool BF16 = false, bool VLLM = false>
 __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbase, uint32_t vbase, int valid,
                                              int key0, int ks, int lane, float scale_log2, int rb) {
   constexpr int KD = WarpState<D, NT>::KD;
@@ -257,6 +287,13 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbas
   const int v_c0 = (lane >> 3) & 1;
   const int k_off = row_offset<BOXP>(k_row, rb), v_off = row_offset<BOXP>(v_row, rb);
   const int plane = rb * 128;
+  // VLLM: box of this lane's K row and of its V key group (keys ks*16 + 8*(lane >> 4) ..+7)
+  const int box_bytes = rb * 128 * BOXP;
+  const uint32_t kvb = kbase + (k_row / rb) * box_bytes + (k_row % rb) * 16;
+  const int v_key = ks * 16 + (lane >> 4) * 8;
+  const uint32_t vvb = vbase + (v_key / rb) * box_bytes;
+  const int v_kb = v_key % rb;
+  const int v_dr = (lane & 7) + ((lane >> 3) & 1) * 8;
 
   // ---- S^T = K Q^T : 16 keys x 8*NT query rows, fp32
   float sc[NT][4];
@@ -265,7 +302,11 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbas
 #pragma unroll
   for (int kk = 0; kk < KD; ++kk) {
     uint32_t af[4];
-    ptx::ldmatrix_x4(af, chunk_addr(kbase, k_off, k_row, kk * 2 + k_c0, plane));
+    if constexpr (VLLM) {
+      ptx::ldmatrix_x4(af, kvb + (kk * 2 + k_c0) * rb * 16);
+    } else {
+      ptx::ldmatrix_x4(af, chunk_addr(kbase, k_off, k_row, kk * 2 + k_c0, plane));
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) Elem<BF16>::mma(sc[nt], af, st.qf[nt][kk]);
   }
@@ -335,7 +376,12 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbas
 #pragma unroll
   for (int i = 0; i < KD; ++i) {
     uint32_t af[4];
-    ptx::ldmatrix_x4_trans(af, chunk_addr(vbase, v_off, v_row, i * 2 + v_c0, plane));
+    if constexpr (VLLM) {
+      // V^T is stored: rows d 16i .. 16i+15, 8 keys per ldmatrix row
+      ptx::ldmatrix_x4(af, vvb + vllm_v_offset(i * 16 + v_dr, v_kb, rb));
+    } else {
+      ptx::ldmatrix_x4_trans(af, chunk_addr(vbase, v_off, v_row, i * 2 + v_c0, plane));
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) Elem<BF16>::mma(st.acc[i][nt], af, pf[nt]);
   }
@@ -688,7 +734,7 @@ static_assert(sizeof(ItemDesc) == 48, "descriptor slot size");
 //  * epilogue: combines the consumer warps of a finished item and writes the f16
 //    output (one-partition sequences) or the partition's fp32 partial; the partials
 //    are folded by gqa_paged_merge_kernel (the second pass of paged attention v2).
-template <int D, int NT, int WN, int STAGES, int HG, bool BF16>
+template <int D, int NT, int WN, int STAGES, int HG, bool BF16, bool VLLM>
 __global__ void __launch_bounds__(Cfg<D, NT, WN, STAGES>::PTHREADS)
 gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const DecodeArgs a) {
@@ -866,6 +912,7 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     if (lane == 0) {
       const uint64_t pol = ptx::policy_evict_first();
       const int nbox = TK / br;   // boxes per tile
+      const int bs_shift = __ffs(a.block_size) - 1;   // block sizes are powers of two
       int tile_it = 0, stall_tile = -1;
       bool gave_up = false;
       for (int k = 0;; ++k) {
@@ -904,8 +951,16 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             const int y = by[b0 + j];
             if (y < 0) continue;
             const uint32_t off = j * br * 128 * BOXP;
-            ptx::tma_load_3d(kdst + off, &tmK, fb, 0, y, d.g * C::HALVES, pol);
-            ptx::tma_load_3d(vdst + off, &tmV, fb, 0, y, d.g * C::HALVES, pol);
+            if constexpr (VLLM) {
+              // pool row y = block * block_size (boxes are whole blocks): both boxes start at head
+              // block*h_kv + g of the (block, head)-major caches
+              const int kvh = (y >> bs_shift) * a.h_kv + d.g;
+              ptx::tma_load_4d(kdst + off, &tmK, fb, 0, 0, 0, kvh, pol);
+              ptx::tma_load_3d(vdst + off, &tmV, fb, 0, 0, kvh, pol);
+            } else {
+              ptx::tma_load_3d(kdst + off, &tmK, fb, 0, y, d.g * C::HALVES, pol);
+              ptx::tma_load_3d(vdst + off, &tmV, fb, 0, y, d.g * C::HALVES, pol);
+            }
           }
         }
         ptx::mbar_arrive(ptx::smem_u32(iempty + slot));
@@ -957,10 +1012,17 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         const uint32_t vbase = kbase + C::KV_BYTES;
         const int64_t key0 = d.key_begin + (int64_t)t * TK + ks * 16;
         const int valid = (int)max((int64_t)0, min((int64_t)16, d.key_end - key0));
-        if (valid < 16)
-          zero_masked_v<C::HALVES, BOXP>(smem + s * C::STAGE_BYTES + C::KV_BYTES + head_off, ks, valid, lane, br);
+        if (valid < 16) {
+          uint8_t* vh = smem + s * C::STAGE_BYTES + C::KV_BYTES + head_off;
+          if constexpr (VLLM) {
+            zero_masked_v_vllm<D>(vh, ks, valid, lane, br, br * 128 * BOXP);
+          } else {
+            zero_masked_v<C::HALVES, BOXP>(vh, ks, valid, lane, br);
+          }
+        }
         if (valid > 0)
-          consume_tile<D, NT, BOXP, false, BF16>(st, kbase, vbase, valid, (int)key0, ks, lane, a.scale_log2, br);
+          consume_tile<D, NT, BOXP, false, BF16, VLLM>(st, kbase, vbase, valid, (int)key0, ks, lane, a.scale_log2,
+                                                       br);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(empty + s));
       }

@@ -2,5 +2,5 @@
 #include "gqa_instances.cuh"
 
 namespace gqa {
-GQA_DEFINE_PAGED_UNIT(paged_d128_bf16, 128, true)
+GQA_DEFINE_PAGED_UNIT(paged_d128_bf16, 128, true, false)
 }  // namespace gqa

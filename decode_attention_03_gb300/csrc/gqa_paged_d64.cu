@@ -2,5 +2,5 @@
 #include "gqa_instances.cuh"
 
 namespace gqa {
-GQA_DEFINE_PAGED_UNIT(paged_d64, 64, false)
+GQA_DEFINE_PAGED_UNIT(paged_d64, 64, false, false)
 }  // namespace gqa

@@ -2,5 +2,5 @@
 #include "gqa_instances.cuh"
 
 namespace gqa {
-GQA_DEFINE_PAGED_UNIT(paged_d64_bf16, 64, true)
+GQA_DEFINE_PAGED_UNIT(paged_d64_bf16, 64, true, false)
 }  // namespace gqa

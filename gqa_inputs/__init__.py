@@ -143,6 +143,8 @@ class Workload:
     len_lo: int = 0      # paged: inclusive bounds of the per-sequence length
     len_hi: int = 0
     elem: str = "f16"    # element type of Q, K, V: "f16" or "bf16" (bit patterns)
+    layout: str = "rows"  # paged: "rows" pools (num_blocks, block_size, h_kv*d) or "vllm" caches
+                          # k (num_blocks, h_kv, d/8, block_size, 8), v (num_blocks, h_kv, d, block_size)
 
     @property
     def G(self) -> int:
@@ -175,6 +177,14 @@ WORKLOADS: Dict[str, Workload] = {
     # distributions (1% of key rows x8, V uniform in [-1, 1)); seed 5
     "verify16": Workload("verify16", "contiguous", 1, 16, 262143, 64, 8, 128, seed=5,
                          v_dist="uniform", spike_frac=0.01, spike_mult=8.0),
+    # the paged workload's values (seed 3) in vLLM's cache layout, partitions chosen automatically
+    "paged_vllm": Workload("paged_vllm", "paged", 64, 1, 16384, 32, 8, 128, seed=3,
+                           block_size=16, partition_size=0, len_lo=1024, len_hi=16384, layout="vllm"),
+    # many short sequences (<= 8192 keys: the page's single-pass v1 regime), vLLM layout, run as
+    # v1 (one partition of 2048 keys per sequence): 384 sequences, lengths uniform in [128, 2048],
+    # block 16; seed 6
+    "paged_v1": Workload("paged_v1", "paged", 384, 1, 2048, 32, 8, 128, seed=6,
+                         block_size=16, partition_size=2048, len_lo=128, len_hi=2048, layout="vllm"),
 }
 
 
@@ -230,8 +240,18 @@ def paged_layout(w: Workload):
     return lens.astype(np.int32), tables, num_blocks
 
 
+def to_vllm_layout(k_pool: np.ndarray, v_pool: np.ndarray, h_kv: int, d_head: int):
+    """The same keys and values rearranged into vLLM's caches: k (num_blocks, h_kv, d/8,
+    block_size, 8), v (num_blocks, h_kv, d, block_size)."""
+    nb, bs, _ = k_pool.shape
+    k = k_pool.reshape(nb, bs, h_kv, d_head // 8, 8).transpose(0, 2, 3, 1, 4)
+    v = v_pool.reshape(nb, bs, h_kv, d_head).transpose(0, 2, 3, 1)
+    return np.ascontiguousarray(k), np.ascontiguousarray(v)
+
+
 def make_paged(w: Workload, tail_fill: str = "normal") -> dict:
-    """Q ``(num_seqs, h_q*d)``, K/V pools ``(num_blocks, block_size, h_kv*d)``.
+    """Q ``(num_seqs, h_q*d)``, K/V pools ``(num_blocks, block_size, h_kv*d)`` (``layout='vllm'``:
+    the same values in vLLM's caches, under the same keys).
 
     ``tail_fill='nan'`` overwrites the pool slots past each sequence's end (the
     unused tail of its last block) with float16 NaN in both K and V; a correct
@@ -252,7 +272,11 @@ def make_paged(w: Workload, tail_fill: str = "normal") -> dict:
                 vp[last, L % w.block_size:, :] = nan
     elif tail_fill != "normal":
         raise ValueError(tail_fill)
-    return dict(workload=w, q=q, k_pool=kp, v_pool=vp, block_tables=tables, seq_lens=lens, elem=e,
+    if w.layout == "vllm":
+        kp, vp = to_vllm_layout(kp, vp, w.h_kv, w.d_head)
+    elif w.layout != "rows":
+        raise ValueError(w.layout)
+    return dict(workload=w, q=q, k_pool=kp, v_pool=vp, block_tables=tables, seq_lens=lens, elem=e, layout=w.layout,
                 num_seqs=w.batch, T_q=w.T_q, h_q=w.h_q, h_kv=w.h_kv, d_head=w.d_head,
                 scale=w.scale, num_blocks=num_blocks, block_size=w.block_size,
                 partition_size=w.partition_size, max_blocks_per_seq=tables.shape[1],

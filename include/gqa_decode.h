@@ -112,9 +112,18 @@ gqa_status gqa_decode_plan(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, 
 size_t gqa_decode_workspace_size(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head,
                                  int n_splits);
 
-/* Workspace bytes for gqa_decode_paged (T_q = 1).  Returns 0 on invalid arguments. */
+/* Workspace bytes for gqa_decode_paged and gqa_decode_paged_vllm (T_q = 1); partition_size 0 sizes
+ * for the automatic choice.  Returns 0 on invalid arguments. */
 size_t gqa_paged_workspace_size(int num_seqs, int h_q, int h_kv, int d_head, int max_seq_len,
                                 int partition_size);
+
+/* What a paged call (vllm_layout 0: gqa_decode_paged, 1: gqa_decode_paged_vllm) with these shapes
+ * and options (NULL = defaults) does on the current device: the partition size (the automatic
+ * choice resolved), the KV heads per work item, and the kernel launches (two per 1024 sequences
+ * when some sequence spans several partitions, else one).  Outputs may be NULL. */
+gqa_status gqa_paged_plan(int num_seqs, int h_q, int h_kv, int d_head, int block_size, int max_seq_len,
+                          int partition_size, int vllm_layout, const gqa_options* opt, int* partition_out,
+                          int* head_group_out, int* launches_out);
 
 /* Zero-fill a workspace (asynchronous memset on `stream`).  A workspace must be zero before
  * its first use; every call that completes without a device fault leaves it so again. */
@@ -180,8 +189,13 @@ gqa_status gqa_merge_partial(const float* m, const float* l, const float* o_part
  *                 a length-0 sequence gets O = 0
  *   o             (num_seqs, h_q*d_head) f16, written
  * block_size in {8, 16, 32, 64}; partition_size a multiple of 64 with
- * partition_size / min(block_size, 16) <= 256; max_seq_len (host-known bound on seq_lens) sizes the grid.
- * Block ids outside [0, num_blocks) are not loaded and are reported by gqa_workspace_check. */
+ * partition_size / min(block_size, 16) <= 1024, or 0 = automatic (the page's v2: 512-token
+ * partitions, a partition pass and a merge pass).  A partition_size of at least max_seq_len is
+ * the page's single-pass v1 (page "muh_kernel_map.py", paged_attention_v1, for seq_len <= 8192):
+ * one pass over each whole sequence and no merge launch; on GB300 it measured no faster than v2
+ * on any batch tried, so the automatic choice does not take it.  max_seq_len (host-known bound
+ * on seq_lens) sizes the grid.  Block ids outside [0, num_blocks) are not loaded and are
+ * reported by gqa_workspace_check. */
 gqa_status gqa_decode_paged(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
                             const int32_t* block_tables, const int32_t* seq_lens, uint16_t* o,
                             int num_seqs, int max_blocks_per_seq, int num_blocks, int block_size,
@@ -194,6 +208,30 @@ gqa_status gqa_decode_paged_ex(const uint16_t* q, const uint16_t* k_pool, const 
                                int partition_size, int h_q, int h_kv, int d_head, float scale,
                                int max_seq_len, void* workspace, size_t ws_bytes, void* stream,
                                const gqa_options* opt);
+
+/* Paged decode over vLLM's cache layout (page "muh_kernel_map.py", VLLM_KERNEL_MAP
+ * 'paged_attention_v1': key_cache [num_blocks, num_kv_heads, head_dim/x, block_size, x]), read in
+ * place.  x = 8 (16-byte vectors of 16-bit elements).  The page gives no value-cache layout; the
+ * same serving stack's [num_blocks, num_kv_heads, head_dim, block_size] is taken:
+ *   k_cache  (num_blocks, h_kv, d_head/8, block_size, 8) f16 / bf16
+ *   v_cache  (num_blocks, h_kv, d_head, block_size)      f16 / bf16
+ * Everything else -- q, block_tables, seq_lens, o, partition_size (0 = automatic, 512),
+ * workspace (gqa_paged_workspace_size), options, errors -- as gqa_decode_paged, except that a
+ * work item's KV heads (gqa_options.paged_head_group) are at most 64 / block_size (a TMA box
+ * holds whole blocks; the automatic choice respects it).  Additionally
+ * num_blocks * h_kv * d_head / 8 must be < 2^31. */
+gqa_status gqa_decode_paged_vllm(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                 const int32_t* block_tables, const int32_t* seq_lens, uint16_t* o,
+                                 int num_seqs, int max_blocks_per_seq, int num_blocks, int block_size,
+                                 int partition_size, int h_q, int h_kv, int d_head, float scale,
+                                 int max_seq_len, void* workspace, size_t ws_bytes, void* stream);
+
+gqa_status gqa_decode_paged_vllm_ex(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                    const int32_t* block_tables, const int32_t* seq_lens, uint16_t* o,
+                                    int num_seqs, int max_blocks_per_seq, int num_blocks, int block_size,
+                                    int partition_size, int h_q, int h_kv, int d_head, float scale,
+                                    int max_seq_len, void* workspace, size_t ws_bytes, void* stream,
+                                    const gqa_options* opt);
 
 /* Size of the per-GPU device array used by gqa_decode_noalloc: 8 MiB. */
 #define GQA_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)

@@ -219,13 +219,36 @@ def gather_paged(pool, table_row, length: int, block_size: int):
     return np.asarray(pool)[blocks, slots]                 # (length, h_kv*D)
 
 
+def gather_paged_vllm(k_cache, v_cache, table_row, length: int, block_size: int):
+    """Keys and values of one sequence in token order, read from vLLM's cache layout (page
+    "muh_kernel_map.py", VLLM_KERNEL_MAP 'paged_attention_v1': key_cache [num_blocks,
+    num_kv_heads, head_dim/x, block_size, x]; the page gives no value layout, and the same
+    serving stack's [num_blocks, num_kv_heads, head_dim, block_size] is taken).  Token j
+    lives in block ``table_row[j // block_size]``, slot ``j % block_size``; dimension
+    ``c*x + e`` of KV head g is ``k_cache[block, g, c, slot, e]`` and value dimension ``e`` is
+    ``v_cache[block, g, e, slot]``.  Returns both as ``(length, h_kv*D)`` in head-major order."""
+    kc, vc = np.asarray(k_cache), np.asarray(v_cache)
+    _, h_kv, dx, _, x = kc.shape
+    j = np.arange(int(length))
+    blocks = np.asarray(table_row)[j // block_size]
+    slots = j % block_size
+    k = kc[blocks, :, :, slots, :]                        # (length, h_kv, D/x, x)
+    v = vc[blocks, :, :, slots]                           # (length, h_kv, D)
+    return k.reshape(len(j), h_kv * dx * x), v.reshape(len(j), h_kv * dx * x)
+
+
 def decode_paged_seq(q, k_pool, v_pool, block_tables, seq_lens, b: int,
-                     h_q: int, h_kv: int, D: int, scale: float, block_size: int):
+                     h_q: int, h_kv: int, D: int, scale: float, block_size: int, layout: str = "rows"):
     """Output ``(T_q, h_q*D)`` of sequence ``b``: the contiguous definition on
-    its gathered keys and values.  ``seq_len = 0`` gives zeros."""
+    its gathered keys and values.  ``seq_len = 0`` gives zeros.  ``layout``: "rows" for
+    pools ``(num_blocks, block_size, h_kv*D)``, "vllm" for vLLM's caches."""
     L = int(seq_lens[b])
-    kb = gather_paged(k_pool, block_tables[b], L, block_size)[None]
-    vb = gather_paged(v_pool, block_tables[b], L, block_size)[None]
+    if layout == "vllm":
+        kb, vb = gather_paged_vllm(k_pool, v_pool, block_tables[b], L, block_size)
+        kb, vb = kb[None], vb[None]
+    else:
+        kb = gather_paged(k_pool, block_tables[b], L, block_size)[None]
+        vb = gather_paged(v_pool, block_tables[b], L, block_size)[None]
     qb = np.asarray(q[b:b + 1])
     if qb.ndim == 2:
         qb = qb[:, None, :]
@@ -239,9 +262,9 @@ def decode_paged_seq(q, k_pool, v_pool, block_tables, seq_lens, b: int,
 
 
 def decode_paged(q, k_pool, v_pool, block_tables, seq_lens, h_q: int, h_kv: int, D: int,
-                 scale: float, block_size: int, seqs: Optional[Iterable[int]] = None):
+                 scale: float, block_size: int, seqs: Optional[Iterable[int]] = None, layout: str = "rows"):
     """Paged attention output ``(num_seqs, T_q, h_q*D)``; ``seqs`` restricts the
-    work to some sequences (others are NaN)."""
+    work to some sequences (others are NaN).  ``layout`` as in ``decode_paged_seq``."""
     q = np.asarray(q)
     if q.ndim == 2:
         q = q[:, None, :]
@@ -249,7 +272,7 @@ def decode_paged(q, k_pool, v_pool, block_tables, seq_lens, h_q: int, h_kv: int,
     out = torch.full((N, T_q, h_q * D), float("nan"), dtype=torch.float64)
     for b in (range(N) if seqs is None else seqs):
         out[b] = decode_paged_seq(q, k_pool, v_pool, block_tables, seq_lens, b,
-                                  h_q, h_kv, D, scale, block_size)
+                                  h_q, h_kv, D, scale, block_size, layout)
     return out
 
 

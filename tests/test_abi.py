@@ -123,7 +123,8 @@ def test_paged_validation(binding):
 
     assert paged(bs=12) == binding.GQA_ERR_INVALID_ARG
     assert paged(part=500) == binding.GQA_ERR_INVALID_ARG            # not a multiple of 64
-    assert paged(bs=8, part=8192) == binding.GQA_ERR_INVALID_ARG     # > 256 blocks per partition
+    assert paged(bs=8, part=16384) == binding.GQA_ERR_INVALID_ARG    # > 1024 blocks per partition
+    assert paged(part=-64) == binding.GQA_ERR_INVALID_ARG
     assert paged(d=256) == binding.GQA_ERR_UNSUPPORTED
     assert paged(maxlen=-1) == binding.GQA_ERR_INVALID_ARG
     assert paged(N=0) == binding.GQA_OK
@@ -136,6 +137,29 @@ def test_paged_validation(binding):
                                    ctypes.byref(opt)) == binding.GQA_ERR_INVALID_ARG
     assert lib.gqa_paged_workspace_size(64, 32, 8, 128, 16384, 512) > 0
     assert lib.gqa_paged_workspace_size(64, 32, 8, 128, 16384, 500) == 0
+    # partition 0 (automatic v1 / v2) is sized as v2 with 512-token partitions
+    assert lib.gqa_paged_workspace_size(64, 32, 8, 128, 16384, 0) == lib.gqa_paged_workspace_size(64, 32, 8, 128,
+                                                                                                16384, 512)
+
+
+def test_paged_vllm_validation(binding):
+    """The vLLM-layout entry point rejects bad shapes on the host, before any device access."""
+    lib = binding.lib
+    _b, p = _fake()
+    st = ctypes.c_void_p(0)
+
+    def paged(bs=16, part=0, N=2, hq=8, hkv=2, d=128, maxlen=1000, maxblk=64, nblk=100, wsb=1 << 20):
+        return lib.gqa_decode_paged_vllm(p, p, p, p, p, p, N, maxblk, nblk, bs, part, hq, hkv, d, 0.1, maxlen,
+                                         p, wsb, st)
+
+    assert paged(bs=12) == binding.GQA_ERR_INVALID_ARG
+    assert paged(part=500) == binding.GQA_ERR_INVALID_ARG
+    assert paged(d=96) == binding.GQA_ERR_UNSUPPORTED
+    assert paged(hq=9, hkv=2) == binding.GQA_ERR_INVALID_ARG          # h_q % h_kv
+    assert paged(hq=130, hkv=1) == binding.GQA_ERR_UNSUPPORTED        # G > 64
+    assert paged(N=0) == binding.GQA_OK
+    assert paged(wsb=255) == binding.GQA_ERR_WORKSPACE
+    assert paged(nblk=1 << 27, hkv=2, hq=8) == binding.GQA_ERR_INVALID_ARG   # blocks * h_kv * d/8 >= 2^31
 
 
 def test_workspace_layout_sizes(binding):

@@ -254,6 +254,29 @@ def pin_paged(orc) -> bool:
     return ok
 
 
+def pin_paged_vllm(orc) -> bool:
+    """vLLM's cache layout (key cache [blocks, h_kv, D/x, block, x], x = 8; value cache
+    [blocks, h_kv, D, block]) holding the same keys and values as a row pool gives the same
+    output: the caches are filled here element by element from the layout statement."""
+    w = gqa_inputs.custom(4, 1, 70, 8, 2, 16, 93, kind="paged", block_size=8, partition_size=64,
+                          len_lo=1, len_hi=70)
+    p = gqa_inputs.make_paged(w)
+    kp, vp, lens, tab = p["k_pool"], p["v_pool"], p["seq_lens"], p["block_tables"]
+    nb, bs, h_kv, D, x = p["num_blocks"], 8, 2, 16, 8
+    kc = np.empty((nb, h_kv, D // x, bs, x), dtype=kp.dtype)
+    vc = np.empty((nb, h_kv, D, bs), dtype=vp.dtype)
+    for n in range(nb):
+        for slot in range(bs):
+            for g in range(h_kv):
+                for dd in range(D):
+                    kc[n, g, dd // x, slot, dd % x] = kp[n, slot, g * D + dd]
+                    vc[n, g, dd, slot] = vp[n, slot, g * D + dd]
+    rows = orc.decode_paged(p["q"], kp, vp, tab, lens, 8, 2, D, 0.3, bs)
+    got = orc.decode_paged(p["q"], kc, vc, tab, lens, 8, 2, D, 0.3, bs, layout="vllm")
+    k2, v2 = gqa_inputs.to_vllm_layout(kp, vp, h_kv, D)      # the input module's rearrangement agrees
+    return _close(got, rows) and np.array_equal(k2, kc) and np.array_equal(v2, vc)
+
+
 def pin_causal(orc) -> bool:
     """Causal tail (token t of T_q sees keys j <= S - T_q + t): equals PyTorch SDPA with the
     explicit bottom-right mask, equals the plain decode of each token over its visible
@@ -330,7 +353,8 @@ def _read_golden(path: str) -> dict:
 
 
 PINS = [pin_brute_force, pin_sdpa, pin_constant_scores, pin_one_hot, pin_single_key,
-        pin_split_merge, pin_merge_closed_form, pin_permutation, pin_shift, pin_paged, pin_causal, pin_golden]
+        pin_split_merge, pin_merge_closed_form, pin_permutation, pin_shift, pin_paged, pin_paged_vllm, pin_causal,
+        pin_golden]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -426,6 +450,31 @@ def _m_no_normalize(l, o):
     return _f64(o)
 
 
+def _m_vllm_chunk_swap(k_cache, v_cache, table_row, length, block_size):
+    # reads the key's d as (x, D/x) instead of (D/x, x)
+    kc, vc = np.asarray(k_cache), np.asarray(v_cache)
+    _, h_kv, dx, _, x = kc.shape
+    j = np.arange(int(length))
+    blocks = np.asarray(table_row)[j // block_size]
+    slots = j % block_size
+    k = kc[blocks, :, :, slots, :].transpose(0, 1, 3, 2)
+    v = vc[blocks, :, :, slots]
+    return k.reshape(len(j), h_kv * dx * x), v.reshape(len(j), h_kv * dx * x)
+
+
+def _m_vllm_v_transposed(k_cache, v_cache, table_row, length, block_size):
+    # takes the value cache as [blocks, h_kv, block, D] (the key's slot-major order)
+    kc, vc = np.asarray(k_cache), np.asarray(v_cache)
+    _, h_kv, dx, bs, x = kc.shape
+    j = np.arange(int(length))
+    blocks = np.asarray(table_row)[j // block_size]
+    slots = j % block_size
+    k = kc[blocks, :, :, slots, :]
+    vr = vc.reshape(vc.shape[0], h_kv, bs, dx * x)
+    v = vr[blocks, :, slots, :]
+    return k.reshape(len(j), h_kv * dx * x), v.reshape(len(j), h_kv * dx * x)
+
+
 def _m_gather_off_by_one(pool, table_row, length, block_size):
     j = np.arange(int(length))
     blocks = np.asarray(table_row)[j // block_size]
@@ -460,6 +509,8 @@ MUTANTS = {
     "merge_drops_l_term": dict(merge_pair=_m_merge_drop_l),
     "no_normalize": dict(normalize=_m_no_normalize),
     "paged_slot_off_by_one": dict(gather_paged=_m_gather_off_by_one),
+    "vllm_key_chunk_order_swapped": dict(gather_paged_vllm=_m_vllm_chunk_swap),
+    "vllm_value_transposed": dict(gather_paged_vllm=_m_vllm_v_transposed),
     "causal_limit_off_by_one": dict(decode_unit=_m_causal_off_by_one),
 }
 
