@@ -11,6 +11,7 @@
 
 #include "../../include/gqa_decode.h"
 #include "gqa_instances.cuh"
+#include "gqa_merge.cuh"
 #include "gqa_tc.cuh"
 
 namespace gqa {
@@ -18,7 +19,7 @@ namespace {
 
 constexpr int kVersion = 10000;            // 1.0.0
 constexpr size_t kHeaderBytes = 256;        // status word (+ reserved)
-constexpr int kMinTilesPerSplit = 4;        // a split streams at least 4 x 64 keys
+constexpr int kMinTilesPerSplit = 1;        // a split streams at least one 64-key tile
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;
 constexpr int kMaxDevices = 64;
 // Automatic merge choice of the tcgen05 kernel: the last CTA of a unit folds the splits
@@ -27,6 +28,10 @@ constexpr int kMaxDevices = 64;
 // against a few us for the separate merge kernel spread over the whole GPU).
 constexpr int64_t kInKernelMergeBytes = 256 * 1024;
 constexpr int kTcMinRows = 16;              // automatic MMA path: tcgen05 from this many rows per KV head
+// Automatic merge: more splits than this go to the separate merge kernel (the last CTA folding
+// them serialises the fold: tiny workload, 64 splits, 16.7 us in-kernel vs 11.9 us with the merge
+// kernel; 16 splits in-kernel 12.7 us)
+constexpr int kInKernelMaxSplits = 32;
 // Paged partitions chosen automatically (partition_size 0).  Page "muh_kernel_map.py" picks v1 --
 // one pass over each whole sequence, no merge pass -- for seq_len <= 8192 and v2 with 512-token
 // partitions above.  On GB300 the persistent kernel with 512-token partitions (and the merge pass
@@ -199,7 +204,9 @@ gqa_status encode_vllm_v(CUtensorMap* map, const void* base, uint64_t num_blocks
 
 // Split count: about one (b, g, split) CTA per SM -- ceil(SMs / units) splits per unit --
 // with every CTA co-resident (at most the resident slots of the GPU) and each split at
-// least kMinTilesPerSplit tiles long.  Measured on GB300: one CTA per SM streaming a
+// least kMinTilesPerSplit tiles long (short sweeps are latency-bound: more, shorter splits
+// measured faster -- tiny workload, 4096 keys: 16 splits of 4 tiles 12.7 us, 64 of one tile
+// 11.9 us with the merge kernel).  Measured on GB300: one CTA per SM streaming a
 // long split beats two shorter ones (long context: 591 vs 608 us; 8 x 32768 keys: 153
 // vs 156 us).  Prior art: page "muh_cc_dispatch.py", grid_even_share (grid = min(tiles,
 // SMs x subscription), even shares of tiles).
@@ -317,26 +324,50 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, 
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// one warp per row while a warp's first chunk of loads covers every partial, else four
+int merge_warps(int n_parts) { return n_parts <= kMergeChunk ? 1 : 4; }
+
+template <int D, bool BF16, int W>
+cudaError_t merge_launch_w(const float* m, const float* l, const float* op, int n_parts, int64_t rows, __half* o,
+                           float* mo, float* lo, float* oo, cudaStream_t st) {
+  const int64_t rpb = kMergeThreads / (32 * W);
+  const int64_t blocks = (rows + rpb - 1) / rpb;
+  if (blocks > 2147483647LL) return cudaErrorInvalidValue;
+  return launch_pdl(gqa_merge_kernel<D, BF16, W>, (unsigned)blocks, kMergeThreads, st, m, l, op, n_parts, rows, o,
+                    mo, lo, oo);
+}
+
 gqa_status merge_launch(const float* m, const float* l, const float* op, int n_parts, int64_t rows, int D,
                         __half* o, float* mo, float* lo, float* oo, cudaStream_t st, int bf16 = 0) {
   if (rows == 0) return GQA_OK;
-  const int64_t blocks = (rows + kMergeRows - 1) / kMergeRows;
-  if (blocks > 2147483647LL) return GQA_ERR_INVALID_ARG;
-  const unsigned g = (unsigned)blocks, t = kMergeWarps * kMergeRows * 32;
+  if (rows > 2147483647LL) return GQA_ERR_INVALID_ARG;
+  const bool one = merge_warps(n_parts) == 1;
   cudaError_t e = cudaErrorInvalidValue;
-  if (D == 64 && !bf16) e = launch_pdl(gqa_merge_kernel<64, false>, g, t, st, m, l, op, n_parts, rows, o, mo, lo, oo);
-  if (D == 64 && bf16) e = launch_pdl(gqa_merge_kernel<64, true>, g, t, st, m, l, op, n_parts, rows, o, mo, lo, oo);
-  if (D == 128 && !bf16) e = launch_pdl(gqa_merge_kernel<128, false>, g, t, st, m, l, op, n_parts, rows, o, mo, lo, oo);
-  if (D == 128 && bf16) e = launch_pdl(gqa_merge_kernel<128, true>, g, t, st, m, l, op, n_parts, rows, o, mo, lo, oo);
+#define GQA_MERGE_CASE(DD, BB)                                                                    \
+  if (D == DD && bf16 == BB)                                                                      \
+    e = one ? merge_launch_w<DD, BB, 1>(m, l, op, n_parts, rows, o, mo, lo, oo, st)               \
+            : merge_launch_w<DD, BB, 4>(m, l, op, n_parts, rows, o, mo, lo, oo, st);
+  GQA_MERGE_CASE(64, false)
+  GQA_MERGE_CASE(64, true)
+  GQA_MERGE_CASE(128, false)
+  GQA_MERGE_CASE(128, true)
+#undef GQA_MERGE_CASE
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
-// merge_mode 0 (automatic): in-kernel for the mma.sync kernel, and for the tcgen05 kernel while a
-// unit's partials are at most kInKernelMergeBytes; 1 separate kernel; 2 in-kernel
+template <int D, bool BF16, int W>
+cudaError_t paged_merge_launch_w(const DecodeArgs& a, cudaStream_t st) {
+  const int64_t rpb = kMergeThreads / (32 * W);
+  return launch_pdl(gqa_paged_merge_kernel<D, BF16, W>, (unsigned)((a.R + rpb - 1) / rpb), kMergeThreads, st, a);
+}
+
+// merge_mode 0 (automatic): in-kernel up to kInKernelMaxSplits splits (and, for the tcgen05 kernel,
+// while a unit's partials are at most kInKernelMergeBytes); 1 separate kernel; 2 in-kernel
 bool merge_in_kernel(const ContigPlan& p, int D, int merge_mode) {
   if (merge_mode == 1) return false;
-  if (merge_mode == 2 || !p.tc) return true;
-  return (int64_t)p.n_splits * p.rows * (D + 2) * 4 <= kInKernelMergeBytes;
+  if (merge_mode == 2) return true;
+  if (p.n_splits > kInKernelMaxSplits) return false;
+  return !p.tc || (int64_t)p.n_splits * p.rows * (D + 2) * 4 <= kInKernelMergeBytes;
 }
 
 gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* m_out,
@@ -551,12 +582,13 @@ gqa_status paged_impl(const uint16_t* q, const uint16_t* k_pool, const uint16_t*
       return GQA_ERR_CUDA;
     if (p.max_parts > 1) {
       // second pass: fold the partitions of every multi-partition sequence
-      const unsigned blocks = (unsigned)((a.R + kMergeRows - 1) / kMergeRows), t = kMergeWarps * kMergeRows * 32;
+      const bool one = merge_warps(p.max_parts) == 1;
       cudaError_t e = cudaErrorInvalidValue;
-      if (D == 64 && !bf16) e = launch_pdl(gqa_paged_merge_kernel<64, false>, blocks, t, st, a);
-      if (D == 64 && bf16) e = launch_pdl(gqa_paged_merge_kernel<64, true>, blocks, t, st, a);
-      if (D == 128 && !bf16) e = launch_pdl(gqa_paged_merge_kernel<128, false>, blocks, t, st, a);
-      if (D == 128 && bf16) e = launch_pdl(gqa_paged_merge_kernel<128, true>, blocks, t, st, a);
+      if (D == 64 && !bf16) e = one ? paged_merge_launch_w<64, false, 1>(a, st) : paged_merge_launch_w<64, false, 4>(a, st);
+      if (D == 64 && bf16) e = one ? paged_merge_launch_w<64, true, 1>(a, st) : paged_merge_launch_w<64, true, 4>(a, st);
+      if (D == 128 && !bf16)
+        e = one ? paged_merge_launch_w<128, false, 1>(a, st) : paged_merge_launch_w<128, false, 4>(a, st);
+      if (D == 128 && bf16) e = one ? paged_merge_launch_w<128, true, 1>(a, st) : paged_merge_launch_w<128, true, 4>(a, st);
       if (e != cudaSuccess) return GQA_ERR_CUDA;
     }
   }

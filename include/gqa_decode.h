@@ -63,8 +63,9 @@ typedef enum {
 typedef struct {
   int n_splits;          /* contiguous calls: splits per (sequence, KV head); 0 = heuristic */
   int merge_mode;        /* how a unit's splits are folded: 0 = automatic (the last-arriving CTA of the
-                            unit in the same kernel, except for the tcgen05 kernel when a unit's
-                            partials exceed 256 KB), 1 = separate merge kernel, 2 = last-arriving CTA */
+                            unit in the same kernel, except above 32 splits or, for the tcgen05
+                            kernel, when a unit's partials exceed 256 KB), 1 = separate merge kernel,
+                            2 = last-arriving CTA */
   uint32_t timeout_us;   /* limit of every device wait; 0 = 1,000,000 us */
   int test_stall_cta;    /* test hook, -1 = off.  Contiguous calls: linear id (x + X*(y + Y*z)) of
                             one CTA whose producer never loads its second tile; paged calls: the
