@@ -1,0 +1,124 @@
+"""Decode calls captured in CUDA graphs and run concurrently on several streams.
+
+Serving stacks capture the decode step in a CUDA graph and run independent batches on separate
+streams.  A call that launches two kernels (split pass + merge kernel, launched as a
+programmatic dependent) must replay correctly from a graph, and calls with separate workspaces
+on separate streams must not interfere.  Checked against the CPU float64 oracle with the f16
+parity tolerance (|o - o_ref| <= 2e-3 + 2e-3 |o_ref|, relative L2 <= 5e-3).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_inputs as gi
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gqa():
+    from decode_attention_03_gb300 import build
+    build.build()
+    import decode_attention_03_gb300._binding as b
+    assert torch.cuda.is_available()
+    return b
+
+
+def cuda(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def assert_close(got, ref, where):
+    got = got.detach().double().cpu().reshape(ref.shape)
+    mask = ~torch.isnan(ref)
+    g, r = got[mask], ref[mask].double()
+    assert torch.isfinite(g).all(), where
+    err = (g - r).abs()
+    assert not (err > 2e-3 + 2e-3 * r.abs()).any(), f"{where}: max err {float(err.max()):.3e}"
+    assert float((g - r).norm() / r.norm()) <= 5e-3, where
+
+
+@pytest.mark.parametrize("shape,kw", [((1, 16, 6000, 64, 8, 128), {}),                  # tcgen05 + merge kernel
+                                      ((2, 1, 4096, 8, 2, 64), {"n_splits": 64}),       # one-tile splits + merge
+                                      ((2, 1, 9000, 32, 8, 128), {})])                  # in-kernel merge
+def test_graph_replay_contiguous(gqa, shape, kw):
+    B, T, S, hq, hkv, D = shape
+    x = gi.make_contiguous(gi.custom(B, T, S, hq, hkv, D, 4000 + S))
+    q, k, v = cuda(x["q"]), cuda(x["k"]), cuda(x["v"])
+    out = torch.empty_like(q)
+    ws = torch.zeros(gqa.gqa_decode_workspace_size(B, T, S, hq, hkv, D, kw.get("n_splits", 0)), dtype=torch.uint8,
+                     device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        gqa.gqa_decode(q, k, v, hq, hkv, x["scale"], out=out, workspace_tensor=ws, **kw)   # warm-up, outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        gqa.gqa_decode(q, k, v, hq, hkv, x["scale"], out=out, workspace_tensor=ws, **kw)
+    ref = oracle.decode(x["q"], x["k"], x["v"], hq, hkv, D, x["scale"])
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert_close(out, ref, f"graph replay {shape}")
+    # new inputs in the captured buffers: the replay computes on them
+    x2 = gi.make_contiguous(gi.custom(B, T, S, hq, hkv, D, 4100 + S))
+    q.copy_(cuda(x2["q"])), k.copy_(cuda(x2["k"])), v.copy_(cuda(x2["v"]))
+    g.replay()
+    torch.cuda.synchronize()
+    assert_close(out, oracle.decode(x2["q"], x2["k"], x2["v"], hq, hkv, D, x2["scale"]), "graph replay, new inputs")
+    assert gqa.gqa_workspace_check(ws) == gqa.GQA_OK
+
+
+def test_graph_replay_paged(gqa):
+    w = gi.custom(16, 1, 3000, 32, 8, 128, 4200, kind="paged", block_size=16, partition_size=512,
+                  len_lo=1, len_hi=3000)
+    p = gi.make_paged(w)
+    q = cuda(p["q"]).reshape(16, -1)
+    kp, vp, tb, ln = cuda(p["k_pool"]), cuda(p["v_pool"]), cuda(p["block_tables"]), cuda(p["seq_lens"])
+    out = torch.empty_like(q)
+    ws = torch.zeros(gqa.gqa_paged_workspace_size(16, 32, 8, 128, p["max_seq_len"], 512), dtype=torch.uint8,
+                     device="cuda")
+    s = torch.cuda.Stream()
+    call = lambda: gqa.gqa_decode_paged(q, kp, vp, tb, ln, 32, 8, p["scale"], max_seq_len=p["max_seq_len"],
+                                        out=out, workspace_tensor=ws)
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    ref = oracle.decode_paged(p["q"], p["k_pool"], p["v_pool"], p["block_tables"], p["seq_lens"], 32, 8, 128,
+                              p["scale"], 16).reshape(16, -1)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert_close(out, ref, "paged graph replay")
+    assert gqa.gqa_workspace_check(ws) == gqa.GQA_OK
+
+
+def test_concurrent_streams(gqa):
+    """Four calls on four streams at once (different shapes and kernels), each with its own workspace."""
+    cases = [(1, 16, 5000, 64, 8, 128), (2, 1, 7000, 32, 8, 128), (1, 4, 3000, 64, 8, 64), (3, 2, 2500, 16, 2, 128)]
+    xs, outs, wss, streams = [], [], [], []
+    for i, (B, T, S, hq, hkv, D) in enumerate(cases):
+        x = gi.make_contiguous(gi.custom(B, T, S, hq, hkv, D, 4300 + i))
+        xs.append((x, cuda(x["q"]), cuda(x["k"]), cuda(x["v"])))
+        wss.append(torch.zeros(gqa.gqa_decode_workspace_size(B, T, S, hq, hkv, D, 0), dtype=torch.uint8,
+                               device="cuda"))
+        streams.append(torch.cuda.Stream())
+    torch.cuda.synchronize()
+    for rep in range(3):
+        outs = []
+        for (x, q, k, v), ws, s, c in zip(xs, wss, streams, cases):
+            with torch.cuda.stream(s):
+                outs.append(gqa.gqa_decode(q, k, v, c[3], c[4], x["scale"], workspace_tensor=ws, stream=s))
+        torch.cuda.synchronize()
+        for (x, _, _, _), o, c in zip(xs, outs, cases):
+            assert_close(o, oracle.decode(x["q"], x["k"], x["v"], c[3], c[4], c[5], x["scale"]), f"stream {c} rep {rep}")
+    for ws in wss:
+        assert gqa.gqa_workspace_check(ws) == gqa.GQA_OK
