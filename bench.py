@@ -21,6 +21,7 @@ from __future__ import annotations
 import argparse
 import glob
 import hashlib
+import re
 import json
 import math
 import os
@@ -109,15 +110,23 @@ KERNEL_SOURCES = {
 }
 
 
-def kernel_source_hash(kernel: str) -> str:
+def _code_only(text: str) -> str:
+    """Source without comments and blank-line / trailing-space differences: a comment edit does not
+    change the kernel the counters were taken on."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
+def kernel_source_hash(kernel: str, root: str = ROOT) -> str:
     h = hashlib.sha256()
     files = set()
     for pat in KERNEL_SOURCES[kernel]:
-        files.update(glob.glob(os.path.join(ROOT, "decode_attention_03_gb300", "csrc", pat)))
+        files.update(glob.glob(os.path.join(root, "decode_attention_03_gb300", "csrc", pat)))
     for p in sorted(files):
-        with open(p, "rb") as f:
+        with open(p, encoding="utf-8") as f:
             h.update(os.path.basename(p).encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
