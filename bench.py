@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--workload", choices=sorted(gi.WORKLOADS), default="long")
     ap.add_argument("--s-kv", type=int, default=0,
                     help="contiguous workloads: override S_kv (smaller cases for profiler captures)")
+    ap.add_argument("--elem", choices=["f16", "bf16"], default="f16",
+                    help="element type of Q, K, V and O (the same draws, rounded to bfloat16 for bf16)")
     ap.add_argument("--block-size", type=int, default=0,
                     help="paged workload: override the KV block size")
     ap.add_argument("--head-group", type=int, default=0,
@@ -203,9 +205,11 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------------------------
-def load_inputs(name: str, s_kv: int = 0, block_size: int = 0, partition_size: int = -1):
+def load_inputs(name: str, s_kv: int = 0, block_size: int = 0, partition_size: int = -1, elem: str = "f16"):
     import dataclasses
     w = gi.WORKLOADS[name]
+    if elem != w.elem:
+        w = dataclasses.replace(w, name=f"{w.name}[{elem}]", elem=elem)
     if partition_size >= 0 and w.kind == "paged" and partition_size != w.partition_size:
         w = dataclasses.replace(w, name=f"{w.name}[partition={partition_size}]", partition_size=int(partition_size))
     if s_kv and w.kind == "contiguous" and s_kv != w.S_kv:
@@ -216,9 +220,17 @@ def load_inputs(name: str, s_kv: int = 0, block_size: int = 0, partition_size: i
     return w, x
 
 
+def host_tensor(a: np.ndarray) -> torch.Tensor:
+    """A CPU tensor of an input array: bfloat16 bit patterns (uint16) become torch.bfloat16."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(a)
+
+
 def to_device(x: dict, dev):
     keys = ("q", "k", "v") if "k" in x else ("q", "k_pool", "v_pool", "block_tables", "seq_lens")
-    return {k: torch.from_numpy(np.ascontiguousarray(x[k])).to(dev) for k in keys}
+    return {k: host_tensor(x[k]).to(dev) for k in keys}
 
 
 def make_step(pkg, w, x, d, out, ws, args):
@@ -242,14 +254,18 @@ def oracle_sample(x, w, target_s: float):
     import oracle
     threads = os.cpu_count() or 1
     torch.set_num_threads(threads)
+
+    def vals(a):   # exact values of the inputs (bfloat16 bit patterns decoded)
+        return a if w.elem == "f16" else gi.values(a, w.elem)
+
     if w.kind == "contiguous":
         S = x["k"].shape[1]
         s_len = min(S, 4096)
         units = [(0, 0)]
 
         def run(n):
-            oracle.decode(x["q"][:1], x["k"][:1, :n], x["v"][:1, :n], w.h_q, w.h_kv, w.d_head, w.scale,
-                          units=units)
+            oracle.decode(vals(x["q"][:1]), vals(x["k"][:1, :n]), vals(x["v"][:1, :n]), w.h_q, w.h_kv, w.d_head,
+                          w.scale, units=units)
 
         def nbytes(n):
             return 2 * n * w.d_head * 2 + 2 * w.T_q * w.G * w.d_head * 2
@@ -272,6 +288,7 @@ def oracle_sample(x, w, target_s: float):
         return reps * nbytes(s_len) / t_tot, desc, threads
     else:
         lens = x["seq_lens"]
+        q, kp, vp = vals(x["q"]), vals(x["k_pool"]), vals(x["v_pool"])
         seqs = []
         total, t_tot, reps = 0, 0.0, 0
         row = w.h_kv * w.d_head * 2
@@ -280,8 +297,8 @@ def oracle_sample(x, w, target_s: float):
         while t_tot < target_s or reps == 0:
             b = order[i % len(order)]
             t0 = time.perf_counter()
-            oracle.decode_paged_seq(x["q"], x["k_pool"], x["v_pool"], x["block_tables"], lens, b, w.h_q, w.h_kv,
-                                    w.d_head, w.scale, w.block_size)
+            oracle.decode_paged_seq(q, kp, vp, x["block_tables"], lens, b, w.h_q, w.h_kv, w.d_head, w.scale,
+                                    w.block_size, w.layout)
             t_tot += time.perf_counter() - t0
             total += 2 * int(lens[b]) * row + 2 * w.h_q * w.d_head * 2
             reps += 1
@@ -295,7 +312,7 @@ def run_reference(args, rank, world):
     """The oracle as the reference arm: host cores, bounded samples, the same metric."""
     if rank != 0:
         return 0
-    w, x = load_inputs(args.workload, args.s_kv, args.block_size, args.partition_size)
+    w, x = load_inputs(args.workload, args.s_kv, args.block_size, args.partition_size, args.elem)
     steps = args.steps if args.steps is not None else 5
     warm = args.warmup if args.warmup is not None else 1
     per_step = max(0.2, min(10.0, 150.0 / max(1, steps + warm)))
@@ -354,13 +371,14 @@ def main():
     _b.build()
     import decode_attention_03_gb300 as pkg
 
-    w, x = load_inputs(args.workload, args.s_kv, args.block_size, args.partition_size)
+    w, x = load_inputs(args.workload, args.s_kv, args.block_size, args.partition_size, args.elem)
     d = to_device(x, dev)
     bytes_step = gi.kv_bytes(x)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     big = bytes_step > 2 * l2
     stream = torch.cuda.Stream(dev)
-    out = torch.empty(w.batch * w.T_q * w.h_q * w.d_head, dtype=torch.float16, device=dev)
+    out = torch.empty(w.batch * w.T_q * w.h_q * w.d_head, dtype=torch.bfloat16 if w.elem == "bf16" else torch.float16,
+                      device=dev)
     out = out.reshape(w.batch, w.T_q, -1) if w.kind == "contiguous" else out.reshape(w.batch, -1)
     if w.kind == "contiguous":
         nbytes = pkg.gqa_decode_workspace_size(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head, args.n_splits)
@@ -481,7 +499,7 @@ def main():
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
             "warmup": warm, "ms_per_step": round(ms_step, 6), "us_per_step": round(ms_step * 1e3, 3),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.elem,
             "data": "synthetic",
             "config": dict(config_of(w, x, n_splits), accum="f32",
                            l2=("inputs larger than L2, no flush" if flush is None
@@ -501,7 +519,7 @@ def main():
 
 def end_to_end(pkg, w, x, d, out, ws, stream, args, steps_hint):
     keys = list(d.keys())
-    host = {k: torch.from_numpy(np.ascontiguousarray(x[k])).pin_memory() for k in keys}
+    host = {k: host_tensor(x[k]).pin_memory() for k in keys}
     host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = host_out.numel() * host_out.element_size()

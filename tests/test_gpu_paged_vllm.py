@@ -200,3 +200,25 @@ def test_vllm_timeout_is_reported_not_hung(gqa):
     o = run(gqa, p, partition_size=512, workspace_tensor=ws)
     assert gqa.gqa_workspace_check(ws) == gqa.GQA_OK
     assert_close(o, ref(p), "vllm after a timeout")
+
+
+@pytest.mark.parametrize("layout", ["rows", "vllm"])
+def test_partition_at_the_box_table_limit(gqa, layout):
+    """Block size 8 and an 8192-key single-pass partition: 1024 TMA boxes in one work item, the
+    most the scheduler's per-item table holds (one more block per partition is rejected)."""
+    N, bs = 6, 8
+    w = gi.custom(N, 1, 8192, 16, 4, 64, 3400, kind="paged", block_size=bs, partition_size=8192,
+                  len_lo=7000, len_hi=8192, layout=layout)
+    p = gi.make_paged(w)
+    fn = gqa.gqa_decode_paged_vllm if layout == "vllm" else gqa.gqa_decode_paged
+    args = (dev(p["q"]).reshape(N, -1), dev(p["k_pool"]), dev(p["v_pool"]), dev(p["block_tables"]),
+            dev(p["seq_lens"]), 16, 4, p["scale"])
+    o = fn(*args, max_seq_len=8192, partition_size=8192, head_group=1 if layout == "vllm" else 0)
+    torch.cuda.synchronize()
+    assert gqa.gqa_paged_plan(N, 16, 4, 64, 8192, 8192, block_size=bs)[2] == 1     # single pass
+    assert_close(o, ref(p) if layout == "vllm" else
+                 torch.from_numpy(np.asarray(oracle.decode_paged(p["q"], p["k_pool"], p["v_pool"], p["block_tables"],
+                                                                 p["seq_lens"], 16, 4, 64, p["scale"], bs)))
+                 .reshape(N, -1), f"8192-key partition, block 8 ({layout})")
+    with pytest.raises(gqa.GQAError):
+        fn(*args, max_seq_len=8192, partition_size=8256)
