@@ -210,13 +210,13 @@ gqa_status encode_vllm_v(CUtensorMap* map, const void* base, uint64_t num_blocks
 // long split beats two shorter ones (long context: 591 vs 608 us; 8 x 32768 keys: 153
 // vs 156 us).  Prior art: page "muh_cc_dispatch.py", grid_even_share (grid = min(tiles,
 // SMs x subscription), even shares of tiles).
-int heuristic_splits(int64_t units, int64_t tiles, int sms, int occ) {
+int heuristic_splits(int64_t units, int64_t tiles, int sms, int occ, int min_tiles = kMinTilesPerSplit) {
   const int64_t slots = (int64_t)sms * occ;
   if (tiles <= 0) return 1;
   if (units >= sms) return 1;
   int64_t n = (sms + units - 1) / units;
   if (n > slots / units) n = slots / units;
-  const int64_t cap = tiles / kMinTilesPerSplit;
+  const int64_t cap = tiles / min_tiles;
   if (n > cap) n = cap;
   if (n < 1) n = 1;
   if (n > 65535) n = 65535;
@@ -299,6 +299,9 @@ gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_
     int sms = 0, occ = 0;
     gqa_status s = device_info(p->di, p->cls, p->tc ? 2 : 0, 0, &sms, &occ);
     if (s != GQA_OK) return s;
+    // one-tile splits even where a stage holds two tiles (d_head 64): the latency-bound tiny
+    // workload measured 12.3 us with 64 one-tile splits and the merge kernel, 13.5 us with 32
+    // two-tile splits folded in-kernel
     p->n_splits = heuristic_splits(p->units, p->tiles, sms, occ);
   } else {
     p->n_splits = 1;
@@ -400,7 +403,7 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
 
   CUtensorMap tk, tv;
   const uint64_t cols = (uint64_t)h_kv * D, nrows = (uint64_t)B * (uint64_t)S_kv;
-  const uint32_t box_rows = p.tc ? kTcKeys : kTile;   // keys per pipeline stage
+  const uint32_t box_rows = p.tc ? kTcKeys : kTile * split_sub(D);   // keys per pipeline stage
   if ((s = encode_map(&tk, k, cols, nrows, box_rows, (uint32_t)D / 64, bf16)) != GQA_OK) return s;
   if ((s = encode_map(&tv, v, cols, nrows, box_rows, (uint32_t)D / 64, bf16)) != GQA_OK) return s;
 

@@ -40,19 +40,20 @@ template <int D, int CLS, bool CAUSAL, bool BF16>
 struct Inst {
   static constexpr int NT = cls_nt(CLS);
   static constexpr int WN = cls_wn(CLS);
-  static constexpr int STAGES = stages_for<D, NT, WN>();
-  using C = Cfg<D, NT, WN, STAGES>;
+  static constexpr int SUB = split_sub(D);
+  static constexpr int STAGES = stages_for<D, NT, WN>() / SUB;   // ring stages of SUB tiles
+  using C = Cfg<D, NT, WN, STAGES * SUB>;
   static_assert(C::SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
   static cudaError_t prepare(int* occupancy) {
-    auto fn = gqa_split_kernel<D, NT, WN, STAGES, CAUSAL, BF16>;
+    auto fn = gqa_split_kernel<D, NT, WN, STAGES, SUB, CAUSAL, BF16>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, fn, C::THREADS, C::SMEM_BYTES);
   }
   static cudaError_t launch(dim3 grid, cudaStream_t st, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a) {
-    gqa_split_kernel<D, NT, WN, STAGES, CAUSAL, BF16><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tk, tv, a);
+    gqa_split_kernel<D, NT, WN, STAGES, SUB, CAUSAL, BF16><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tk, tv, a);
     return cudaGetLastError();
   }
 };
