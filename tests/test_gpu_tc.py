@@ -94,6 +94,17 @@ def test_tc_forced_on_small_units(gqa, rows):
     assert_close(run(gqa, x, mma_path=1), r, f"mma.sync G={G} T={T}")
 
 
+@pytest.mark.parametrize("hq,T", [(20, 1), (33, 1), (16, 3), (8, 6), (64, 1)])
+@pytest.mark.parametrize("D", [64, 128])
+def test_tc_odd_row_counts(gqa, hq, T, D):
+    """Row counts that are not multiples of a warp (20, 33, 48) and that leave warps of a
+    warpgroup idle, with a ragged key tail, plain and causal."""
+    x = gi.make_contiguous(gi.custom(2, T, 1000 + 7 * hq, hq, 1, D, 2150 + hq * T + D))
+    assert_close(run(gqa, x, mma_path=2), ref(x), f"rows hq={hq} T={T} D={D}")
+    assert_close(run(gqa, x, mma_path=2, n_splits=3, causal=True), ref(x, causal=True),
+                 f"rows causal hq={hq} T={T} D={D}")
+
+
 def test_tc_forced_on_ragged_workload(gqa):
     x = gi.make("ragged")
     assert_close(run(gqa, x, mma_path=2), ref(x), "ragged on tcgen05")
@@ -115,10 +126,12 @@ def test_tc_causal(gqa, n_splits):
 
 
 @pytest.mark.parametrize("rng", [(0, 3000), (100, 1000), (2999, 1), (5, 0)])
-def test_tc_partial(gqa, rng):
-    """The partial a split emits is the exact-max partial (m = the row max, l and O relative to it)."""
+@pytest.mark.parametrize("T", [16, 2])
+def test_tc_partial(gqa, rng, T):
+    """The partial a split emits is the exact-max partial (m = the row max, l and O relative to it),
+    with all 128 TMEM lanes holding rows (T = 16) and with only 16 of them (T = 2)."""
     s0, n = rng
-    B, T, hq, hkv, D = 2, 16, 64, 8, 64
+    B, hq, hkv, D = 2, 64, 8, 64
     x = gi.make_contiguous(gi.custom(B, T, 3000, hq, hkv, D, 2300, spike_frac=0.01, spike_mult=8.0))
     k, v = x["k"].copy(), x["v"].copy()
     mask = np.ones(3000, dtype=bool)
