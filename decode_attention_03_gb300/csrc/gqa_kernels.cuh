@@ -58,6 +58,7 @@ constexpr int kMaxBoxesPerPart = 1024;  // paged: TMA boxes (blocks or block sli
 // instead of 306.8 us; 64 sequences of 1024-16384 keys: 333.0 instead of 331.9 us)
 constexpr int kItemSlots = 2;
 constexpr int kPagedSeqs = 1024;   // paged kernel: sequences per launch (the host splits larger batches)
+constexpr int kSizeClasses = 64;   // paged kernel, single pass: length classes of the longest-first order
 
 struct DecodeArgs {
   const __half* q;        // (B, T_q, h_q*D)
@@ -120,7 +121,7 @@ struct Cfg {
   static constexpr int PCTRL_OFF = PIPE_BYTES + EPI_BUFS * PSCRATCH_STRIDE;
   static constexpr int PCTRL_BYTES = (2 * STAGES + 2 * kItemSlots + 2 * EPI_BUFS) * 8 + 16 +
                                      (kItemSlots + EPI_BUFS) * 48 + kItemSlots * kMaxBoxesPerPart * 4 +
-                                     (2 * kPagedSeqs + 1) * 4;
+                                     (3 * kPagedSeqs + 1 + kSizeClasses) * 4;
   static constexpr int PSMEM_BYTES = 1024 + PCTRL_OFF + PCTRL_BYTES;
   static constexpr int PTHREADS = (CONSUMERS + 3) * 32;          // + producer, scheduler, epilogue
 };
@@ -729,6 +730,45 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 // =====================================================================================
 // paged K/V: persistent CTAs over (sequence, partition, KV head) items
 // =====================================================================================
+// Longest-first order of the non-empty sequences of a single-pass launch (every length <= P;
+// one warp, the same result in every CTA): a stable counting sort on kSizeClasses classes of
+// the length, longest class first; order[0, non-empty sequences) receives the indices.
+__device__ __forceinline__ void sort_by_length(const int* lens, int N, int P, int* order, int* cls, int lane) {
+  for (int c = lane; c < kSizeClasses; c += 32) cls[c] = 0;
+  __syncwarp();
+  auto class_of = [&](int i) {
+    const int len = i < N ? lens[i] : 0;
+    return len > 0 ? kSizeClasses - 1 - (int)((int64_t)(len - 1) * kSizeClasses / P) : kSizeClasses;
+  };
+  for (int base = 0; base < N; base += 32) {   // class sizes
+    const int c = class_of(base + lane);
+    const unsigned peers = __match_any_sync(0xffffffffu, c);
+    if (c < kSizeClasses && lane == __ffs(peers) - 1) cls[c] += __popc(peers);
+    __syncwarp();
+  }
+  static_assert(kSizeClasses == 64, "two classes per lane");
+  const int h0 = cls[2 * lane], h1 = cls[2 * lane + 1];
+  int incl = h0 + h1;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  __syncwarp();
+  cls[2 * lane] = incl - h0 - h1;             // first slot of each class
+  cls[2 * lane + 1] = incl - h1;
+  __syncwarp();
+  for (int base = 0; base < N; base += 32) {   // scatter, in index order within a class
+    const int i = base + lane;
+    const int c = class_of(i);
+    const unsigned peers = __match_any_sync(0xffffffffu, c);
+    if (c < kSizeClasses) order[cls[c] + __popc(peers & ((1u << lane) - 1u))] = i;
+    __syncwarp();
+    if (c < kSizeClasses && lane == __ffs(peers) - 1) cls[c] += __popc(peers);
+    __syncwarp();
+  }
+}
+
 struct ItemDesc {
   int b, g, p, kind;        // g: first KV head of the item's group; kind: 0 partition, 2 no more items
   int n_tiles, n_parts, n_boxes, item;   // item: queue index (test hook)
@@ -739,8 +779,9 @@ static_assert(sizeof(ItemDesc) == 48, "descriptor slot size");
 // Warps: consumers 0..CONSUMERS-1, TMA producer CONSUMERS, scheduler CONSUMERS+1,
 // epilogue CONSUMERS+2.
 //  * scheduler: takes item indices from the queue (one at a time), maps an index to
-//    (sequence, partition, group of HG KV heads) through a prefix sum of the
-//    sequences' partition counts (so no index is empty), reads the partition's block
+//    (sequence, partition, group of HG KV heads) through a prefix sum of the sequences'
+//    partition counts (so no index is empty; a single-pass launch takes the sequences
+//    longest first), reads the partition's block
 //    ids and publishes a descriptor into a kItemSlots-deep ring -- claiming an item only
 //    when a slot is free.
 //  * producer: for each descriptor, TMA-loads the partition's K/V blocks into the ring,
@@ -778,6 +819,8 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   int* boxy = reinterpret_cast<int*>(edesc + C::EPI_BUFS);      // [kItemSlots][kMaxBoxesPerPart] box rows
   int* pre = boxy + kItemSlots * kMaxBoxesPerPart;              // [N + 1] partition-count prefix
   int* lens_s = pre + kPagedSeqs + 1;                           // [N] clamped lengths
+  int* order = lens_s + kPagedSeqs;                             // [N] single pass: sequences, longest first
+  int* cls = order + kPagedSeqs;                                // [kSizeClasses] counting-sort cursors
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P = a.partition_size;
@@ -865,6 +908,7 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 
   // ---------------------------------------------------------------- scheduler warp
   if (warp == C::CONSUMERS + 1) {
+    bool sorted = false;
     for (int k = 0;; ++k) {
       const int slot = k % kItemSlots;
       int ok = 1;
@@ -888,17 +932,27 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       if ((int64_t)it < total) {
         d.g = (int)(it % (uint32_t)groups) * HG;
         const int j = (int)(it / (uint32_t)groups);
-        int lo = 0, hi = N;                        // pre[lo] <= j < pre[hi]
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (pre[mid] <= j) lo = mid; else hi = mid;
+        if (a.n_splits > 1) {
+          int lo = 0, hi = N;                        // pre[lo] <= j < pre[hi]
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pre[mid] <= j) lo = mid; else hi = mid;
+          }
+          d.b = lo;
+          d.p = j - pre[lo];
+        } else {
+          // single pass: sequences longest first, so that the queue ends with its shortest items
+          if (!sorted) {
+            sort_by_length(lens_s, N, P, order, cls, lane);
+            sorted = true;
+          }
+          d.b = order[j];
+          d.p = 0;
         }
-        d.b = lo;
-        d.p = j - pre[lo];
-        d.n_parts = pre[lo + 1] - pre[lo];
+        d.n_parts = (lens_s[d.b] + P - 1) / P;
         d.kind = 0;
         d.key_begin = (int64_t)d.p * P;
-        d.key_end = min(d.key_begin + P, (int64_t)lens_s[lo]);
+        d.key_end = min(d.key_begin + P, (int64_t)lens_s[d.b]);
         d.n_tiles = (int)((d.key_end - d.key_begin + TK - 1) / TK);
         d.n_boxes = (int)((d.key_end - d.key_begin + br - 1) / br);
         // pool row of every box of the partition (-1: block id outside the pool, not loaded),

@@ -68,9 +68,11 @@ def ref(p, seqs=None):
                                p["scale"], p["block_size"], seqs=seqs, layout="vllm").reshape(N, -1)
 
 
-def edge_case(bs, hq, hkv, D, seed, elem="f16"):
-    """Sequences of 0, 1, block +- 1, partition +- 1 ... keys; NaN in every unused tail slot."""
-    lens = np.array([0, 1, 15, 16, 17, 511, 512, 513, 1000, 64, 2049], dtype=np.int32)
+def edge_case(bs, hq, hkv, D, seed, elem="f16", lens=None):
+    """Sequences of 0, 1, block +- 1, partition +- 1 ... keys (or `lens`); NaN in every unused
+    tail slot."""
+    if lens is None:
+        lens = np.array([0, 1, 15, 16, 17, 511, 512, 513, 1000, 64, 2049], dtype=np.int32)
     N = len(lens)
     nblk = (lens + bs - 1) // bs
     num_blocks = int(nblk.sum()) + 3
@@ -150,6 +152,26 @@ def test_v1_workload_sampled(gqa):
     r = ref(p, seqs)
     assert_close(run(gqa, p, partition_size=2048), r, "paged_v1, single pass")
     assert_close(run(gqa, p), r, "paged_v1, 512-token partitions")
+
+
+def test_single_pass_takes_every_sequence_once(gqa):
+    """A single-pass launch hands its sequences out longest first (a counting sort in every CTA):
+    300 sequences whose lengths repeat (ties), include 0, 1 and the partition itself, and span
+    every length class; every output row is checked, on both cache layouts."""
+    rng = np.random.Generator(np.random.PCG64(3500))
+    lens = np.concatenate([np.array([0, 1, 2048, 2048, 2047, 0, 32, 33, 31, 1024] * 6),
+                           rng.integers(1, 2049, 240)]).astype(np.int32)
+    rng.shuffle(lens)
+    p = edge_case(16, 8, 2, 64, 3501, lens=lens)
+    assert gqa.gqa_paged_plan(len(lens), 8, 2, 64, 2048, 2048, block_size=16, vllm_layout=True)[2] == 1
+    r = ref(p)
+    assert_close(run(gqa, p, partition_size=2048), r, "single pass, vLLM caches")
+    kp, vp = p["rows"]
+    N = len(lens)
+    o = gqa.gqa_decode_paged(dev(p["q"]).reshape(N, -1), dev(kp), dev(vp), dev(p["block_tables"]),
+                             dev(p["seq_lens"]), 8, 2, p["scale"], max_seq_len=2048, partition_size=2048)
+    torch.cuda.synchronize()
+    assert_close(o, r, "single pass, row pools")
 
 
 def test_vllm_workload_sampled(gqa):
