@@ -249,12 +249,20 @@ def make_step(pkg, w, x, d, out, ws, args):
     return step
 
 
-def oracle_sample(x, w, target_s: float):
-    """Time the CPU oracle on a bounded sample of the workload; returns (bytes/s, desc, threads)."""
+def oracle_sample(x, w, target_s: float, threads: int = 0):
+    """Time the CPU oracle on a bounded sample of the workload (all host cores, or ``threads``);
+    returns (bytes/s, desc, threads)."""
     import oracle
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
+    prev = torch.get_num_threads()
     torch.set_num_threads(threads)
+    try:
+        return _oracle_sample(oracle, x, w, target_s, threads)
+    finally:
+        torch.set_num_threads(prev)
 
+
+def _oracle_sample(oracle, x, w, target_s: float, threads: int):
     def vals(a):   # exact values of the inputs (bfloat16 bit patterns decoded)
         return a if w.elem == "f16" else gi.values(a, w.elem)
 
@@ -484,6 +492,9 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         bps, desc, threads = oracle_sample(x, w, 10.0)
         cpu = {"value": round(bps / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc}
+        if w.name == "tiny":   # the launch-bound case: the oracle on one core as well
+            bps1, desc1, _ = oracle_sample(x, w, 3.0, threads=1)
+            cpu["one_core"] = {"value": round(bps1 / 1e9, 4), "cores": 1, "sample": desc1}
 
     if rank == 0:
         if w.kind == "paged":   # partition pass, plus the merge pass when a sequence spans partitions
