@@ -155,7 +155,16 @@ def workspace(nbytes: int, device=None, stream=None) -> torch.Tensor:
     with _ws_lock:
         t = _ws_cache.get(key)
         if t is None or t.numel() < nbytes:
+            # growing the cache (rare): the replaced workspace may still be in use on `stream`, and
+            # the new one is zero-filled on the current stream, which need not be `stream`; a device
+            # synchronisation orders both (not while a graph is being captured: there the fill is
+            # captured on the capturing stream)
+            capturing = torch.cuda.is_current_stream_capturing()
+            if not capturing:
+                torch.cuda.synchronize(dev)
             t = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=dev)
+            if not capturing:
+                torch.cuda.synchronize(dev)
             _ws_cache[key] = t
         return t
 

@@ -122,3 +122,16 @@ def test_concurrent_streams(gqa):
             assert_close(o, oracle.decode(x["q"], x["k"], x["v"], c[3], c[4], c[5], x["scale"]), f"stream {c} rep {rep}")
     for ws in wss:
         assert gqa.gqa_workspace_check(ws) == gqa.GQA_OK
+
+
+def test_cached_workspace_on_a_side_stream(gqa):
+    """Without a workspace argument the binding keeps one per (device, stream); one created for a
+    stream other than the current one is ready (zero-filled) before the call's kernels run there."""
+    x = gi.make_contiguous(gi.custom(1, 4, 30000, 64, 8, 128, 4400))
+    q, k, v = cuda(x["q"]), cuda(x["k"]), cuda(x["v"])
+    ref = oracle.decode(x["q"], x["k"], x["v"], 64, 8, 128, x["scale"])
+    for _ in range(2):
+        s = torch.cuda.Stream()
+        o = gqa.gqa_decode(q, k, v, 64, 8, x["scale"], stream=s)
+        s.synchronize()
+        assert_close(o, ref, "cached workspace, side stream")
