@@ -202,19 +202,21 @@ gqa_status encode_vllm_v(CUtensorMap* map, const void* base, uint64_t num_blocks
   return r == CUDA_SUCCESS ? GQA_OK : GQA_ERR_CUDA;
 }
 
-// Split count: about one (b, g, split) CTA per SM -- ceil(SMs / units) splits per unit --
-// with every CTA co-resident (at most the resident slots of the GPU) and each split at
-// least kMinTilesPerSplit tiles long (short sweeps are latency-bound: more, shorter splits
-// measured faster -- tiny workload, 4096 keys: 16 splits of 4 tiles 12.7 us, 64 of one tile
-// 11.9 us with the merge kernel).  Measured on GB300: one CTA per SM streaming a
-// long split beats two shorter ones (long context: 591 vs 608 us; 8 x 32768 keys: 153
-// vs 156 us).  Prior art: page "muh_cc_dispatch.py", grid_even_share (grid = min(tiles,
-// SMs x subscription), even shares of tiles).
+// Split count: about 1.25 (b, g, split) CTAs per SM -- ceil(1.25 SMs / units) splits per
+// unit -- with every CTA co-resident (at most the resident slots of the GPU) and each split
+// at least kMinTilesPerSplit tiles long (short sweeps are latency-bound: more, shorter
+// splits measured faster -- tiny workload, 4096 keys: 16 splits of 4 tiles 12.7 us, 64 of
+// one tile 11.9 us with the merge kernel).  Measured on GB300 (a CTA streams at about
+// 45 GB/s, bounded by its own ring, so a second CTA on some SMs adds bandwidth, while two on
+// every SM split the work too finely): long context, 8 KV heads, splits 16 / 19 / 24 / 32 /
+// 38 -> 610 / 591 / 586 / 603 / 597 us; 8 x 32768 keys, 64 units: 3 splits (192 CTAs) 153 us,
+// 4 splits 157 us.  Prior art: page "muh_cc_dispatch.py", grid_even_share (grid =
+// min(tiles, SMs x subscription), even shares of tiles).
 int heuristic_splits(int64_t units, int64_t tiles, int sms, int occ, int min_tiles = kMinTilesPerSplit) {
   const int64_t slots = (int64_t)sms * occ;
   if (tiles <= 0) return 1;
   if (units >= sms) return 1;
-  int64_t n = (sms + units - 1) / units;
+  int64_t n = ((int64_t)sms * 5 + units * 4 - 1) / (units * 4);
   if (n > slots / units) n = slots / units;
   const int64_t cap = tiles / min_tiles;
   if (n > cap) n = cap;
