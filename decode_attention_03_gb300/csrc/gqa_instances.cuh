@@ -16,8 +16,8 @@ constexpr int cls_wn(int cls) { return cls <= 1 ? 1 : (cls == 2 ? 2 : 4); }
 // pipeline depth: ~96 KB of K/V stages when two CTAs fit on an SM; ~192 KB when
 // one CTA per SM is all that fits anyway (merge scratch above 96 KB, or more than
 // half of the register file: d_head 128 with two warp columns).  A deeper ring is not
-// better where the split heuristic runs one CTA per SM anyway: 6 x 32 KB stages took the
-// 2^20-key step from 581-592 to 631 us on GB300.
+// better where the split heuristic runs about one CTA per SM anyway: 6 x 32 KB stages took
+// the 2^20-key step (19 splits) from 581-592 to 631 us on GB300.
 template <int D, int NT, int WN>
 constexpr int stages_for() {
   constexpr int stage = 2 * (D / 64) * kTile * 128;
