@@ -39,8 +39,9 @@ constexpr int kInKernelMaxSplits = 32;
 // (vLLM layout, block 16, h_q 32, h_kv 8, d 128; us, v1 / v2-512: 384 seqs of 128-2048 keys
 // 398 / 354; 1024 seqs 797 / 787; 2048 seqs 1618 / 1616; 512 seqs of 2048-8192 keys 1886 / 1637;
 // 1024 seqs of 1024-8192 keys 3112 / 2945): a v1 item is a whole sequence, and whichever SMs take
-// the longest ones finish last.  So the automatic choice is v2; v1 is a partition_size of at
-// least max_seq_len.
+// the longest ones finish last.  (Handing the sequences of a single pass out longest first, and a
+// scheduler that claims items only as it needs them, later brought the first case to 314.5 /
+// 306.5.)  So the automatic choice is v2; v1 is a partition_size of at least max_seq_len.
 constexpr int kV2Partition = 512;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
