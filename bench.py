@@ -23,7 +23,6 @@ import glob
 import hashlib
 import re
 import json
-import math
 import os
 import statistics
 import subprocess

@@ -33,8 +33,7 @@ whole key range; a torch float64 matmul is the only library primitive.
 """
 from __future__ import annotations
 
-import math
-from typing import Iterable, List, Optional, Sequence, Tuple
+from typing import Iterable, Optional, Sequence, Tuple
 
 import numpy as np
 import torch

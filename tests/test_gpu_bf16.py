@@ -8,7 +8,6 @@ relative L2 error must stay below 1e-2 (rounding noise alone is about 2.3e-3).
 """
 from __future__ import annotations
 
-import math
 
 import numpy as np
 import pytest

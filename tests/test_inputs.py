@@ -1,6 +1,5 @@
 """The seeded input generators: frozen draws and workload structure (CPU only)."""
 import numpy as np
-import pytest
 
 import gqa_inputs as gi
 
