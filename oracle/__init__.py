@@ -20,7 +20,6 @@ Pins (brute force, closed forms, library special cases, invariants) are in
 ``tests/test_oracle_pins.py``; every function here is pinned.
 """
 from .gqa_oracle import (  # noqa: F401
-    attend_rows,
     partial_rows,
     merge_pair,
     merge_parts,
@@ -29,7 +28,12 @@ from .gqa_oracle import (  # noqa: F401
     decode_unit,
     decode_partial,
     gather_paged,
+    gather_paged_vllm,
     decode_paged,
     decode_paged_seq,
-    round_f16,
 )
+
+__all__ = [
+    "partial_rows", "merge_pair", "merge_parts", "normalize", "decode", "decode_unit",
+    "decode_partial", "gather_paged", "gather_paged_vllm", "decode_paged", "decode_paged_seq",
+]

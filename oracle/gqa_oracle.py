@@ -39,9 +39,9 @@ import numpy as np
 import torch
 
 __all__ = [
-    "attend_rows", "partial_rows", "merge_pair", "merge_parts", "normalize",
-    "decode", "decode_unit", "decode_partial", "gather_paged", "decode_paged",
-    "decode_paged_seq", "round_f16",
+    "partial_rows", "merge_pair", "merge_parts", "normalize",
+    "decode", "decode_unit", "decode_partial", "gather_paged", "gather_paged_vllm", "decode_paged",
+    "decode_paged_seq",
 ]
 
 NEG_INF = float("-inf")
@@ -88,12 +88,6 @@ def normalize(l, o):
     safe = torch.where(l > 0, l, torch.ones_like(l))
     out = o / safe[..., None]
     return torch.where((l > 0)[..., None], out, torch.zeros_like(out))
-
-
-def attend_rows(q_rows, k_rows, v_rows, scale: float):
-    """Normalised attention output of query rows ``(n, D)`` over keys ``(S, D)``."""
-    m, l, o = partial_rows(q_rows, k_rows, v_rows, scale)
-    return normalize(l, o)
 
 
 # ---------------------------------------------------------------------------
@@ -274,8 +268,3 @@ def decode_paged(q, k_pool, v_pool, block_tables, seq_lens, h_q: int, h_kv: int,
                                   h_q, h_kv, D, scale, block_size, layout)
     return out
 
-
-def round_f16(x):
-    """Round float64 results to float16 (nearest even) and back: the output
-    dtype of the pages' decode kernels is float16."""
-    return _f64(x).to(torch.float16).to(torch.float64)

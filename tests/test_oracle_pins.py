@@ -168,6 +168,14 @@ def pin_split_merge(orc) -> bool:
         m, l, o = orc.merge_parts(ms, ls, os_)
         got = orc.normalize(l, o).reshape(B, T_q, h_q * D)
         ok &= _close(got, full)
+    # one unit (sequence b, KV head g) over a key range is the slice of the all-rows partial
+    G = h_q // h_kv
+    mp, lp, op = orc.decode_partial(x["q"], x["k"], x["v"], h_q, h_kv, D, scale, 13, 41)
+    for b in range(B):
+        for g in range(h_kv):
+            mu, lu, ou = orc.decode_unit(x["q"], x["k"], x["v"], b, g, h_q, h_kv, D, scale, 13, 41)
+            ok &= _close(mu, mp[b, :, g * G:(g + 1) * G]) and _close(lu, lp[b, :, g * G:(g + 1) * G])
+            ok &= _close(ou, op[b, :, g * G:(g + 1) * G])
     return ok
 
 
@@ -191,6 +199,44 @@ def pin_merge_closed_form(orc) -> bool:
         ok &= _close(orc.normalize(l2, o2), ref)
         m3, l3, o3 = orc.merge_pair(e_m, e_l, e_o, e_m, e_l, e_o)
         ok &= bool(torch.isneginf(m3).all()) and float(l3[0]) == 0.0 and bool((o3 == 0).all())
+    return ok
+
+
+def pin_empty(orc) -> bool:
+    """Empty key ranges (reading R7 of the pages' merge): an empty partial is (-inf, 0, 0),
+    normalising l = 0 gives exactly 0 while the other rows are still divided by their l, an
+    all-empty merge normalises to 0, and a length-0 paged sequence has an all-zero output
+    (its neighbours unchanged)."""
+    f64 = torch.float64
+    ok = True
+    # closed form, mixed rows: O / l where l > 0, exactly 0 where l = 0
+    l = torch.tensor([2.0, 0.0, 4.0], dtype=f64)
+    o = torch.tensor([[2.0, -4.0], [0.0, 0.0], [4.0, 8.0]], dtype=f64)
+    got = orc.normalize(l, o)
+    ok &= _close(got, torch.tensor([[1.0, -2.0], [0.0, 0.0], [1.0, 2.0]], dtype=f64), 0.0)
+    # an empty key range through the partial path
+    x = _inputs(1, 2, 9, 4, 2, 8, 131)
+    m, l0, o0 = orc.decode_partial(x["q"], x["k"], x["v"], 4, 2, 8, 0.5, 3, 0)
+    ok &= bool(torch.isneginf(m).all()) and bool((l0 == 0).all()) and bool((o0 == 0).all())
+    ok &= _close(orc.normalize(l0, o0), torch.zeros(1, 2, 4, 8, dtype=f64), 0.0)
+    # merging only empty partials, then normalising: zeros
+    mm, lm, om = orc.merge_parts([m, m, m], [l0, l0, l0], [o0, o0, o0])
+    ok &= _close(orc.normalize(lm, om), torch.zeros(1, 2, 4, 8, dtype=f64), 0.0)
+    # a length-0 paged sequence among non-empty ones
+    w = gqa_inputs.custom(3, 1, 40, 4, 2, 8, 132, kind="paged", block_size=8, partition_size=64,
+                          len_lo=1, len_hi=40)
+    p = gqa_inputs.make_paged(w)
+    lens = p["seq_lens"].copy()
+    lens[1] = 0
+    one = orc.decode_paged_seq(p["q"], p["k_pool"], p["v_pool"], p["block_tables"], lens, 1, 4, 2, 8, 0.3, 8)
+    ok &= _close(one, torch.zeros(1, 4 * 8, dtype=f64), 0.0)
+    allp = orc.decode_paged(p["q"], p["k_pool"], p["v_pool"], p["block_tables"], lens, 4, 2, 8, 0.3, 8)
+    ok &= _close(allp[1], torch.zeros(1, 4 * 8, dtype=f64), 0.0)
+    for b in (0, 2):
+        L = int(lens[b])
+        kb = orc.gather_paged(p["k_pool"], p["block_tables"][b], L, 8)[None]
+        vb = orc.gather_paged(p["v_pool"], p["block_tables"][b], L, 8)[None]
+        ok &= _close(allp[b], orc.decode(p["q"][b:b + 1].reshape(1, 1, -1), kb, vb, 4, 2, 8, 0.3)[0])
     return ok
 
 
@@ -273,8 +319,15 @@ def pin_paged_vllm(orc) -> bool:
                     vc[n, g, dd, slot] = vp[n, slot, g * D + dd]
     rows = orc.decode_paged(p["q"], kp, vp, tab, lens, 8, 2, D, 0.3, bs)
     got = orc.decode_paged(p["q"], kc, vc, tab, lens, 8, 2, D, 0.3, bs, layout="vllm")
+    ok = True
+    for b in range(4):   # the gathered rows themselves, key by key, from the layout statement
+        L = int(lens[b])
+        kg, vg = orc.gather_paged_vllm(kc, vc, tab[b], L, bs)
+        kr = np.stack([kp[tab[b, j // bs], j % bs] for j in range(L)])
+        vr = np.stack([vp[tab[b, j // bs], j % bs] for j in range(L)])
+        ok &= np.array_equal(kg, kr) and np.array_equal(vg, vr)
     k2, v2 = gqa_inputs.to_vllm_layout(kp, vp, h_kv, D)      # the input module's rearrangement agrees
-    return _close(got, rows) and np.array_equal(k2, kc) and np.array_equal(v2, vc)
+    return ok and _close(got, rows) and np.array_equal(k2, kc) and np.array_equal(v2, vc)
 
 
 def pin_causal(orc) -> bool:
@@ -353,13 +406,22 @@ def _read_golden(path: str) -> dict:
 
 
 PINS = [pin_brute_force, pin_sdpa, pin_constant_scores, pin_one_hot, pin_single_key,
-        pin_split_merge, pin_merge_closed_form, pin_permutation, pin_shift, pin_paged, pin_paged_vllm, pin_causal,
+        pin_split_merge, pin_merge_closed_form, pin_empty, pin_permutation, pin_shift, pin_paged, pin_paged_vllm, pin_causal,
         pin_golden]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
 def test_pin_holds(pin):
     assert pin(gqa_oracle)
+
+
+def test_every_exported_function_is_pinned():
+    """Each function the oracle exports is called by name in at least one pin."""
+    import inspect
+    src = "\n".join(inspect.getsource(p) for p in PINS)
+    missing = [n for n in oracle.__all__ if f"orc.{n}(" not in src]
+    assert not missing, f"oracle functions no pin calls: {missing}"
+    assert sorted(oracle.__all__) == sorted(gqa_oracle.__all__)
 
 
 def test_golden_files_present():
@@ -450,6 +512,11 @@ def _m_no_normalize(l, o):
     return _f64(o)
 
 
+def _m_normalize_nan_when_empty(l, o):
+    l, o = _f64(l), _f64(o)
+    return o / l[..., None]
+
+
 def _m_vllm_chunk_swap(k_cache, v_cache, table_row, length, block_size):
     # reads the key's d as (x, D/x) instead of (D/x, x)
     kc, vc = np.asarray(k_cache), np.asarray(v_cache)
@@ -508,6 +575,7 @@ MUTANTS = {
     "merge_sign_flip": dict(merge_pair=_m_merge_sign),
     "merge_drops_l_term": dict(merge_pair=_m_merge_drop_l),
     "no_normalize": dict(normalize=_m_no_normalize),
+    "normalize_nan_for_empty_rows": dict(normalize=_m_normalize_nan_when_empty),
     "paged_slot_off_by_one": dict(gather_paged=_m_gather_off_by_one),
     "vllm_key_chunk_order_swapped": dict(gather_paged_vllm=_m_vllm_chunk_swap),
     "vllm_value_transposed": dict(gather_paged_vllm=_m_vllm_v_transposed),
