@@ -12,9 +12,9 @@ from __future__ import annotations
 import importlib
 
 _BINDING_NAMES = (
-    "gqa_decode", "gqa_decode_noalloc", "gqa_decode_partial", "gqa_merge", "gqa_merge_partial", "gqa_decode_paged",
+    "gqa_decode", "gqa_decode_noalloc", "gqa_decode_noalloc_check", "gqa_decode_partial", "gqa_merge", "gqa_merge_partial", "gqa_decode_paged",
     "gqa_decode_paged_vllm",
-    "gqa_decode_workspace_size", "gqa_paged_workspace_size", "gqa_decode_num_splits",
+    "gqa_decode_workspace_size", "gqa_workspace_size", "gqa_paged_workspace_size", "gqa_decode_num_splits",
     "gqa_decode_plan", "gqa_paged_plan",
     "gqa_workspace_init", "gqa_workspace_check", "gqa_status_string", "gqa_version",
     "GQAError", "gqa_options", "workspace", "lib", "LIB_PATH", "EXPORTED",

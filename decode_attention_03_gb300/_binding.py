@@ -61,6 +61,7 @@ _SIGS = {
     "gqa_decode_plan": ([_i, _i, _i64, _i, _i, _i, _opt, _p, _p, _p], _i),
     "gqa_paged_plan": ([_i, _i, _i, _i, _i, _i, _i, _i, _opt, _p, _p, _p], _i),
     "gqa_decode_workspace_size": ([_i, _i, _i64, _i, _i, _i, _i], _sz),
+    "gqa_workspace_size": ([_i, _i, _i64, _i, _i, _i], _sz),
     "gqa_paged_workspace_size": ([_i, _i, _i, _i, _i, _i], _sz),
     "gqa_workspace_init": ([_p, _sz, _p], _i),
     "gqa_workspace_check": ([_p, _p], _i),
@@ -75,6 +76,7 @@ _SIGS = {
     "gqa_decode_paged_ex": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p, _opt],
                             _i),
     "gqa_decode_noalloc": ([_p, _p, _p, _p, _i, _i, _i64, _i, _i, _i, _f, _p], _i),
+    "gqa_decode_noalloc_check": ([_p], _i),
     "gqa_decode_paged_vllm": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p], _i),
     "gqa_decode_paged_vllm_ex": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p,
                                   _opt], _i),
@@ -199,6 +201,11 @@ def gqa_decode_plan(batch, T_q, S_kv, h_q, h_kv, d_head, *, n_splits=0, merge_mo
 
 def gqa_decode_workspace_size(batch, T_q, S_kv, h_q, h_kv, d_head, n_splits=0) -> int:
     return lib.gqa_decode_workspace_size(batch, T_q, S_kv, h_q, h_kv, d_head, n_splits)
+
+
+def gqa_workspace_size(batch, T_q, S_kv, h_q, h_kv, d_head) -> int:
+    """Workspace bytes of a gqa_decode call with the automatic split count (0: invalid shape)."""
+    return lib.gqa_workspace_size(batch, T_q, S_kv, h_q, h_kv, d_head)
 
 
 def gqa_paged_workspace_size(num_seqs, h_q, h_kv, d_head, max_seq_len, partition_size=512) -> int:
@@ -392,3 +399,9 @@ def gqa_decode_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, h_q: i
                                 _stream(stream))
     _check(st, "gqa_decode_noalloc")
     return out
+
+
+def gqa_decode_noalloc_check(stream=None) -> int:
+    """Status of the gqa_decode_noalloc calls on the current device since the last check
+    (synchronises ``stream``; GQA_OK or GQA_ERR_TIMEOUT); clears it."""
+    return lib.gqa_decode_noalloc_check(_stream(stream))

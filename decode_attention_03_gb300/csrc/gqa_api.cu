@@ -662,6 +662,10 @@ size_t gqa_decode_workspace_size(int batch, int T_q, int64_t S_kv, int h_q, int 
   }
 }
 
+size_t gqa_workspace_size(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head) {
+  return gqa_decode_workspace_size(batch, T_q, S_kv, h_q, h_kv, d_head, 0);
+}
+
 gqa_status gqa_paged_plan(int num_seqs, int h_q, int h_kv, int d_head, int block_size, int max_seq_len,
                           int partition_size, int vllm_layout, const gqa_options* opt, int* partition_out,
                           int* head_group_out, int* launches_out) {

@@ -13,12 +13,14 @@
 #include <mutex>
 
 #include "../../include/gqa_decode.h"
+#include "gqa_kernels.cuh"   // the status word's bits (kDevTimeout, kDevBadInput)
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[GQA_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr size_t kStatusBytes = 4;   // the device status word at the start of the array
 std::mutex g_mu;
 void* g_scratch[kMaxDevices] = {};
 
@@ -53,12 +55,29 @@ extern "C" gqa_status gqa_decode_noalloc(const uint16_t* q, const uint16_t* k, c
   void* scratch = nullptr;
   gqa_status s = scratch_on_current_device(&scratch);
   if (s != GQA_OK) return s;
-  // the status word and the arrival counters must start at zero; the array keeps the
-  // previous call's contents (partials need no clearing: every one read is written first)
+  // the arrival counters must start at zero, and the array keeps the previous call's contents:
+  // clear everything the header and counters span except the status word, which keeps the
+  // error bits of earlier calls until gqa_decode_noalloc_check reads them.  Split partials need
+  // no clearing: a call that completes without a device fault writes every partial it reads
+  // (after a fault the outputs are invalid anyway, and the check reports it).
   const size_t zeroed = gqa_decode_workspace_size(batch, T_q, S_kv, h_q, h_kv, d_head, 1);
-  if (zeroed == 0 || zeroed > GQA_NOALLOC_SCRATCH_BYTES) return GQA_ERR_INVALID_ARG;
-  if (cudaMemsetAsync(scratch, 0, zeroed, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (zeroed <= kStatusBytes || zeroed > GQA_NOALLOC_SCRATCH_BYTES) return GQA_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + kStatusBytes, 0, zeroed - kStatusBytes,
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return GQA_ERR_CUDA;
   return gqa_decode(q, k, v, o, batch, T_q, S_kv, h_q, h_kv, d_head, scale, scratch, GQA_NOALLOC_SCRATCH_BYTES,
                     stream);
+}
+
+extern "C" gqa_status gqa_decode_noalloc_check(void* stream) {
+  void* scratch = nullptr;
+  gqa_status s = scratch_on_current_device(&scratch);
+  if (s != GQA_OK) return s;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GQA_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return GQA_ERR_CUDA;
+  if (word != 0 && cudaMemset(scratch, 0, sizeof(word)) != cudaSuccess) return GQA_ERR_CUDA;
+  if (word & gqa::kDevTimeout) return GQA_ERR_TIMEOUT;
+  if (word & gqa::kDevBadInput) return GQA_ERR_INVALID_ARG;
+  return GQA_OK;
 }

@@ -113,6 +113,11 @@ gqa_status gqa_decode_plan(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, 
 size_t gqa_decode_workspace_size(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head,
                                  int n_splits);
 
+/* Workspace bytes for a gqa_decode call with the automatic split count on the current device:
+ * gqa_decode_workspace_size(batch, T_q, S_kv, h_q, h_kv, d_head, 0).  0 on invalid arguments or
+ * when no device is usable. */
+size_t gqa_workspace_size(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head);
+
 /* Workspace bytes for gqa_decode_paged and gqa_decode_paged_vllm (T_q = 1); partition_size 0 sizes
  * for the automatic choice.  Returns 0 on invalid arguments. */
 size_t gqa_paged_workspace_size(int num_seqs, int h_q, int h_kv, int d_head, int max_seq_len,
@@ -251,10 +256,19 @@ gqa_status gqa_decode_paged_vllm_ex(const uint16_t* q, const uint16_t* k_cache, 
  *    stream capture.
  *  - Every call on a device shares the one array: calls that overlap on the GPU (other
  *    streams, other host threads) race and corrupt each other's results.  Each call
- *    clears the array's status word and counters on `stream` before its kernel. */
+ *    clears the array's arrival counters on `stream` before its kernel.
+ *  - Faults seen on the device (a bounded wait that gave up) set bits in the array's status
+ *    word, which calls do not clear: they accumulate until gqa_decode_noalloc_check reads
+ *    them.  Outputs of calls made since the last clean check are then invalid. */
 gqa_status gqa_decode_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
                               int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head, float scale,
                               void* stream);
+
+/* The status word of the current device's gqa_decode_noalloc array: synchronise `stream`, read
+ * and clear it.  GQA_OK, or GQA_ERR_TIMEOUT (a bounded device wait gave up in some call since the
+ * last check; those outputs are invalid).  Allocates nothing.  Like gqa_decode_noalloc, it must
+ * not overlap other calls on the same device. */
+gqa_status gqa_decode_noalloc_check(void* stream);
 
 #ifdef __cplusplus
 }

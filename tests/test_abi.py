@@ -177,3 +177,11 @@ def test_workspace_layout_sizes(binding):
     many = lib.gqa_decode_workspace_size(1, 1, 1 << 20, 32, 8, 128, n)
     al = lambda x: (x + 255) // 256 * 256
     assert many == 256 + 256 + 2 * al(n * R * 4) + al(n * R * 128 * 4)
+
+
+def test_workspace_size_alias(binding):
+    """gqa_workspace_size(batch, T_q, S_kv, h_q, h_kv, d_head) is the automatic-split size query."""
+    assert binding.gqa_workspace_size(1, 1, 100, 8, 3, 128) == 0        # h_q % h_kv != 0
+    assert binding.gqa_workspace_size(1, 1, 100, 8, 2, 96) == 0         # unsupported d_head
+    for shape in [(1, 1, 4096, 8, 2, 64), (8, 1, 32768, 32, 8, 128), (1, 4, 131071, 64, 8, 128)]:
+        assert binding.gqa_workspace_size(*shape) == binding.gqa_decode_workspace_size(*shape, 0)

@@ -4,8 +4,9 @@ Some callers cannot give the library a workspace: a plugin whose device memory i
 and budgeted by its host framework, a latency-critical loop that cannot take cudaMalloc's
 implicit synchronisation, a C / FFI caller without a device allocator.  For them
 gqa_decode_noalloc uses a device array the library owns (8 MiB per GPU).  These tests
-call it through the C ABI and check it against gqa_decode (the regular entry point, with
-a caller workspace) on two calls in a row, within the tolerance the parity tests use.
+call it through the C ABI and check it, on two calls in a row, against the CPU float64
+oracle and against gqa_decode (the regular entry point, with a caller workspace), within
+the tolerance the parity tests use; gqa_decode_noalloc_check then reports a clean status.
 This file is collected last on purpose and also passes on its own in a fresh process.
 """
 import ctypes
@@ -15,6 +16,7 @@ import pytest
 import torch
 
 import gqa_inputs as gi
+import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -33,8 +35,13 @@ def _p(t):
 
 
 def _within(a, b):
-    a, b = a.double(), b.double()
+    a, b = a.double().cpu().reshape(b.shape), b.double().cpu()
     return bool(((a - b).abs() <= 2e-3 + 2e-3 * b.abs()).all())
+
+
+def _rel_l2(a, b):
+    a, b = a.double().cpu().reshape(b.shape), b.double().cpu()
+    return float((a - b).norm() / b.norm())
 
 
 @pytest.mark.parametrize("shape", [(2, 1, 5000, 32, 8, 128), (1, 4, 131071, 64, 8, 128), (1, 1, 4096, 8, 2, 64)])
@@ -52,13 +59,17 @@ def test_noalloc_matches_regular_entry_point_twice(lib, shape):
     st = lib.lib.gqa_decode(_p(q), _p(k), _p(v), _p(ref), B, T_q, S, hq, hkv, D, scale, _p(ws), nbytes, stream)
     assert st == lib.GQA_OK
 
+    exact = oracle.decode(x["q"], x["k"], x["v"], hq, hkv, D, scale)
     for call in range(2):                       # the array keeps the previous call's contents
         out = torch.full_like(q, float("nan"))
         st = lib.lib.gqa_decode_noalloc(_p(q), _p(k), _p(v), _p(out), B, T_q, S, hq, hkv, D, scale, stream)
         assert st == lib.GQA_OK, lib.gqa_status_string(st)
         torch.cuda.synchronize()
         assert torch.isfinite(out.float()).all()
-        assert _within(out, ref), f"call {call}"
+        assert _within(out, exact), f"call {call} against the oracle"
+        assert _rel_l2(out, exact) <= 5e-3, f"call {call} against the oracle"
+        assert _within(out, ref), f"call {call} against gqa_decode"
+    assert lib.lib.gqa_decode_noalloc_check(stream) == lib.GQA_OK
 
 
 def test_noalloc_rejects_shapes_beyond_its_array(lib):
