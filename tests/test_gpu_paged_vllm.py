@@ -109,8 +109,8 @@ def test_vllm_edges(gqa, bs, part, hq, hkv, hg, D):
         hg = 0
     o = run(gqa, p, partition_size=part, head_group=hg)
     r = ref(p)
-    assert (o[0].float() == 0).all()                         # empty sequence -> zeros
-    r[0] = 0.0
+    assert bool((r[0] == 0).all())                           # the oracle's empty sequence: exact zeros
+    assert (o[0].float() == 0).all()                         # and the kernel's
     assert_close(o, r, f"vllm bs={bs} part={part} hq={hq} hkv={hkv} hg={hg} D={D}")
 
 
@@ -143,13 +143,12 @@ def test_partition_plan(gqa):
     assert gqa.gqa_paged_plan(64, 32, 8, 128, 16384, 0, block_size=64)[1] == 4
 
 
-def test_v1_workload_sampled(gqa):
+def test_v1_workload(gqa):
     """The paged_v1 workload (384 sequences of at most 2048 keys): single pass (partition 2048)
-    and the automatic 512-token partitions, sampled sequences."""
+    and the automatic 512-token partitions, every sequence."""
     p = gi.make("paged_v1")
-    lens = p["seq_lens"]
-    seqs = sorted(set([int(np.argmin(lens)), int(np.argmax(lens))] + list(range(0, 384, 37))))
-    r = ref(p, seqs)
+    r = ref(p)
+    assert not bool(torch.isnan(r).any())
     assert_close(run(gqa, p, partition_size=2048), r, "paged_v1, single pass")
     assert_close(run(gqa, p), r, "paged_v1, 512-token partitions")
 
@@ -174,12 +173,13 @@ def test_single_pass_takes_every_sequence_once(gqa):
     assert_close(o, r, "single pass, row pools")
 
 
-def test_vllm_workload_sampled(gqa):
+def test_vllm_workload(gqa):
+    # full size, the benchmark's launch configuration; every sequence against the oracle
     p = gi.make("paged_vllm")
     o = run(gqa, p)
-    lens = p["seq_lens"]
-    seqs = sorted(set([int(np.argmin(lens)), int(np.argmax(lens))] + list(range(0, 64, 9))))
-    assert_close(o, ref(p, seqs), "paged_vllm (sampled sequences)")
+    r = ref(p)
+    assert not bool(torch.isnan(r).any())
+    assert_close(o, r, "paged_vllm (all 64 sequences)")
 
 
 @pytest.mark.parametrize("bs,part", [(16, 0), (32, 512)])
@@ -188,7 +188,7 @@ def test_vllm_bf16(gqa, bs, part):
     o = run(gqa, p, partition_size=part)
     assert o.dtype == torch.bfloat16
     r = ref(p)
-    r[0] = 0.0
+    assert bool((r[0] == 0).all())                  # the oracle's empty sequence: exact zeros
     assert_close(o, r, f"vllm bf16 bs={bs}", rel_tol=8e-3, rel_l2=1e-2)
 
 

@@ -110,13 +110,13 @@ def test_tc_forced_on_ragged_workload(gqa):
     assert_close(run(gqa, x, mma_path=2), ref(x), "ragged on tcgen05")
 
 
-def test_verify16_workload_sampled(gqa):
-    # full size, the benchmark's launch configuration; the oracle checks 2 of the 8 KV heads
+def test_verify16_workload(gqa):
+    # full size, the benchmark's launch configuration; every KV head against the oracle
     x = gi.make("verify16")
     o = run(gqa, x)
-    units = [(0, 0), (0, 5)]
-    r = ref(x, units=units)
-    assert_close(o, r, "verify16 (sampled heads)")
+    r = ref(x)
+    assert not bool(torch.isnan(r).any())
+    assert_close(o, r, "verify16 (all 8 KV heads)")
 
 
 @pytest.mark.parametrize("n_splits", [0, 1, 5])
