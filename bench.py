@@ -64,6 +64,10 @@ def parse():
     ap.add_argument("--merge-mode", type=int, default=0)
     ap.add_argument("--mma-path", type=int, default=0,
                     help="contiguous workloads: 0 automatic, 1 mma.sync split kernel, 2 tcgen05 kernel")
+    ap.add_argument("--shard", choices=["none", "skv"], default="none",
+                    help="contiguous workloads under torchrun: 'skv' splits every sequence's keys over the "
+                         "ranks (sharded_decode: a partial per rank, one all-gather, the merge); the job's "
+                         "bytes are counted once (strong scaling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -233,6 +237,12 @@ def to_device(x: dict, dev):
 
 
 def make_step(pkg, w, x, d, out, ws, args):
+    if w.kind == "contiguous" and args.shard == "skv":
+        from decode_attention_03_gb300.sharded import sharded_decode
+
+        def step():
+            sharded_decode(d["q"], d["k"], d["v"], w.h_q, w.h_kv, w.scale, out=out)
+        return step
     if w.kind == "contiguous":
         def step():
             pkg.gqa_decode(d["q"], d["k"], d["v"], w.h_q, w.h_kv, w.scale, out=out, workspace_tensor=ws,
@@ -347,9 +357,11 @@ def run_reference(args, rank, world):
     return 0
 
 
-def config_of(w, x, n_splits, note=None):
+def config_of(w, x, n_splits, note=None, shard_world=None):
     c = {"workload": w.name, "kind": w.kind, "batch": w.batch, "T_q": w.T_q, "h_q": w.h_q, "h_kv": w.h_kv,
          "d_head": w.d_head, "scale": w.scale, "parallelism": "replicas (no exchange)"}
+    if shard_world is not None:
+        c["parallelism"] = f"S_kv sharded over {shard_world} rank(s): one partial each, all-gather, merge"
     if w.kind == "contiguous":
         c["S_kv"] = w.S_kv
     else:
@@ -379,15 +391,29 @@ def main():
     import decode_attention_03_gb300 as pkg
 
     w, x = load_inputs(args.workload, args.s_kv, args.block_size, args.partition_size, args.elem)
-    d = to_device(x, dev)
     bytes_step = gi.kv_bytes(x)
+    shard = None
+    if args.shard == "skv":
+        if w.kind != "contiguous" or w.elem != "f16":
+            raise SystemExit("--shard skv takes a contiguous float16 workload")
+        from decode_attention_03_gb300.sharded import shard_range
+        shard = shard_range(w.S_kv, rank, world)          # this rank's keys of every sequence
+        b0, n = shard
+        x = dict(x, k=np.ascontiguousarray(x["k"][:, b0:b0 + n]), v=np.ascontiguousarray(x["v"][:, b0:b0 + n]))
+        args.no_e2e = True
+    d = to_device(x, dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     big = bytes_step > 2 * l2
     stream = torch.cuda.Stream(dev)
     out = torch.empty(w.batch * w.T_q * w.h_q * w.d_head, dtype=torch.bfloat16 if w.elem == "bf16" else torch.float16,
                       device=dev)
     out = out.reshape(w.batch, w.T_q, -1) if w.kind == "contiguous" else out.reshape(w.batch, -1)
-    if w.kind == "contiguous":
+    if w.kind == "contiguous" and shard is not None:
+        nbytes = 256
+        n_splits, mma_path, contig_launches = pkg.gqa_decode_plan(
+            w.batch, w.T_q, max(shard[1], 1), w.h_q, w.h_kv, w.d_head)
+        contig_launches += 1                              # the merge of the ranks' partials
+    elif w.kind == "contiguous":
         nbytes = pkg.gqa_decode_workspace_size(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head, args.n_splits)
         n_splits, mma_path, contig_launches = pkg.gqa_decode_plan(
             w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head, n_splits=args.n_splits, merge_mode=args.merge_mode,
@@ -478,8 +504,10 @@ def main():
                   "how": f"CUDA graph of {n_graph} back-to-back steps, inputs L2-resident"}
     t_max = max_over_ranks(t_ms)
     ms_step = t_max / steps
-    value = job_throughput(bytes_step, steps, world, t_max)
-    per_launch_gbs = bytes_step / (ms_step * 1e-3) / 1e9
+    # replicas: every rank moved the workload's bytes; key shards: the ranks moved them once between them
+    value = job_throughput(bytes_step, steps, 1 if shard is not None else world, t_max)
+    rank_bytes = bytes_step / world if shard is not None else bytes_step     # what one GPU moved per step
+    per_launch_gbs = rank_bytes / (ms_step * 1e-3) / 1e9
     peak, peak_src = measured_peak()
 
     # ---- end to end: pinned host inputs -> device, decode, output -> host, every step
@@ -509,9 +537,9 @@ def main():
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
             "warmup": warm, "ms_per_step": round(ms_step, 6), "us_per_step": round(ms_step * 1e3, 3),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.elem,
-            "data": "synthetic",
-            "config": dict(config_of(w, x, n_splits), accum="f32",
+            "higher_is_better": True, "scaling": "strong" if shard is not None else "weak", "vs_baseline": None,
+            "dtype": w.elem, "data": "synthetic",
+            "config": dict(config_of(w, x, n_splits, shard_world=world if shard is not None else None), accum="f32",
                            l2=("inputs larger than L2, no flush" if flush is None
                                else f"L2 flushed ({2 * l2 >> 20} MiB write) before every timed step, outside events")),
             "roofline": {"bound": "hbm", "achieved": round(per_launch_gbs, 2), "peak": peak, "unit": "GB/s",

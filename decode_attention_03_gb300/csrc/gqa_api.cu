@@ -389,7 +389,12 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
   gqa_status s = plan_contig(B, T_q, S_kv, s_begin, s_len, h_q, h_kv, D, 1, false, &p, opt.mma_path);
   if (s != GQA_OK) return s;
   if (B == 0) return GQA_OK;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(ws)) return GQA_ERR_INVALID_ARG;
+  // an empty key range (partial calls) loads no key or value: k and v may then be null (a rank
+  // holding no keys), and the tensor maps are encoded over q, which is never read through them
+  const bool no_keys = partial && s_len == 0;
+  if (!aligned16(q) || !aligned16(ws)) return GQA_ERR_INVALID_ARG;
+  if (!no_keys && (!aligned16(k) || !aligned16(v))) return GQA_ERR_INVALID_ARG;
+  if (no_keys) k = v = q;
   if (partial) {
     if (!aligned16(m_out) || !aligned16(l_out) || !aligned16(op_out)) return GQA_ERR_INVALID_ARG;
   } else if (!aligned16(o)) {

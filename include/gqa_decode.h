@@ -156,7 +156,8 @@ gqa_status gqa_decode_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v
                          void* workspace, size_t ws_bytes, void* stream, const gqa_options* opt);
 
 /* Partial over keys [s_begin, s_begin + s_len) of every sequence (0 <= s_begin,
- * s_begin + s_len <= S_kv; s_len = 0 gives the empty partial m = -inf, l = 0, O = 0).
+ * s_begin + s_len <= S_kv; s_len = 0 gives the empty partial m = -inf, l = 0, O = 0, and then
+ * k and v are not read and may be NULL, with S_kv = 0 for a caller that holds no keys).
  * Outputs, rows ordered like Q's (b, t, h): m, l (batch*T_q*h_q) fp32 and the
  * unnormalised o_part (batch*T_q*h_q, d_head) fp32.  This is the (m, l, O) a rank of the
  * page's kernel sends toward the root; gqa_merge folds several of them. */
