@@ -32,6 +32,16 @@ constexpr int kTcMinRows = 16;              // automatic MMA path: tcgen05 from 
 // them serialises the fold: tiny workload, 64 splits, 16.7 us in-kernel vs 11.9 us with the merge
 // kernel; 16 splits in-kernel 12.7 us)
 constexpr int kInKernelMaxSplits = 32;
+// Automatic merge, short sweeps: where the heuristic asks for more splits than a cluster holds and
+// every CTA of a 16-CTA cluster gets at most this many 64-key tiles, the unit's splits run as one
+// cluster folding through distributed shared memory (one launch, no partials in global memory).
+// Measured on GB300, 2 KV heads, 4 query rows, d_head 64, L2 flushed (us per step; heuristic's
+// choice / merge kernel / one cluster of 16): 2048 keys 13.2 (32 splits folded by the last CTA) /
+// 11.5 / 10.6; 4096 keys - / 12.2 (64 splits) / 11.0; 6144 keys 13.7 / 13.4 (95 splits) / 12.4;
+// 8192 keys 13.8 / 13.8 / 12.6; 16384 keys 15.6 / 15.7 / 15.4 (and 9.0 vs 10.2 with the inputs in
+// L2: there the heuristic's 95 splits stream faster).  Clusters of 12 / 8 / 4 at 4096 keys: 11.6 /
+// 12.2 / 14.6.  Longer sweeps keep the splits, and the bandwidth, of the heuristic.
+constexpr int kClusterMaxTilesPerSplit = 8;
 // Paged partitions chosen automatically (partition_size 0).  Page "muh_kernel_map.py" picks v1 --
 // one pass over each whole sequence, no merge pass -- for seq_len <= 8192 and v2 with 512-token
 // partitions above.  On GB300 the persistent kernel with 512-token partitions (and the merge pass
@@ -62,8 +72,9 @@ bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 struct DevState {
   bool ready = false;
   int sms = 0;
-  int occ[2][4][10][2] = {};   // [d index][row class][kernel: see kernel_slot][bf16] resident CTAs
-                               // per SM, 0 = not prepared
+  int occ[2][4][12][2] = {};   // [d index][row class][kernel: see kernel_slot][bf16] resident CTAs
+                               // per SM (cluster variant: clusters of kMaxClusterSplits the GPU holds),
+                               // 0 = not prepared
 };
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
@@ -74,7 +85,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 EncodeTiledFn g_encode = nullptr;
 
 // Kernel selector `kind`: 0 contiguous, 1 contiguous with the causal tail, 2 / 3 the same two
-// on the tcgen05 kernel (row class 0 stands for its single configuration), and for the paged
+// on the tcgen05 kernel (row class 0 stands for its single configuration), 4 / 5 the same two as
+// the cluster variant of the split kernel (a unit's splits merged in one cluster), and for the paged
 // kernel 100 + its head group (101, 102, 104) over the row-layout pool, 200 + its head group over
 // the vLLM cache layout.
 typedef cudaError_t (*PrepareFn)(int, int, int*);
@@ -94,6 +106,12 @@ const LaunchFn kLaunch[3][2][2] = {{{contig_d64_launch, contig_d64_bf16_launch},
                                    {{paged_vllm_d64_launch, paged_vllm_d64_bf16_launch},
                                     {paged_vllm_d128_launch, paged_vllm_d128_bf16_launch}}};
 
+// cluster variant of the split kernel [d index][bf16]
+const PrepareFn kClusterPrepare[2][2] = {{cluster_d64_prepare, cluster_d64_bf16_prepare},
+                                         {cluster_d128_prepare, cluster_d128_bf16_prepare}};
+const LaunchFn kClusterLaunch[2][2] = {{cluster_d64_launch, cluster_d64_bf16_launch},
+                                       {cluster_d128_launch, cluster_d128_bf16_launch}};
+
 const PrepareFn kTcPrepare[2] = {tc_d64_prepare, tc_d128_prepare};
 typedef cudaError_t (*TcLaunchFn)(int, int, dim3, cudaStream_t, const CUtensorMap&, const CUtensorMap&,
                                   const DecodeArgs&);
@@ -101,6 +119,7 @@ const TcLaunchFn kTcLaunch[2] = {tc_d64_launch, tc_d128_launch};
 
 cudaError_t prepare_unit(int di, int cls, int kind, int bf16, int* occ) {
   if (kind == 2 || kind == 3) return kTcPrepare[di](kind - 2, bf16, occ);
+  if (kind == 4 || kind == 5) return kClusterPrepare[di][bf16](cls, kind - 4, occ);
   const int family = kind / 100;   // 0 contiguous, 1 paged, 2 paged over the vLLM layout
   return kPrepare[family][di][bf16](cls, kind - 100 * family, occ);
 }
@@ -108,13 +127,15 @@ cudaError_t prepare_unit(int di, int cls, int kind, int bf16, int* occ) {
 cudaError_t launch_unit(int di, int cls, int kind, int bf16, dim3 grid, cudaStream_t st, const CUtensorMap& tk,
                         const CUtensorMap& tv, const DecodeArgs& a) {
   if (kind == 2 || kind == 3) return kTcLaunch[di](kind - 2, bf16, grid, st, tk, tv, a);
+  if (kind == 4 || kind == 5) return kClusterLaunch[di][bf16](cls, kind - 4, grid, st, tk, tv, a);
   const int family = kind / 100;   // 0 contiguous, 1 paged, 2 paged over the vLLM layout
   return kLaunch[family][di][bf16](cls, kind - 100 * family, grid, st, tk, tv, a);
 }
 
 int kernel_slot(int kind) {
   if (kind < 2) return kind;
-  if (kind < 100) return kind + 3;   // tcgen05: 5, 6
+  if (kind < 4) return kind + 3;     // tcgen05: 5, 6
+  if (kind < 100) return kind + 6;   // cluster variant: 10, 11
   const int hg_slot = (kind % 100) == 1 ? 0 : ((kind % 100) == 2 ? 1 : 2);
   return (kind < 200 ? 2 : 7) + hg_slot;   // paged: 2-4, vLLM layout: 7-9
 }
@@ -141,8 +162,10 @@ gqa_status device_info(int di, int cls, int kind, int bf16, int* sms, int* occ) 
   int& o = st.occ[di][cls][kernel_slot(kind)][bf16];
   if (o == 0) {
     int v = 0;
-    if (prepare_unit(di, cls, kind, bf16, &v) != cudaSuccess || v <= 0) return GQA_ERR_CUDA;
-    o = v;
+    if (prepare_unit(di, cls, kind, bf16, &v) != cudaSuccess) return GQA_ERR_CUDA;
+    // the cluster variant reports how many of its largest clusters fit (-1: none); others need >= 1
+    if (v <= 0 && !(kind == 4 || kind == 5)) return GQA_ERR_CUDA;
+    o = v > 0 ? v : -1;
   }
   *sms = st.sms;
   *occ = o;
@@ -265,6 +288,7 @@ gqa_options defaults() {
 struct ContigPlan {
   int di, cls, rows, n_splits;
   bool tc;                     // the tcgen05 kernel (else the mma.sync split kernel)
+  bool cluster;                // the split kernel's cluster variant (merge_mode 3)
   int64_t units, tiles, R;
   Layout lay;
 };
@@ -272,7 +296,7 @@ struct ContigPlan {
 // validation shared by the size query and the calls
 // mma_path: 0 auto (tcgen05 above 64 query rows per KV head), 1 mma.sync, 2 tcgen05
 gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_len, int h_q, int h_kv, int D,
-                       int forced_splits, bool need_device, ContigPlan* p, int mma_path = 0) {
+                       int forced_splits, bool need_device, ContigPlan* p, int mma_path = 0, int merge_mode = 0) {
   if (B < 0 || T_q < 1 || h_q < 1 || h_kv < 1 || S_kv < 0 || s_begin < 0 || s_len < 0) return GQA_ERR_INVALID_ARG;
   if (s_begin + s_len > S_kv) return GQA_ERR_INVALID_ARG;
   if (h_q % h_kv != 0 || forced_splits < 0) return GQA_ERR_INVALID_ARG;
@@ -287,7 +311,9 @@ gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_
   // automatic: the tcgen05 kernel from kTcMinRows rows (measured on GB300 at 2^18 keys, 8 KV
   // heads, d_head 128: 4-8 rows 171-173 us on mma.sync vs 175 us; 16 rows 177-179 vs 175; 32 rows
   // 193-195 vs 177; 64 rows 451 vs 179)
-  p->tc = mma_path == 2 || (mma_path == 0 && rows >= kTcMinRows);
+  // (merge_mode 3, a cluster of the split kernel, exists on the mma.sync kernel only: the automatic
+  // choice takes that kernel then while it can serve the rows)
+  p->tc = mma_path == 2 || (mma_path == 0 && rows >= kTcMinRows && !(merge_mode == 3 && rows <= 64));
   if (!p->tc && rows > 64) return GQA_ERR_UNSUPPORTED;
   p->cls = p->tc ? 0 : row_class(p->rows);
   p->units = (int64_t)B * h_kv;
@@ -309,7 +335,23 @@ gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_
   } else {
     p->n_splits = 1;
   }
+  // the workspace holds the partials of the heuristic's (or the forced) split count, whatever the
+  // merge: the size query serves every merge mode
   p->lay = ws_layout(p->units, p->n_splits, p->R, D);
+  // merge_mode 3: the unit's splits form one thread-block cluster, at most kMaxClusterSplits CTAs
+  p->cluster = false;
+  if (merge_mode == 3) {
+    if (p->tc) return GQA_ERR_UNSUPPORTED;
+    if (p->n_splits > kMaxClusterSplits) p->n_splits = kMaxClusterSplits;
+    p->cluster = p->n_splits > 1;
+  } else if (merge_mode == 0 && !p->tc && forced_splits == 0 && need_device && p->n_splits > kMaxClusterSplits &&
+             p->tiles <= (int64_t)kMaxClusterSplits * kClusterMaxTilesPerSplit) {
+    int sms = 0, clusters = 0;   // only where a cluster of kMaxClusterSplits can be scheduled
+    if (device_info(p->di, p->cls, 4, 0, &sms, &clusters) == GQA_OK && clusters > 0) {
+      p->n_splits = kMaxClusterSplits;
+      p->cluster = true;
+    }
+  }
   return GQA_OK;
 }
 
@@ -370,6 +412,7 @@ cudaError_t paged_merge_launch_w(const DecodeArgs& a, cudaStream_t st) {
 // merge_mode 0 (automatic): in-kernel up to kInKernelMaxSplits splits (and, for the tcgen05 kernel,
 // while a unit's partials are at most kInKernelMergeBytes); 1 separate kernel; 2 in-kernel
 bool merge_in_kernel(const ContigPlan& p, int D, int merge_mode) {
+  if (p.cluster) return true;
   if (merge_mode == 1) return false;
   if (merge_mode == 2) return true;
   if (p.n_splits > kInKernelMaxSplits) return false;
@@ -381,7 +424,7 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
                        int h_q, int h_kv, int D, float scale, void* ws, size_t ws_bytes, void* stream,
                        const gqa_options* opt_in, bool partial) {
   const gqa_options opt = opt_in ? *opt_in : defaults();
-  if (opt.merge_mode < 0 || opt.merge_mode > 2) return GQA_ERR_INVALID_ARG;
+  if (opt.merge_mode < 0 || opt.merge_mode > 3) return GQA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
   if (!partial && S_kv < 1) return GQA_ERR_INVALID_ARG;
   ContigPlan p;
@@ -400,11 +443,11 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
   } else if (!aligned16(o)) {
     return GQA_ERR_INVALID_ARG;
   }
-  s = plan_contig(B, T_q, S_kv, s_begin, s_len, h_q, h_kv, D, opt.n_splits, true, &p, opt.mma_path);
+  s = plan_contig(B, T_q, S_kv, s_begin, s_len, h_q, h_kv, D, opt.n_splits, true, &p, opt.mma_path, opt.merge_mode);
   if (s != GQA_OK) return s;
   if (ws_bytes < p.lay.total) return GQA_ERR_WORKSPACE;
   int sms = 0, occ = 0;
-  const int kind = (p.tc ? 2 : 0) + (opt.causal ? 1 : 0);
+  const int kind = (p.tc ? 2 : (p.cluster ? 4 : 0)) + (opt.causal ? 1 : 0);
   const int bf16 = opt.bf16 ? 1 : 0;
   s = device_info(p.di, p.cls, kind, bf16, &sms, &occ);
   if (s != GQA_OK) return s;
@@ -441,7 +484,7 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
   a.s_begin = s_begin;
   a.s_len = s_len;
   a.n_splits = p.n_splits;
-  a.merge_in_kernel = merge_in_kernel(p, D, opt.merge_mode) ? 1 : 0;
+  a.merge_in_kernel = p.cluster || merge_in_kernel(p, D, opt.merge_mode) ? 1 : 0;
   a.causal = opt.causal ? 1 : 0;
   a.scale_log2 = scale * kLog2e;
   a.timeout_ns = opt.timeout_us ? (uint64_t)opt.timeout_us * 1000ull : kDefaultTimeoutNs;
@@ -644,9 +687,10 @@ gqa_status gqa_decode_plan(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, 
                            int* n_splits, int* mma_path, int* launches) {
   try {
     const gqa_options o = opt ? *opt : defaults();
-    if (S_kv < 1 || batch < 1 || o.merge_mode < 0 || o.merge_mode > 2) return GQA_ERR_INVALID_ARG;
+    if (S_kv < 1 || batch < 1 || o.merge_mode < 0 || o.merge_mode > 3) return GQA_ERR_INVALID_ARG;
     ContigPlan p;
-    gqa_status s = plan_contig(batch, T_q, S_kv, 0, S_kv, h_q, h_kv, d_head, o.n_splits, true, &p, o.mma_path);
+    gqa_status s = plan_contig(batch, T_q, S_kv, 0, S_kv, h_q, h_kv, d_head, o.n_splits, true, &p, o.mma_path,
+                               o.merge_mode);
     if (s != GQA_OK) return s;
     if (n_splits) *n_splits = p.n_splits;
     if (mma_path) *mma_path = p.tc ? 2 : 1;

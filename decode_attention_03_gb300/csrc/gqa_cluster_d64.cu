@@ -1,0 +1,7 @@
+// Instances of the split-KV decode kernels, cluster variant (the splits of a unit merged through
+// distributed shared memory): contiguous K/V, d_head = 64, f16 elements.
+#include "gqa_instances.cuh"
+
+namespace gqa {
+GQA_DEFINE_CONTIG_UNIT(cluster_d64, 64, false, true)
+}  // namespace gqa

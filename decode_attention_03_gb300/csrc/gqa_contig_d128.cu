@@ -2,5 +2,5 @@
 #include "gqa_instances.cuh"
 
 namespace gqa {
-GQA_DEFINE_CONTIG_UNIT(contig_d128, 128, false)
+GQA_DEFINE_CONTIG_UNIT(contig_d128, 128, false, false)
 }  // namespace gqa

@@ -2,5 +2,5 @@
 #include "gqa_instances.cuh"
 
 namespace gqa {
-GQA_DEFINE_CONTIG_UNIT(contig_d128_bf16, 128, true)
+GQA_DEFINE_CONTIG_UNIT(contig_d128_bf16, 128, true, false)
 }  // namespace gqa

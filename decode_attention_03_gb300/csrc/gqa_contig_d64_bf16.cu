@@ -2,5 +2,5 @@
 #include "gqa_instances.cuh"
 
 namespace gqa {
-GQA_DEFINE_CONTIG_UNIT(contig_d64_bf16, 64, true)
+GQA_DEFINE_CONTIG_UNIT(contig_d64_bf16, 64, true, false)
 }  // namespace gqa

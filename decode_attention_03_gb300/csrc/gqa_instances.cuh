@@ -36,7 +36,11 @@ constexpr int paged_stages_for() {
   return n < 2 ? 2 : (n > 8 ? 8 : n);
 }
 
-template <int D, int CLS, bool CAUSAL, bool BF16>
+// Largest cluster of the split kernel's cluster variant: 16 CTAs (beyond the portable 8, allowed
+// per kernel with cudaFuncAttributeNonPortableClusterSizeAllowed).
+constexpr int kMaxClusterSplits = 16;
+
+template <int D, int CLS, bool CAUSAL, bool BF16, bool CLUSTER = false>
 struct Inst {
   static constexpr int NT = cls_nt(CLS);
   static constexpr int WN = cls_wn(CLS);
@@ -45,16 +49,47 @@ struct Inst {
   using C = Cfg<D, NT, WN, STAGES * SUB>;
   static_assert(C::SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
+  // resident CTAs per SM; for the cluster variant, the number of clusters of kMaxClusterSplits CTAs
+  // the GPU can hold at once is the occupancy reported (0: that cluster size cannot be scheduled)
   static cudaError_t prepare(int* occupancy) {
-    auto fn = gqa_split_kernel<D, NT, WN, STAGES, SUB, CAUSAL, BF16>;
+    auto fn = gqa_split_kernel<D, NT, WN, STAGES, SUB, CAUSAL, BF16, CLUSTER>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, fn, C::THREADS, C::SMEM_BYTES);
+    if constexpr (!CLUSTER) {
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, fn, C::THREADS, C::SMEM_BYTES);
+    } else {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      cluster_config(cfg, attr, dim3(1, kMaxClusterSplits, 1), nullptr);
+      return cudaOccupancyMaxActiveClusters(occupancy, fn, &cfg);
+    }
+  }
+  static void cluster_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[1], dim3 grid, cudaStream_t st) {
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = grid.y;   // the splits of one unit
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
   }
   static cudaError_t launch(dim3 grid, cudaStream_t st, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a) {
-    gqa_split_kernel<D, NT, WN, STAGES, SUB, CAUSAL, BF16><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tk, tv, a);
-    return cudaGetLastError();
+    if constexpr (!CLUSTER) {
+      gqa_split_kernel<D, NT, WN, STAGES, SUB, CAUSAL, BF16><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tk, tv, a);
+      return cudaGetLastError();
+    } else {
+      if (grid.y < 2 || grid.y > (unsigned)kMaxClusterSplits) return cudaErrorInvalidValue;
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      cluster_config(cfg, attr, grid, st);
+      return cudaLaunchKernelEx(&cfg, gqa_split_kernel<D, NT, WN, STAGES, SUB, CAUSAL, BF16, true>, tk, tv, a);
+    }
   }
 };
 
@@ -87,20 +122,21 @@ struct PagedInst {
   cudaError_t NAME##_launch(int cls, int variant, dim3 grid, cudaStream_t st, const CUtensorMap& tk, \
                             const CUtensorMap& tv, const DecodeArgs& a);
 
-#define GQA_CONTIG_CASES(D, BF, CALL)                                                            \
-  if (cls == 0) return variant ? Inst<D, 0, true, BF>::CALL : Inst<D, 0, false, BF>::CALL;       \
-  if (cls == 1) return variant ? Inst<D, 1, true, BF>::CALL : Inst<D, 1, false, BF>::CALL;       \
-  if (cls == 2) return variant ? Inst<D, 2, true, BF>::CALL : Inst<D, 2, false, BF>::CALL;       \
-  if (cls == 3) return variant ? Inst<D, 3, true, BF>::CALL : Inst<D, 3, false, BF>::CALL;       \
+#define GQA_CONTIG_CASES(D, BF, CL, CALL)                                                        \
+  if (cls == 0) return variant ? Inst<D, 0, true, BF, CL>::CALL : Inst<D, 0, false, BF, CL>::CALL; \
+  if (cls == 1) return variant ? Inst<D, 1, true, BF, CL>::CALL : Inst<D, 1, false, BF, CL>::CALL; \
+  if (cls == 2) return variant ? Inst<D, 2, true, BF, CL>::CALL : Inst<D, 2, false, BF, CL>::CALL; \
+  if (cls == 3) return variant ? Inst<D, 3, true, BF, CL>::CALL : Inst<D, 3, false, BF, CL>::CALL; \
   return cudaErrorInvalidValue;
 
-#define GQA_DEFINE_CONTIG_UNIT(NAME, D, BF)                                                      \
+// CL: the cluster variant (the splits of a unit merged through distributed shared memory)
+#define GQA_DEFINE_CONTIG_UNIT(NAME, D, BF, CL)                                                  \
   cudaError_t NAME##_prepare(int cls, int variant, int* occupancy) {                             \
-    GQA_CONTIG_CASES(D, BF, prepare(occupancy))                                                  \
+    GQA_CONTIG_CASES(D, BF, CL, prepare(occupancy))                                              \
   }                                                                                              \
   cudaError_t NAME##_launch(int cls, int variant, dim3 grid, cudaStream_t st, const CUtensorMap& tk, \
                             const CUtensorMap& tv, const DecodeArgs& a) {                        \
-    GQA_CONTIG_CASES(D, BF, launch(grid, st, tk, tv, a))                                         \
+    GQA_CONTIG_CASES(D, BF, CL, launch(grid, st, tk, tv, a))                                     \
   }
 
 #define GQA_PAGED_CASES(D, BF, VL, CALL)                                                         \
@@ -129,6 +165,10 @@ GQA_DECLARE_UNIT(paged_d64)
 GQA_DECLARE_UNIT(paged_d128)
 GQA_DECLARE_UNIT(contig_d64_bf16)
 GQA_DECLARE_UNIT(contig_d128_bf16)
+GQA_DECLARE_UNIT(cluster_d64)
+GQA_DECLARE_UNIT(cluster_d128)
+GQA_DECLARE_UNIT(cluster_d64_bf16)
+GQA_DECLARE_UNIT(cluster_d128_bf16)
 GQA_DECLARE_UNIT(paged_d64_bf16)
 GQA_DECLARE_UNIT(paged_d128_bf16)
 GQA_DECLARE_UNIT(paged_vllm_d64)

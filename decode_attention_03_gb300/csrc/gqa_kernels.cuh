@@ -440,6 +440,33 @@ __device__ __forceinline__ void stash_warp(WarpState<D, NT>& st, float* scratch,
 // slice, partial mode) or this slice's fp32 partial in the workspace.  With HG heads a
 // head has kWK/HG key-slice warps (hh*KS .. hh*KS+KS-1); with one head, warp col*kWK+k
 // holds key slice k of query column col.
+// The KS key-slice warps w0 .. w0+KS-1 of one query row (row lr of each warp's block) folded
+// into one (M, L, O[d]) -- M in the log2 domain of the scaled logits.
+template <int D, int NT, int WN, int STAGES, int KS>
+__device__ __forceinline__ void combine_warps(const float* scratch, int w0, int lr, int d, float& M, float& L,
+                                              float& O) {
+  using C = Cfg<D, NT, WN, STAGES>;
+  float mk[KS];
+  M = -CUDART_INF_F;
+#pragma unroll
+  for (int k = 0; k < KS; ++k) {
+    const float* wsp = scratch + (w0 + k) * C::WSCRATCH;
+    mk[k] = wsp[C::WROWS * C::OSTRIDE + lr];
+    M = fmaxf(M, mk[k]);
+  }
+  L = 0.f;
+  O = 0.f;
+  if (M != -CUDART_INF_F) {
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      const float* wsp = scratch + (w0 + k) * C::WSCRATCH;
+      const float w = ptx::ex2(mk[k] - M);
+      L += w * wsp[C::WROWS * C::OSTRIDE + C::WROWS + lr];
+      O += w * wsp[lr * C::OSTRIDE + d];
+    }
+  }
+}
+
 template <int D, int NT, int WN, int STAGES, int HG = 1, bool BF16 = false>
 __device__ __forceinline__ void emit_slice(const DecodeArgs& a, const float* scratch, int b, int g0, int slice,
                                            bool single, int tid, int nthreads) {
@@ -453,24 +480,8 @@ __device__ __forceinline__ void emit_slice(const DecodeArgs& a, const float* scr
     const int col = r / C::WROWS, lr = r - col * C::WROWS;
     const int w0 = HG > 1 ? hh * KS : col * kWK;
     const int g = g0 + hh;
-    float mk[KS];
-    float M = -CUDART_INF_F;
-#pragma unroll
-    for (int k = 0; k < KS; ++k) {
-      const float* wsp = scratch + (w0 + k) * C::WSCRATCH;
-      mk[k] = wsp[C::WROWS * C::OSTRIDE + lr];
-      M = fmaxf(M, mk[k]);
-    }
-    float L = 0.f, O = 0.f;
-    if (M != -CUDART_INF_F) {
-#pragma unroll
-      for (int k = 0; k < KS; ++k) {
-        const float* wsp = scratch + (w0 + k) * C::WSCRATCH;
-        const float w = ptx::ex2(mk[k] - M);
-        L += w * wsp[C::WROWS * C::OSTRIDE + C::WROWS + lr];
-        O += w * wsp[lr * C::OSTRIDE + d];
-      }
-    }
+    float M, L, O;
+    combine_warps<D, NT, WN, STAGES, KS>(scratch, w0, lr, d, M, L, O);
     const int64_t orow = out_row(a, b, g, r);
     if (single) {
       if (a.o != nullptr) {
@@ -593,6 +604,101 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int g, in
 }
 
 // =====================================================================================
+// merge inside a thread-block cluster: the splits of one unit are the CTAs of one cluster
+// =====================================================================================
+// Layout of a CTA's partial in its own shared memory (the cluster variant of the split
+// kernel): m, l [RMAX] (log2 domain) and O [RMAX][D], fp32, at byte offset `off`.
+template <int RMAX, int D>
+struct ClusterPartial {
+  static constexpr int M = 0;
+  static constexpr int L = RMAX * 4;
+  static constexpr int O = 2 * RMAX * 4;   // 16-byte aligned (RMAX is a multiple of 8)
+  static constexpr int BYTES = O + RMAX * D * 4;
+};
+
+// This CTA's combined partial: every query row of the unit, its key-slice warps folded.
+template <int D, int NT, int WN, int STAGES>
+__device__ __forceinline__ void emit_cta_partial(const DecodeArgs& a, const float* scratch, uint8_t* cp, int tid,
+                                                 int nthreads) {
+  using C = Cfg<D, NT, WN, STAGES>;
+  using P = ClusterPartial<C::WROWS * WN, D>;
+  float* cm = reinterpret_cast<float*>(cp + P::M);
+  float* cl = reinterpret_cast<float*>(cp + P::L);
+  float* co = reinterpret_cast<float*>(cp + P::O);
+  for (int idx = tid; idx < a.rows * D; idx += nthreads) {
+    const int r = idx / D, d = idx - r * D;
+    const int col = r / C::WROWS, lr = r - col * C::WROWS;
+    float M, L, O;
+    combine_warps<D, NT, WN, STAGES, kWK>(scratch, col * kWK, lr, d, M, L, O);
+    co[r * D + d] = O;
+    if (d == 0) {
+      cm[r] = M;
+      cl[r] = L;
+    }
+  }
+}
+
+// Fold the n CTAs' partials of unit (b, g) (page: _merge_running over the splits in order, then
+// O / l) for this CTA's share of the unit's outputs -- items (row, 4 columns) [lo, hi) of
+// rows * D/4 -- reading every partial through distributed shared memory, and write the output
+// (or the merged partial).  `cp` is the shared-memory address of this CTA's partial (the same
+// offset in every CTA); `valid` its flag word.  Nothing is written unless every CTA of the
+// cluster completed its slice (a wait that gave up leaves the output alone).
+template <int RMAX, int D, int NTH, bool BF16>
+__device__ __forceinline__ void cluster_merge(const DecodeArgs& a, int b, int g, uint32_t cp, uint32_t valid, int n,
+                                              int rank) {
+  using P = ClusterPartial<RMAX, D>;
+  constexpr int DQ = D / 4;
+  constexpr int UNR = 8;
+  bool all_valid = true;
+  for (int s = 0; s < n; ++s) all_valid &= ptx::ld_cluster_s32(ptx::mapa(valid, (uint32_t)s)) != 0;
+  if (!all_valid) return;
+  const int n_items = a.rows * DQ;
+  const int lo = (int)((int64_t)n_items * rank / n), hi = (int)((int64_t)n_items * (rank + 1) / n);
+  for (int item = lo + (int)threadIdx.x; item < hi; item += NTH) {
+    const int r = item / DQ, c4 = item - r * DQ;
+    float M = -CUDART_INF_F, L = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < n; s0 += UNR) {
+      float ms[UNR], ls[UNR];
+      float4 os[UNR];
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {   // every load of the chunk issued before any fold
+        const bool have = s0 + u < n;
+        const uint32_t base = ptx::mapa(cp, (uint32_t)(have ? s0 + u : 0));
+        ms[u] = have ? ptx::ld_cluster_f32(base + P::M + r * 4) : -CUDART_INF_F;
+        ls[u] = have ? ptx::ld_cluster_f32(base + P::L + r * 4) : 0.f;
+        os[u] = have ? ptx::ld_cluster_v4(base + P::O + (r * D + c4 * 4) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const float m_new = fmaxf(M, ms[u]);
+        const float ref = m_new == -CUDART_INF_F ? 0.f : m_new;   // both sides empty so far
+        const float so = ptx::ex2(M - ref), sn = ptx::ex2(ms[u] - ref);
+        L = L * so + ls[u] * sn;
+        O.x = O.x * so + os[u].x * sn;
+        O.y = O.y * so + os[u].y * sn;
+        O.z = O.z * so + os[u].z * sn;
+        O.w = O.w * so + os[u].w * sn;
+        M = m_new;
+      }
+    }
+    const int64_t orow = out_row(a, b, g, r);
+    if (a.o != nullptr) {
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      Elem<BF16>::store2(a.o, orow * D + c4 * 4, O.x * inv, O.y * inv);
+      Elem<BF16>::store2(a.o, orow * D + c4 * 4 + 2, O.z * inv, O.w * inv);
+    } else {
+      if (c4 == 0) {
+        a.m_out[orow] = M * kLn2;
+        a.l_out[orow] = L;
+      }
+      reinterpret_cast<float4*>(a.o_part_out + orow * D)[c4] = O;
+    }
+  }
+}
+
+// =====================================================================================
 // contiguous K/V: one CTA per (KV head, split, sequence)
 // =====================================================================================
 // 64-key tiles per pipeline stage of the split kernel: two at d_head 64, so that a stage (one
@@ -601,7 +707,10 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int g, in
 // d_head 64: 4 query rows 111.3 -> 94.9 us, 8 rows 113.3 -> 96.9 us)
 __host__ __device__ constexpr int split_sub(int D) { return D == 64 ? 2 : 1; }
 
-template <int D, int NT, int WN, int STAGES, int SUB, bool CAUSAL, bool BF16>
+// CLUSTER: launched with cluster dimensions (1, n_splits, 1) -- the splits of a unit are the CTAs
+// of one cluster, which fold their partials through distributed shared memory in place of the
+// workspace and the arrival ticket (every thread of the CTA stays until the cluster has read them).
+template <int D, int NT, int WN, int STAGES, int SUB, bool CAUSAL, bool BF16, bool CLUSTER = false>
 __global__ void __launch_bounds__(Cfg<D, NT, WN, STAGES * SUB>::THREADS)
 gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const DecodeArgs a) {
@@ -610,11 +719,15 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   constexpr int KVB = SUB * C::KV_BYTES;     // K (or V) bytes of one stage
   constexpr int STB = 2 * KVB;               // one stage
   constexpr int SROWS = SUB * kTile;         // keys (TMA box rows) per stage
+  using CP = ClusterPartial<C::WROWS * WN, D>;
+  constexpr int CP_OFF = (C::SCRATCH_BYTES + 15) & ~15;   // this CTA's partial (CLUSTER), after the scratch
+  static_assert(!CLUSTER || CP_OFF + CP::BYTES <= C::DATA_BYTES, "cluster partial fits the drained ring");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::DATA_BYTES);
   uint64_t* empty = full + STAGES;
-  volatile int* flags = reinterpret_cast<volatile int*>(empty + STAGES);  // [0] abort, [1] last-CTA
+  // [0] abort, [1] last-CTA, [2] CLUSTER: this CTA's partial is complete
+  volatile int* flags = reinterpret_cast<volatile int*>(empty + STAGES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g_kv = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
@@ -636,6 +749,7 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     }
     flags[0] = 0;
     flags[1] = 0;
+    flags[2] = 0;
     ptx::fence_mbar_init();
   }
   if (warp == C::CONSUMERS && lane == 0) {
@@ -680,6 +794,11 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         }
       }
     }
+    if constexpr (CLUSTER) {   // the producer's threads take part in both cluster barriers too
+      __syncwarp();
+      ptx::cluster_sync();
+      ptx::cluster_sync();
+    }
     return;
   }
 
@@ -716,7 +835,25 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 
   // all tiles consumed (the ring is free); a wait that gave up anywhere -> leave the output alone
   if (threadIdx.x == 0) ptx::grid_launch_dependents();   // a separate merge kernel may start launching
-  if (ptx::named_bar_or(1, C::CTHREADS, flags[0] != 0)) return;
+  const bool aborted = ptx::named_bar_or(1, C::CTHREADS, flags[0] != 0);
+  if constexpr (CLUSTER) {
+    // this CTA's partial into its own shared memory, then the cluster folds all of them; a CTA
+    // whose wait gave up still takes part in both barriers, flagging its partial incomplete
+    if (!aborted) {
+      float* scratch = reinterpret_cast<float*>(smem);
+      stash_warp<D, NT, WN, STAGES>(st, scratch, warp, lane);
+      ptx::named_bar_sync(1, C::CTHREADS);
+      emit_cta_partial<D, NT, WN, STAGES>(a, scratch, smem + CP_OFF, threadIdx.x, C::CTHREADS);
+      if (threadIdx.x == 0) flags[2] = 1;
+    }
+    ptx::cluster_sync();   // every CTA's partial (and flag) visible to the cluster
+    cluster_merge<C::WROWS * WN, D, C::CTHREADS, BF16>(a, b, g_kv, ptx::smem_u32(smem + CP_OFF),
+                                                       ptx::smem_u32(const_cast<int*>(flags + 2)), a.n_splits,
+                                                       split);
+    ptx::cluster_sync();   // no CTA leaves while the cluster may still read its partial
+    return;
+  }
+  if (aborted) return;
   float* scratch = reinterpret_cast<float*>(smem);
   stash_warp<D, NT, WN, STAGES>(st, scratch, warp, lane);
   ptx::named_bar_sync(1, C::CTHREADS);

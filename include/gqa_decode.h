@@ -65,7 +65,11 @@ typedef struct {
   int merge_mode;        /* how a unit's splits are folded: 0 = automatic (the last-arriving CTA of the
                             unit in the same kernel, except above 32 splits or, for the tcgen05
                             kernel, when a unit's partials exceed 256 KB), 1 = separate merge kernel,
-                            2 = last-arriving CTA */
+                            2 = last-arriving CTA, 3 = the unit's splits (at most 16; more are
+                            capped) run as one thread-block cluster and fold their partials through
+                            distributed shared memory, no workspace partials and one launch
+                            (mma.sync kernel only: the automatic mma_path takes it for up to 64
+                            rows; GQA_ERR_UNSUPPORTED on the tcgen05 kernel) */
   uint32_t timeout_us;   /* limit of every device wait; 0 = 1,000,000 us */
   int test_stall_cta;    /* test hook, -1 = off.  Contiguous calls: linear id (x + X*(y + Y*z)) of
                             one CTA whose producer never loads its second tile; paged calls: the

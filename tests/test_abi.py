@@ -89,8 +89,8 @@ def test_validation_codes_without_gpu(binding):
     assert dec_path(2, 9) == binding.GQA_ERR_UNSUPPORTED             # G*T_q = 144
     assert dec_path(3, 1) == binding.GQA_ERR_INVALID_ARG             # no such path
     assert dec_path(-1, 1) == binding.GQA_ERR_INVALID_ARG
-    # merge modes 0-2 only
-    for mm in (-1, 3):
+    # merge modes 0-3 only
+    for mm in (-1, 4):
         opt = binding.gqa_options(0, mm, 0, -1, 0, 0)
         r = lib.gqa_decode_ex(p, p, p, p, 1, 1, 16, 8, 2, 64, s, p, 1 << 12, st, ctypes.byref(opt))
         assert r == binding.GQA_ERR_INVALID_ARG
