@@ -19,7 +19,7 @@ _BINDING_NAMES = (
     "gqa_workspace_init", "gqa_workspace_check", "gqa_status_string", "gqa_version",
     "GQAError", "gqa_options", "workspace", "lib", "LIB_PATH", "EXPORTED",
     "GQA_OK", "GQA_ERR_INVALID_ARG", "GQA_ERR_UNSUPPORTED", "GQA_ERR_WORKSPACE", "GQA_ERR_CUDA",
-    "GQA_ERR_TIMEOUT", "GQA_NOALLOC_SCRATCH_BYTES",
+    "GQA_ERR_TIMEOUT", "GQA_ERR_BOUNDS", "GQA_BUILD_BOUNDS_CHECK", "GQA_NOALLOC_SCRATCH_BYTES", "open_library",
 )
 
 __all__ = list(_BINDING_NAMES)

@@ -26,6 +26,8 @@ GQA_ERR_UNSUPPORTED = 2
 GQA_ERR_WORKSPACE = 3
 GQA_ERR_CUDA = 4
 GQA_ERR_TIMEOUT = 5
+GQA_ERR_BOUNDS = 6
+GQA_BUILD_BOUNDS_CHECK = 1
 
 
 class GQAError(RuntimeError):
@@ -57,6 +59,7 @@ _SIGS = {
     "gqa_default_options": ([], gqa_options),
     "gqa_status_string": ([_i], ctypes.c_char_p),
     "gqa_version": ([], _i),
+    "gqa_build_flags": ([], _i),
     "gqa_decode_num_splits": ([_i, _i, _i64, _i, _i, _i], _i),
     "gqa_decode_plan": ([_i, _i, _i64, _i, _i, _i, _opt, _p, _p, _p], _i),
     "gqa_paged_plan": ([_i, _i, _i, _i, _i, _i, _i, _i, _opt, _p, _p, _p], _i),
@@ -81,10 +84,21 @@ _SIGS = {
     "gqa_decode_paged_vllm_ex": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p,
                                   _opt], _i),
 }
-for _name, (_args, _res) in _SIGS.items():
-    _fn = getattr(lib, _name)
-    _fn.argtypes = _args
-    _fn.restype = _res
+def _bind(cdll):
+    for name, (args, res) in _SIGS.items():
+        fn = getattr(cdll, name)
+        fn.argtypes = args
+        fn.restype = res
+    return cdll
+
+
+_bind(lib)
+
+
+def open_library(path: str):
+    """Another build of the library (e.g. the bounds-checked ``libgqa_decode_checked.so``) as a
+    ctypes handle with every entry point's signature set; its functions are called directly."""
+    return _bind(ctypes.CDLL(path))
 
 EXPORTED = tuple(_SIGS)
 

@@ -5,6 +5,12 @@ then linked into ``decode_attention_03_gb300/libgqa_decode.so`` with the CUDA
 runtime linked statically (the library needs only the NVIDIA driver at run
 time).  A rebuild happens only when a source or header is newer than the
 library.
+
+``build(checked=True)`` makes the checked library instead,
+``libgqa_decode_checked.so`` (objects in ``_build_checked/``): the same sources
+compiled with ``GQA_BOUNDS_CHECK=1``, under which the kernels range-check every
+computed global- and shared-memory offset and report a failure in the status
+word instead of making the access.
 """
 from __future__ import annotations
 
@@ -20,6 +26,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgqa_decode.so")
+BUILD_CHECKED = os.path.join(ROOT, "_build_checked")
+LIB_CHECKED = os.path.join(PKG, "libgqa_decode_checked.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",
           "-I" + os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]
@@ -41,23 +49,26 @@ def _deps():
         [os.path.join(ROOT, "include", "gqa_decode.h"), os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compile and link the library; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False, checked: bool = False) -> str:
+    """Compile and link the library (``checked``: the bounds-checked one); returns its path."""
+    lib, bdir = (LIB_CHECKED, BUILD_CHECKED) if checked else (LIB, BUILD)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    if checked:
+        extra += ["-DGQA_BOUNDS_CHECK=1"]
 
     def compile_one(src: str):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc] + ARCH + CFLAGS + extra + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return obj, cmd, r
@@ -70,16 +81,17 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
             sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {os.path.basename(obj)}")
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc] + ARCH + ["-shared", "-o", tmp] + [o for o, _, _ in results] + ["-lpthread", "-ldl", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if verbose or r.returncode != 0:
         sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
     if r.returncode != 0:
-        raise RuntimeError("link of libgqa_decode.so failed")
-    os.replace(tmp, LIB)
-    return LIB
+        raise RuntimeError(f"link of {os.path.basename(lib)} failed")
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_verbose="-v" in sys.argv,
+                checked="--checked" in sys.argv))

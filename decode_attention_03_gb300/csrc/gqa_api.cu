@@ -377,24 +377,26 @@ int merge_warps(int n_parts) { return n_parts <= kMergeChunk ? 1 : 4; }
 
 template <int D, bool BF16, int W>
 cudaError_t merge_launch_w(const float* m, const float* l, const float* op, int n_parts, int64_t rows, __half* o,
-                           float* mo, float* lo, float* oo, cudaStream_t st) {
+                           float* mo, float* lo, float* oo, cudaStream_t st, uint32_t* status) {
   const int64_t rpb = kMergeThreads / (32 * W);
   const int64_t blocks = (rows + rpb - 1) / rpb;
   if (blocks > 2147483647LL) return cudaErrorInvalidValue;
   return launch_pdl(gqa_merge_kernel<D, BF16, W>, (unsigned)blocks, kMergeThreads, st, m, l, op, n_parts, rows, o,
-                    mo, lo, oo);
+                    mo, lo, oo, status);
 }
 
+// status: the calling decode's workspace status word (null for the public merge calls)
 gqa_status merge_launch(const float* m, const float* l, const float* op, int n_parts, int64_t rows, int D,
-                        __half* o, float* mo, float* lo, float* oo, cudaStream_t st, int bf16 = 0) {
+                        __half* o, float* mo, float* lo, float* oo, cudaStream_t st, int bf16 = 0,
+                        uint32_t* status = nullptr) {
   if (rows == 0) return GQA_OK;
   if (rows > 2147483647LL) return GQA_ERR_INVALID_ARG;
   const bool one = merge_warps(n_parts) == 1;
   cudaError_t e = cudaErrorInvalidValue;
 #define GQA_MERGE_CASE(DD, BB)                                                                    \
   if (D == DD && bf16 == BB)                                                                      \
-    e = one ? merge_launch_w<DD, BB, 1>(m, l, op, n_parts, rows, o, mo, lo, oo, st)               \
-            : merge_launch_w<DD, BB, 4>(m, l, op, n_parts, rows, o, mo, lo, oo, st);
+    e = one ? merge_launch_w<DD, BB, 1>(m, l, op, n_parts, rows, o, mo, lo, oo, st, status)       \
+            : merge_launch_w<DD, BB, 4>(m, l, op, n_parts, rows, o, mo, lo, oo, st, status);
   GQA_MERGE_CASE(64, false)
   GQA_MERGE_CASE(64, true)
   GQA_MERGE_CASE(128, false)
@@ -494,7 +496,8 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
   dim3 grid((unsigned)h_kv, (unsigned)p.n_splits, (unsigned)B);
   if (launch_unit(p.di, p.cls, kind, bf16, grid, st, tk, tv, a) != cudaSuccess) return GQA_ERR_CUDA;
   if (p.n_splits > 1 && !a.merge_in_kernel) {
-    return merge_launch(a.ws_m, a.ws_l, a.ws_o, p.n_splits, p.R, D, a.o, a.m_out, a.l_out, a.o_part_out, st, bf16);
+    return merge_launch(a.ws_m, a.ws_l, a.ws_o, p.n_splits, p.R, D, a.o, a.m_out, a.l_out, a.o_part_out, st, bf16,
+                        a.status);
   }
   return GQA_OK;
 }
@@ -666,11 +669,14 @@ const char* gqa_status_string(int status) {
     case GQA_ERR_WORKSPACE: return "workspace too small";
     case GQA_ERR_CUDA: return "CUDA error";
     case GQA_ERR_TIMEOUT: return "a device wait timed out";
+    case GQA_ERR_BOUNDS: return "a device bounds check failed (checked build)";
   }
   return "unknown status";
 }
 
 int gqa_version(void) { return kVersion; }
+
+int gqa_build_flags(void) { return GQA_BOUNDS_CHECK ? GQA_BUILD_BOUNDS_CHECK : 0; }
 
 int gqa_decode_num_splits(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head) {
   try {
@@ -759,6 +765,7 @@ gqa_status gqa_workspace_check(void* workspace, void* stream) {
   uint32_t word = 0;
   if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return GQA_ERR_CUDA;
   if (word != 0 && cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return GQA_ERR_CUDA;
+  if (word & kDevBounds) return GQA_ERR_BOUNDS;
   if (word & kDevTimeout) return GQA_ERR_TIMEOUT;
   if (word & kDevBadInput) return GQA_ERR_INVALID_ARG;
   return GQA_OK;

@@ -48,6 +48,7 @@ constexpr int kWK = 4;             // consumer warps along the key axis
 constexpr int kTile = 16 * kWK;    // keys per pipeline stage
 constexpr uint32_t kDevTimeout = 1u;
 constexpr uint32_t kDevBadInput = 2u;
+constexpr uint32_t kDevBounds = 4u;     // a bounds check failed (checked build only)
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxBoxesPerPart = 1024;  // paged: TMA boxes (blocks or block slices) of one partition
@@ -124,6 +125,50 @@ struct Cfg {
                                      (3 * kPagedSeqs + 1 + kSizeClasses) * 4;
   static constexpr int PSMEM_BYTES = 1024 + PCTRL_OFF + PCTRL_BYTES;
   static constexpr int PTHREADS = (CONSUMERS + 3) * 32;          // + producer, scheduler, epilogue
+};
+
+// ---- opt-in bounds checks.  Built with -DGQA_BOUNDS_CHECK=1 (the checked library), every
+// computed global-memory index and shared-memory address of the kernels is compared with the
+// extent of the buffer or shared-memory region it falls in before the access; one out of range
+// sets kDevBounds in the status word (when there is one) and the access is skipped, or made at
+// the region's first address where a warp-collective instruction must still execute -- nothing
+// traps.  In the regular build every check is the constant true.
+#ifndef GQA_BOUNDS_CHECK
+#define GQA_BOUNDS_CHECK 0
+#endif
+
+// 0 <= i < n
+__device__ __forceinline__ bool idx_ok(int64_t i, int64_t n, uint32_t* status) {
+#if GQA_BOUNDS_CHECK
+  if (i < 0 || i >= n) {
+    if (status != nullptr) atomicOr(status, kDevBounds);
+    return false;
+  }
+#endif
+  return true;
+}
+
+// [addr, addr + bytes) inside the shared-memory region [lo, hi)
+__device__ __forceinline__ bool smem_ok(uint32_t addr, uint32_t bytes, uint32_t lo, uint32_t hi, uint32_t* status) {
+#if GQA_BOUNDS_CHECK
+  if (addr < lo || addr + bytes > hi) {
+    if (status != nullptr) atomicOr(status, kDevBounds);
+    return false;
+  }
+#endif
+  return true;
+}
+
+// an address for a warp-collective shared-memory read: `addr` when in range, else `lo`
+__device__ __forceinline__ uint32_t smem_clamp(uint32_t addr, uint32_t bytes, uint32_t lo, uint32_t hi,
+                                               uint32_t* status) {
+  return smem_ok(addr, bytes, lo, hi, status) ? addr : lo;
+}
+
+// A shared-memory region [lo, hi) and the status word its checks report to.
+struct Win {
+  uint32_t lo, hi;
+  uint32_t* status;
 };
 
 // Row r of a unit (0 <= r < G*T_q) is query token r / G, head g*G + r % G.
@@ -204,7 +249,7 @@ __device__ __forceinline__ void load_q(WarpState<D, NT>& st, const DecodeArgs& a
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int r = (nc * NT + nt) * 8 + gq;
-    if (r < a.rows) {
+    if (r < a.rows && idx_ok(out_row(a, b, g, r), a.R, a.status)) {   // the row's D elements
       const uint32_t* qp = reinterpret_cast<const uint32_t*>(a.q + out_row(a, b, g, r) * D);
 #pragma unroll
       for (int kk = 0; kk < WarpState<D, NT>::KD; ++kk) {
@@ -238,13 +283,14 @@ __device__ __forceinline__ void reset_state(WarpState<D, NT>& st) {
 // writes before the next asynchronous (TMA) write into the same buffer.
 // `vhead` points at the first plane of this warp's head.
 template <int HALVES, int BOXP>
-__device__ __forceinline__ void zero_masked_v(uint8_t* vhead, int ks, int valid, int lane, int rb) {
+__device__ __forceinline__ void zero_masked_v(uint8_t* vhead, int ks, int valid, int lane, int rb, const Win& ring) {
   const int per_row = 8 * HALVES;                      // 16-byte chunks of one row of the head
   for (int i = lane; i < (16 - valid) * per_row; i += 32) {
     const int row = ks * 16 + valid + i / per_row;
     const int rem = i % per_row;
     const int off = row_offset<BOXP>(row, rb) + (rem >> 3) * (rb * 128) + (rem & 7) * 16;
-    *reinterpret_cast<uint4*>(vhead + off) = make_uint4(0u, 0u, 0u, 0u);
+    if (smem_ok(ptx::smem_u32(vhead + off), 16, ring.lo, ring.hi, ring.status))
+      *reinterpret_cast<uint4*>(vhead + off) = make_uint4(0u, 0u, 0u, 0u);
   }
   ptx::fence_proxy_async_smem();
   __syncwarp();
@@ -269,12 +315,13 @@ __device__ __forceinline__ int vllm_v_offset(int drow, int kb, int rb) {
 // row of this warp's head in the tile's first box; boxes of rb keys are box_bytes apart.
 template <int D>
 __device__ __forceinline__ void zero_masked_v_vllm(uint8_t* vhead, int ks, int valid, int lane, int rb,
-                                                   int box_bytes) {
+                                                   int box_bytes, const Win& ring) {
   const int nmask = 16 - valid;
   for (int i = lane; i < D * nmask; i += 32) {
     const int drow = i / nmask;
     const int key = ks * 16 + valid + (i - drow * nmask);
-    *reinterpret_cast<uint16_t*>(vhead + (key / rb) * box_bytes + vllm_v_offset(drow, key % rb, rb)) = 0;
+    uint8_t* dst = vhead + (key / rb) * box_bytes + vllm_v_offset(drow, key % rb, rb);
+    if (smem_ok(ptx::smem_u32(dst), 2, ring.lo, ring.hi, ring.status)) *reinterpret_cast<uint16_t*>(dst) = 0;
   }
   ptx::fence_proxy_async_smem();
   __syncwarp();
@@ -284,7 +331,7 @@ __device__ __forceinline__ void zero_masked_v_vllm(uint8_t* vhead, int ks, int v
 // the first plane (row layout) or first chunk / d row (VLLM) of the warp's head.
 template <int D, int NT, int BOXP, bool CAUSAL = false, bool BF16 = false, bool VLLM = false>
 __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbase, uint32_t vbase, int valid,
-                                             int key0, int ks, int lane, float scale_log2, int rb) {
+                                             int key0, int ks, int lane, float scale_log2, int rb, const Win& ring) {
   constexpr int KD = WarpState<D, NT>::KD;
   const int gq = lane >> 2;
   const int k_row = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -309,9 +356,10 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbas
   for (int kk = 0; kk < KD; ++kk) {
     uint32_t af[4];
     if constexpr (VLLM) {
-      ptx::ldmatrix_x4(af, kvb + (kk * 2 + k_c0) * rb * 16);
+      ptx::ldmatrix_x4(af, smem_clamp(kvb + (kk * 2 + k_c0) * rb * 16, 16, ring.lo, ring.hi, ring.status));
     } else {
-      ptx::ldmatrix_x4(af, chunk_addr(kbase, k_off, k_row, kk * 2 + k_c0, plane));
+      ptx::ldmatrix_x4(af, smem_clamp(chunk_addr(kbase, k_off, k_row, kk * 2 + k_c0, plane), 16, ring.lo, ring.hi,
+                                      ring.status));
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) Elem<BF16>::mma(sc[nt], af, st.qf[nt][kk]);
@@ -384,9 +432,11 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbas
     uint32_t af[4];
     if constexpr (VLLM) {
       // V^T is stored: rows d 16i .. 16i+15, 8 keys per ldmatrix row
-      ptx::ldmatrix_x4(af, vvb + vllm_v_offset(i * 16 + v_dr, v_kb, rb));
+      ptx::ldmatrix_x4(af, smem_clamp(vvb + vllm_v_offset(i * 16 + v_dr, v_kb, rb), 16, ring.lo, ring.hi,
+                                      ring.status));
     } else {
-      ptx::ldmatrix_x4_trans(af, chunk_addr(vbase, v_off, v_row, i * 2 + v_c0, plane));
+      ptx::ldmatrix_x4_trans(af, smem_clamp(chunk_addr(vbase, v_off, v_row, i * 2 + v_c0, plane), 16, ring.lo,
+                                            ring.hi, ring.status));
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) Elem<BF16>::mma(st.acc[i][nt], af, pf[nt]);
@@ -400,8 +450,11 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbas
 // Reduce l over the lanes that share a query row and write this warp's (O, m, l)
 // into its block of the shared-memory scratch.
 template <int D, int NT, int WN, int STAGES>
-__device__ __forceinline__ void stash_warp(WarpState<D, NT>& st, float* scratch, int warp, int lane) {
+__device__ __forceinline__ void stash_warp(WarpState<D, NT>& st, float* scratch, int warp, int lane,
+                                           uint32_t* status) {
   using C = Cfg<D, NT, WN, STAGES>;
+  // every index below stays inside this warp's block of the scratch: check the block once
+  if (!idx_ok((int64_t)(warp + 1) * C::WSCRATCH - 1, (int64_t)C::CONSUMERS * C::WSCRATCH, status)) return;
   const int gq = lane >> 2, tq4 = lane & 3;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -444,10 +497,16 @@ __device__ __forceinline__ void stash_warp(WarpState<D, NT>& st, float* scratch,
 // into one (M, L, O[d]) -- M in the log2 domain of the scaled logits.
 template <int D, int NT, int WN, int STAGES, int KS>
 __device__ __forceinline__ void combine_warps(const float* scratch, int w0, int lr, int d, float& M, float& L,
-                                              float& O) {
+                                              float& O, uint32_t* status) {
   using C = Cfg<D, NT, WN, STAGES>;
   float mk[KS];
   M = -CUDART_INF_F;
+  L = 0.f;
+  O = 0.f;
+  // the KS warps' blocks, and row lr / column d inside a block
+  if (!idx_ok((int64_t)(w0 + KS) * C::WSCRATCH - 1, (int64_t)C::CONSUMERS * C::WSCRATCH, status) ||
+      !idx_ok(lr, C::WROWS, status) || !idx_ok(d, D, status))
+    return;
 #pragma unroll
   for (int k = 0; k < KS; ++k) {
     const float* wsp = scratch + (w0 + k) * C::WSCRATCH;
@@ -481,8 +540,9 @@ __device__ __forceinline__ void emit_slice(const DecodeArgs& a, const float* scr
     const int w0 = HG > 1 ? hh * KS : col * kWK;
     const int g = g0 + hh;
     float M, L, O;
-    combine_warps<D, NT, WN, STAGES, KS>(scratch, w0, lr, d, M, L, O);
+    combine_warps<D, NT, WN, STAGES, KS>(scratch, w0, lr, d, M, L, O, a.status);
     const int64_t orow = out_row(a, b, g, r);
+    if (!idx_ok(orow, a.R, a.status)) continue;
     if (single) {
       if (a.o != nullptr) {
         Elem<BF16>::store(a.o, orow * D + d, L > 0.f ? O / L : 0.f);
@@ -495,6 +555,7 @@ __device__ __forceinline__ void emit_slice(const DecodeArgs& a, const float* scr
       }
     } else {
       const int64_t prow = (int64_t)slice * a.R + orow;
+      if (!idx_ok(slice, a.n_splits, a.status)) continue;
       if (d == 0) {
         a.ws_m[prow] = M * kLn2;
         a.ws_l[prow] = L;
@@ -511,8 +572,11 @@ __device__ __forceinline__ bool last_to_arrive(const DecodeArgs& a, int unit, in
   __threadfence();
   ptx::named_bar_sync(1, CTHREADS);
   if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(a.counters + unit, 1u);
-    flags[1] = (prev == (unsigned)(n_slices - 1)) ? 1 : 0;
+    flags[1] = 0;
+    if (idx_ok(unit, (int64_t)a.B * a.h_kv, a.status)) {
+      const unsigned prev = atomicAdd(a.counters + unit, 1u);
+      flags[1] = (prev == (unsigned)(n_slices - 1)) ? 1 : 0;
+    }
   }
   ptx::named_bar_sync(1, CTHREADS);
   const bool last = flags[1] != 0;
@@ -532,12 +596,15 @@ __device__ __forceinline__ void merge_pass(const DecodeArgs& a, int b, int g, in
   float4 O[IPT];
   int64_t orow_i[IPT];
   int c4_i[IPT];
+  bool ok_i[IPT];
 #pragma unroll
   for (int i = 0; i < IPT; ++i) {
     const int item = item0 + threadIdx.x + i * NTH;
     const int r = item < n_items ? item / DQ : 0;
     c4_i[i] = item < n_items ? item - r * DQ : 0;
     orow_i[i] = out_row(a, b, g, r);
+    ok_i[i] = idx_ok(orow_i[i], a.R, a.status);
+    if (!ok_i[i]) orow_i[i] = 0;   // read in range, nothing written for it below
     M[i] = -CUDART_INF_F;
     L[i] = 0.f;
     O[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -545,6 +612,7 @@ __device__ __forceinline__ void merge_pass(const DecodeArgs& a, int b, int g, in
   // chunks of UNR partials: all UNR x IPT loads are issued before any is used, about 16
   // float4 loads in flight per thread
   constexpr int UNR = IPT >= 4 ? 4 : 16 / IPT;
+  if (n > 0 && !idx_ok(n - 1, a.n_splits, a.status)) n = 0;   // only this call's splits' partials are read
   for (int s0 = 0; s0 < n; s0 += UNR) {
     float ms[UNR][IPT], ls[UNR][IPT];
     float4 os[UNR][IPT];
@@ -579,6 +647,7 @@ __device__ __forceinline__ void merge_pass(const DecodeArgs& a, int b, int g, in
 #pragma unroll
   for (int i = 0; i < IPT; ++i) {
     if (item0 + threadIdx.x + i * NTH >= n_items) continue;
+    if (!ok_i[i]) continue;
     const int64_t orow = orow_i[i];
     if (a.o != nullptr) {
       const float inv = L[i] > 0.f ? 1.f / L[i] : 0.f;
@@ -600,7 +669,7 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int g, in
   using C = Cfg<D, NT, WN, STAGES>;
   constexpr int IPT = (C::WROWS * WN * (D / 4) + C::CTHREADS - 1) / C::CTHREADS;
   merge_pass<D, C::CTHREADS, IPT, BF16>(a, b, g, 0, n);
-  if (threadIdx.x == 0) atomicExch(a.counters + unit, 0u);
+  if (threadIdx.x == 0 && idx_ok(unit, (int64_t)a.B * a.h_kv, a.status)) atomicExch(a.counters + unit, 0u);
 }
 
 // =====================================================================================
@@ -629,7 +698,8 @@ __device__ __forceinline__ void emit_cta_partial(const DecodeArgs& a, const floa
     const int r = idx / D, d = idx - r * D;
     const int col = r / C::WROWS, lr = r - col * C::WROWS;
     float M, L, O;
-    combine_warps<D, NT, WN, STAGES, kWK>(scratch, col * kWK, lr, d, M, L, O);
+    combine_warps<D, NT, WN, STAGES, kWK>(scratch, col * kWK, lr, d, M, L, O, a.status);
+    if (!idx_ok(r, C::WROWS * WN, a.status)) continue;   // rows of the partial's layout
     co[r * D + d] = O;
     if (d == 0) {
       cm[r] = M;
@@ -657,6 +727,7 @@ __device__ __forceinline__ void cluster_merge(const DecodeArgs& a, int b, int g,
   const int lo = (int)((int64_t)n_items * rank / n), hi = (int)((int64_t)n_items * (rank + 1) / n);
   for (int item = lo + (int)threadIdx.x; item < hi; item += NTH) {
     const int r = item / DQ, c4 = item - r * DQ;
+    if (!idx_ok(r, RMAX, a.status) || !idx_ok(out_row(a, b, g, r), a.R, a.status)) continue;
     float M = -CUDART_INF_F, L = 0.f;
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < n; s0 += UNR) {
@@ -732,6 +803,7 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g_kv = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
   const int unit = b * a.h_kv + g_kv;
+  const Win ring{ptx::smem_u32(smem), ptx::smem_u32(smem) + (uint32_t)C::PIPE_BYTES, a.status};
 
   // ---- this CTA's key range [key_begin, key_end)
   const int64_t tiles_total = (a.s_len + kTile - 1) / kTile;
@@ -780,10 +852,17 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         const uint32_t kdst = ptx::smem_u32(smem + s * STB);
         const uint32_t vdst = kdst + KVB;
         const uint32_t fb = ptx::smem_u32(full + s);
-        ptx::mbar_arrive_expect_tx(fb, STB);
-        const int y = (int)(y_base + key_begin + (int64_t)it * SROWS);
-        ptx::tma_load_3d(kdst, &tmK, fb, 0, y, g_kv * C::HALVES, pol);
-        ptx::tma_load_3d(vdst, &tmV, fb, 0, y, g_kv * C::HALVES, pol);
+        const int64_t y = y_base + key_begin + (int64_t)it * SROWS;
+        // the box starts inside K / V's rows and heads and lands inside the ring (else the stage
+        // completes without data: the check has recorded it)
+        if (idx_ok(y, (int64_t)a.B * a.S_kv, a.status) && idx_ok(g_kv, a.h_kv, a.status) &&
+            smem_ok(kdst, STB, ring.lo, ring.hi, a.status)) {
+          ptx::mbar_arrive_expect_tx(fb, STB);
+          ptx::tma_load_3d(kdst, &tmK, fb, 0, (int)y, g_kv * C::HALVES, pol);
+          ptx::tma_load_3d(vdst, &tmV, fb, 0, (int)y, g_kv * C::HALVES, pol);
+        } else {
+          ptx::mbar_arrive(fb);
+        }
       }
       if (gave_up || stall_tile >= 0) {
         // wait (bounded) for copies still in flight before the CTA can exit
@@ -824,10 +903,10 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       const int kr = sub * kWK + ks;                      // 16-key slice of the stage's box rows
       const int64_t key0 = key_begin + (int64_t)it * SROWS + kr * 16;
       const int valid = (int)max((int64_t)0, min((int64_t)16, key_end - key0));
-      if (valid < 16) zero_masked_v<C::HALVES, C::HALVES>(smem + s * STB + KVB, kr, valid, lane, SROWS);
+      if (valid < 16) zero_masked_v<C::HALVES, C::HALVES>(smem + s * STB + KVB, kr, valid, lane, SROWS, ring);
       if (valid > 0)
         consume_tile<D, NT, C::HALVES, CAUSAL, BF16>(st, kbase, vbase, valid, (int)key0, kr, lane, a.scale_log2,
-                                                     SROWS);
+                                                     SROWS, ring);
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(empty + s));
@@ -841,7 +920,7 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     // whose wait gave up still takes part in both barriers, flagging its partial incomplete
     if (!aborted) {
       float* scratch = reinterpret_cast<float*>(smem);
-      stash_warp<D, NT, WN, STAGES>(st, scratch, warp, lane);
+      stash_warp<D, NT, WN, STAGES>(st, scratch, warp, lane, a.status);
       ptx::named_bar_sync(1, C::CTHREADS);
       emit_cta_partial<D, NT, WN, STAGES>(a, scratch, smem + CP_OFF, threadIdx.x, C::CTHREADS);
       if (threadIdx.x == 0) flags[2] = 1;
@@ -855,7 +934,7 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   }
   if (aborted) return;
   float* scratch = reinterpret_cast<float*>(smem);
-  stash_warp<D, NT, WN, STAGES>(st, scratch, warp, lane);
+  stash_warp<D, NT, WN, STAGES>(st, scratch, warp, lane, a.status);
   ptx::named_bar_sync(1, C::CTHREADS);
   const bool single = (a.n_splits == 1);
   emit_slice<D, NT, WN, STAGES, 1, BF16>(a, scratch, b, g_kv, split, single, threadIdx.x, C::CTHREADS);
@@ -963,6 +1042,9 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   const int P = a.partition_size;
   const int N = a.B;
   const int cap = min(a.max_blocks_per_seq * a.block_size, a.n_splits * P);
+  const Win ring{ptx::smem_u32(smem), ptx::smem_u32(smem) + (uint32_t)C::PIPE_BYTES, a.status};
+  // the per-sequence tables in shared memory hold kPagedSeqs entries (the host splits larger batches)
+  if (!idx_ok(N, kPagedSeqs + 1, a.status)) return;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -1017,7 +1099,7 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   const int br = min(a.block_size, TK);  // rows per box
   // sequences without keys get zero output rows (spread over the CTAs)
   for (int b = blockIdx.x; b < N; b += gridDim.x) {
-    if (lens_s[b] != 0) continue;
+    if (lens_s[b] != 0 || !idx_ok((int64_t)(b + 1) * a.T_q * a.h_q - 1, a.R, a.status)) continue;
     __half* dst = a.o + (int64_t)b * a.T_q * a.h_q * D;
     for (int i = threadIdx.x; i < a.T_q * a.h_q * D; i += blockDim.x) dst[i] = __float2half_rn(0.f);
   }
@@ -1100,6 +1182,12 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         for (int i = lane; i < d.n_boxes; i += 32) {
           const int rel = i * br;                   // key offset in the partition (block aligned start)
           const int blk = rel / bs;
+          // the entry lies in sequence d.b's row of the table, the box in this slot's list
+          if (!idx_ok(d.b, N, a.status) || !idx_ok(d.key_begin / bs + blk, a.max_blocks_per_seq, a.status) ||
+              !idx_ok(i, kMaxBoxesPerPart, a.status)) {
+            if (i < kMaxBoxesPerPart) dst[i] = -1;
+            continue;
+          }
           int id = __ldg(row + blk);
           if (id < 0 || id >= a.num_blocks) {
             atomicOr(a.status, kDevBadInput);
@@ -1156,12 +1244,30 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
           // box j of tile t holds keys [(t*nbox + j)*br, +br) of the partition
           const int b0 = t * nbox;
           const int nb_t = min(nbox, d.n_boxes - b0);
+          // a box is loaded when its pool row is valid -- and, checked, when the box and its
+          // destination are in range
+          auto box_ok = [&](int j) {
+            if (!idx_ok(b0 + j, kMaxBoxesPerPart, a.status)) return false;
+            const int y = by[b0 + j];
+            if (y < 0) return false;
+            const uint32_t off = j * br * 128 * BOXP;
+            if (!smem_ok(kdst + off, br * 128 * BOXP, ring.lo, ring.hi, a.status) ||
+                !smem_ok(vdst + off, br * 128 * BOXP, ring.lo, ring.hi, a.status))
+              return false;
+            if constexpr (VLLM) {
+              return idx_ok((int64_t)(y >> bs_shift) * a.h_kv + d.g + HG - 1, (int64_t)a.num_blocks * a.h_kv,
+                            a.status);
+            } else {
+              return idx_ok(y, (int64_t)a.num_blocks * a.block_size, a.status) &&
+                     idx_ok(d.g + HG - 1, a.h_kv, a.status);
+            }
+          };
           int n_load = 0;
-          for (int j = 0; j < nb_t; ++j) n_load += by[b0 + j] >= 0 ? 1 : 0;
+          for (int j = 0; j < nb_t; ++j) n_load += box_ok(j) ? 1 : 0;
           ptx::mbar_arrive_expect_tx(fb, (uint32_t)(n_load * br * 128 * 2 * BOXP));
           for (int j = 0; j < nb_t; ++j) {
+            if (!box_ok(j)) continue;
             const int y = by[b0 + j];
-            if (y < 0) continue;
             const uint32_t off = j * br * 128 * BOXP;
             if constexpr (VLLM) {
               // pool row y = block * block_size (boxes are whole blocks): both boxes start at head
@@ -1227,14 +1333,14 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         if (valid < 16) {
           uint8_t* vh = smem + s * C::STAGE_BYTES + C::KV_BYTES + head_off;
           if constexpr (VLLM) {
-            zero_masked_v_vllm<D>(vh, ks, valid, lane, br, br * 128 * BOXP);
+            zero_masked_v_vllm<D>(vh, ks, valid, lane, br, br * 128 * BOXP, ring);
           } else {
-            zero_masked_v<C::HALVES, BOXP>(vh, ks, valid, lane, br);
+            zero_masked_v<C::HALVES, BOXP>(vh, ks, valid, lane, br, ring);
           }
         }
         if (valid > 0)
           consume_tile<D, NT, BOXP, false, BF16, VLLM>(st, kbase, vbase, valid, (int)key0, ks, lane, a.scale_log2,
-                                                       br);
+                                                       br, ring);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(empty + s));
       }
@@ -1253,7 +1359,7 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     if (ptx::named_bar_or(1, C::CTHREADS, aborted || flags[0] != 0)) return;
     if (d.kind != 2) {
       float* sb = reinterpret_cast<float*>(smem + C::PSCRATCH_OFF + buf * C::PSCRATCH_STRIDE);
-      stash_warp<D, NT, WN, STAGES>(st, sb, warp, lane);
+      stash_warp<D, NT, WN, STAGES>(st, sb, warp, lane, a.status);
     }
     if (warp == 0 && lane == 0) edesc[buf] = d;
     __threadfence_block();

@@ -22,9 +22,11 @@ constexpr int kMergeChunk = 8;      // partials whose loads a warp issues before
 template <int D, int W>
 __device__ __forceinline__ void fold_row(const float* m, const float* l, const float* op, int n, int64_t rows,
                                          int64_t r, int w, int lane, float* sm, float& M_out, float& L_out,
-                                         float (&acc)[D / 32]) {
+                                         float (&acc)[D / 32], int64_t n_cap, uint32_t* status) {
   constexpr int PER = D / 32;
   float M = -CUDART_INF_F, L = 0.f;
+  // partial slots s < n of row r, inside the n_cap slots of `rows` rows the buffers hold
+  if (n > 0 && (!idx_ok((int64_t)(n - 1) * rows + r, n_cap * rows, status) || !idx_ok(r, rows, status))) n = 0;
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
   for (int s0 = w; s0 < n; s0 += W * kMergeChunk) {
@@ -110,7 +112,7 @@ gqa_paged_merge_kernel(const DecodeArgs a) {
   const int rr = warp / W, w = warp % W;
   const int64_t r = (int64_t)blockIdx.x * RPB + rr;
   int n = 0;
-  if (r < a.R) {
+  if (r < a.R && idx_ok(r / (a.T_q * a.h_q), a.B, a.status)) {
     const int b = (int)(r / (a.T_q * a.h_q));
     const int cap = min(a.max_blocks_per_seq * a.block_size, a.n_splits * a.partition_size);
     int len = __ldg(a.seq_lens + b);
@@ -118,7 +120,8 @@ gqa_paged_merge_kernel(const DecodeArgs a) {
     n = (len + a.partition_size - 1) / a.partition_size;
   }
   float M, L, acc[PER];
-  fold_row<D, W>(a.ws_m, a.ws_l, a.ws_o, n > 1 ? n : 0, a.R, r < a.R ? r : 0, w, lane, sm[rr], M, L, acc);
+  fold_row<D, W>(a.ws_m, a.ws_l, a.ws_o, n > 1 ? n : 0, a.R, r < a.R ? r : 0, w, lane, sm[rr], M, L, acc,
+                 a.n_splits, a.status);
   if (n <= 1 || w != 0) return;
   const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
@@ -128,10 +131,12 @@ gqa_paged_merge_kernel(const DecodeArgs a) {
 // Public merge of n_parts partials laid out [n_parts][rows] and [n_parts][rows][D]
 // (natural-log m).  W warps per row; a programmatic dependent of the kernel before it in the
 // stream when the decode call launches it.
+// `status`: the workspace status word that bounds checks report to (null for the public merge,
+// which has no workspace: a check that fails there only skips the access).
 template <int D, bool BF16, int W>
 __global__ void __launch_bounds__(kMergeThreads)
 gqa_merge_kernel(const float* __restrict__ m, const float* __restrict__ l, const float* __restrict__ op,
-                 int n_parts, int64_t rows, __half* o, float* m_out, float* l_out, float* o_out) {
+                 int n_parts, int64_t rows, __half* o, float* m_out, float* l_out, float* o_out, uint32_t* status) {
   constexpr int PER = D / 32, RPB = kMergeThreads / (32 * W);
   __shared__ float sm[RPB][W * (D + 2)];
   ptx::grid_dependency_wait();
@@ -139,7 +144,8 @@ gqa_merge_kernel(const float* __restrict__ m, const float* __restrict__ l, const
   const int rr = warp / W, w = warp % W;
   const int64_t r = (int64_t)blockIdx.x * RPB + rr;
   float M, L, acc[PER];
-  fold_row<D, W>(m, l, op, r < rows ? n_parts : 0, rows, r < rows ? r : 0, w, lane, sm[rr], M, L, acc);
+  fold_row<D, W>(m, l, op, r < rows ? n_parts : 0, rows, r < rows ? r : 0, w, lane, sm[rr], M, L, acc, n_parts,
+                 status);
   if (r >= rows || w != 0) return;
   if (o != nullptr) {
     const float inv = L > 0.f ? 1.f / L : 0.f;

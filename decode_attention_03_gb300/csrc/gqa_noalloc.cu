@@ -77,6 +77,7 @@ extern "C" gqa_status gqa_decode_noalloc_check(void* stream) {
   uint32_t word = 0;
   if (cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return GQA_ERR_CUDA;
   if (word != 0 && cudaMemset(scratch, 0, sizeof(word)) != cudaSuccess) return GQA_ERR_CUDA;
+  if (word & gqa::kDevBounds) return GQA_ERR_BOUNDS;
   if (word & gqa::kDevTimeout) return GQA_ERR_TIMEOUT;
   if (word & gqa::kDevBadInput) return GQA_ERR_INVALID_ARG;
   return GQA_OK;

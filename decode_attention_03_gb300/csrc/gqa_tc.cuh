@@ -43,6 +43,9 @@ constexpr int kTcCols = 512;        // TMEM columns allocated: S buffers at [0, 
 constexpr int kTcOCol = 128;        //   O accumulators at [128, 128 + D) and [256, 256 + D)
 constexpr int kTcOStride = 128;
 constexpr float kTcRescale = 8.f;   // log2 growth of a row max that forces an O rescale
+// tensor-memory columns: two S buffers below the first O accumulator, two O accumulators of up to
+// 128 columns inside the allocation
+static_assert(2 * kTcKeys <= kTcOCol && kTcOCol + kTcOStride + 128 <= kTcCols, "TMEM column map");
 
 template <int D, int STAGES>
 struct TcCfg {
@@ -133,6 +136,10 @@ gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   const int g_kv = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
   const int unit = b * a.h_kv + g_kv;
   const int nact = (a.rows + 31) >> 5;    // warps of a warpgroup holding real query rows
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const Win ring{sbase + C::RING_OFF, sbase + C::CTRL_OFF, a.status};
+  const Win qwin{sbase + C::Q_OFF, sbase + C::Q_OFF + C::Q_BYTES, a.status};
+  const Win pwin{sbase + C::P_OFF, sbase + C::P_OFF + 2 * C::P_BYTES, a.status};
 
   const int64_t tiles_total = (a.s_len + kTile - 1) / kTile;
   const int64_t t0 = tiles_total * split / a.n_splits;
@@ -191,11 +198,19 @@ gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         issued = it + 1;
         if (it == stall_tile) continue;  // test hook: this tile is never loaded
         const uint32_t kdst = ptx::smem_u32(smem + C::RING_OFF + s * C::STAGE_BYTES);
-        const int y = (int)(y_base + key_begin + (int64_t)it * kTcKeys);
-        ptx::mbar_arrive_expect_tx(ptx::smem_u32(k_full + s), C::KV_BYTES);
-        ptx::tma_load_3d(kdst, &tmK, ptx::smem_u32(k_full + s), 0, y, g_kv * C::HALVES, pol);
-        ptx::mbar_arrive_expect_tx(ptx::smem_u32(v_full + s), C::KV_BYTES);
-        ptx::tma_load_3d(kdst + C::KV_BYTES, &tmV, ptx::smem_u32(v_full + s), 0, y, g_kv * C::HALVES, pol);
+        const int64_t y = y_base + key_begin + (int64_t)it * kTcKeys;
+        // the boxes start inside K / V's rows and heads and land inside the ring (else the stage
+        // completes without data: the check has recorded it)
+        if (idx_ok(y, (int64_t)a.B * a.S_kv, a.status) && idx_ok(g_kv, a.h_kv, a.status) &&
+            smem_ok(kdst, C::STAGE_BYTES, ring.lo, ring.hi, a.status)) {
+          ptx::mbar_arrive_expect_tx(ptx::smem_u32(k_full + s), C::KV_BYTES);
+          ptx::tma_load_3d(kdst, &tmK, ptx::smem_u32(k_full + s), 0, (int)y, g_kv * C::HALVES, pol);
+          ptx::mbar_arrive_expect_tx(ptx::smem_u32(v_full + s), C::KV_BYTES);
+          ptx::tma_load_3d(kdst + C::KV_BYTES, &tmV, ptx::smem_u32(v_full + s), 0, (int)y, g_kv * C::HALVES, pol);
+        } else {
+          ptx::mbar_arrive(ptx::smem_u32(k_full + s));
+          ptx::mbar_arrive(ptx::smem_u32(v_full + s));
+        }
       }
       if (gave_up || stall_tile >= 0) {
         // wait (bounded) for copies still in flight before the CTA can exit
@@ -251,8 +266,9 @@ gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         uint8_t* vrow = smem + C::RING_OFF + s * C::STAGE_BYTES + C::KV_BYTES;
         for (int i = lane; i < (kTcKeys - valid) * 8 * C::HALVES; i += 32) {
           const int row = valid + i / (8 * C::HALVES), rem = i % (8 * C::HALVES);
-          *reinterpret_cast<uint4*>(vrow + (rem >> 3) * C::KPLANE + row * 128 + (rem & 7) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
+          uint8_t* dst = vrow + (rem >> 3) * C::KPLANE + row * 128 + (rem & 7) * 16;
+          if (smem_ok(ptx::smem_u32(dst), 16, ring.lo, ring.hi, a.status))
+            *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
@@ -286,11 +302,14 @@ gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
     if (wg == 0) {
       // Q row r into HALVES swizzled [128][64] planes; rows past the unit are zero
       uint8_t* qs = smem + C::Q_OFF;
-      const uint4* src = r < a.rows ? reinterpret_cast<const uint4*>(a.q + out_row(a, b, g_kv, r) * D) : nullptr;
+      const uint4* src = r < a.rows && idx_ok(out_row(a, b, g_kv, r), a.R, a.status)
+                             ? reinterpret_cast<const uint4*>(a.q + out_row(a, b, g_kv, r) * D)
+                             : nullptr;
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
         const uint4 v = src ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(qs + (c >> 3) * C::QPLANE + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+        uint8_t* dst = qs + (c >> 3) * C::QPLANE + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+        if (smem_ok(ptx::smem_u32(dst), 16, qwin.lo, qwin.hi, a.status)) *reinterpret_cast<uint4*>(dst) = v;
       }
       ptx::fence_proxy_async_smem();
       ptx::named_bar_arrive(2, 4 * 32 + 32);
@@ -382,9 +401,11 @@ gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         l += ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
         if (!prev_done && !warp_wait(empty + tp % STAGES, (uint32_t)(tp / STAGES) & 1u, a, flags, lane)) break;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        for (int c = 0; c < 8; ++c) {
+          uint8_t* dst = prow + ((c ^ (r & 7)) << 4);
+          if (smem_ok(ptx::smem_u32(dst), 16, pwin.lo, pwin.hi, a.status))
+            *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncwarp();
@@ -423,7 +444,9 @@ gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         const float f1 = mu1 == -CUDART_INF_F ? 0.f : ptx::ex2(mu1 - M);
         const float L = l * f0 + l1 * f1;
         const bool has0 = n_tiles > 0, has1 = n_tiles > 1;
-        const bool row_ok = r < a.rows;
+        // a real row, whose output (or partial) row and split slot are in range
+        const bool row_ok = r < a.rows && idx_ok(out_row(a, b, g_kv, r), a.R, a.status) &&
+                            (single || idx_ok(split, a.n_splits, a.status));
         const int64_t orow = out_row(a, b, g_kv, row_ok ? r : 0);
         const float inv = L > 0.f ? 1.f / L : 0.f;
         const uint32_t o0 = tmem + t_lane + kTcOCol, o1 = o0 + kTcOStride;
@@ -480,7 +503,7 @@ gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         const int n_items = a.rows * (D / 4);
         for (int i0 = 0; i0 < n_items; i0 += C::SOFTMAX_THREADS * 2)
           merge_pass<D, C::SOFTMAX_THREADS, 2, BF16>(a, b, g_kv, i0, a.n_splits);
-        if (threadIdx.x == 0) atomicExch(a.counters + unit, 0u);
+        if (threadIdx.x == 0 && idx_ok(unit, (int64_t)a.B * a.h_kv, a.status)) atomicExch(a.counters + unit, 0u);
       }
     }
   }

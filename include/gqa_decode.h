@@ -56,8 +56,14 @@ typedef enum {
   GQA_ERR_UNSUPPORTED = 2, /* d_head or G*T_q outside the supported set */
   GQA_ERR_WORKSPACE = 3,   /* workspace smaller than the size query asks for */
   GQA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a launch failed */
-  GQA_ERR_TIMEOUT = 5      /* a bounded device wait gave up (reported by gqa_workspace_check) */
+  GQA_ERR_TIMEOUT = 5,     /* a bounded device wait gave up (reported by gqa_workspace_check) */
+  GQA_ERR_BOUNDS = 6       /* checked build only: a device bounds check failed (gqa_workspace_check) */
 } gqa_status;
+
+/* Bits of gqa_build_flags(). */
+#define GQA_BUILD_BOUNDS_CHECK 1 /* every computed global- and shared-memory offset of the kernels is
+                                    range-checked on the device; a failure sets a status bit
+                                    (GQA_ERR_BOUNDS) and skips the access -- nothing traps */
 
 /* Optional knobs for tests and benchmarks (NULL = defaults everywhere). */
 typedef struct {
@@ -100,6 +106,10 @@ const char* gqa_status_string(int status);
 /* Library version, major*10000 + minor*100 + patch. */
 int gqa_version(void);
 
+/* How this library was built: GQA_BUILD_BOUNDS_CHECK for the checked build (libgqa_decode_checked.so,
+ * compiled with GQA_BOUNDS_CHECK=1; slower, for tests and debugging), 0 for the regular one. */
+int gqa_build_flags(void);
+
 /* Splits per (sequence, KV head) the heuristic picks on the current device for a contiguous
  * call sweeping S_kv keys; <= 0 on invalid arguments or when no device is usable. */
 int gqa_decode_num_splits(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head);
@@ -141,8 +151,9 @@ gqa_status gqa_workspace_init(void* workspace, size_t ws_bytes, void* stream);
 
 /* Synchronise `stream`, read and clear the workspace's device status word.  Returns GQA_OK,
  * GQA_ERR_TIMEOUT (a bounded wait gave up; outputs of that call are invalid and the
- * workspace must be re-initialised) or GQA_ERR_INVALID_ARG (a block id or sequence length
- * outside the pool / table was seen; affected outputs are invalid). */
+ * workspace must be re-initialised), GQA_ERR_INVALID_ARG (a block id or sequence length
+ * outside the pool / table was seen; affected outputs are invalid) or, in the checked build
+ * only, GQA_ERR_BOUNDS (a device bounds check failed: a library fault; outputs invalid). */
 gqa_status gqa_workspace_check(void* workspace, void* stream);
 
 /* Full decode step (contiguous KV).

@@ -41,8 +41,9 @@ def test_every_declared_symbol_is_exported(binding):
 
 def test_version_and_status_strings(binding):
     assert binding.gqa_version() == 10000
-    for s in range(6):
-        assert binding.gqa_status_string(s)
+    for s in range(7):
+        assert binding.gqa_status_string(s) != "unknown status"
+    assert binding.lib.gqa_build_flags() == 0                       # the regular build checks no bounds
     assert binding.gqa_status_string(99) == "unknown status"
 
 
