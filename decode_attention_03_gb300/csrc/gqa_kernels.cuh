@@ -565,6 +565,73 @@ __device__ __forceinline__ void emit_slice(const DecodeArgs& a, const float* scr
   }
 }
 
+// The same for one warp (the paged kernel's epilogue warp): a row per step, each lane folding and
+// writing D/32 consecutive columns, so that the output row's index arithmetic runs once per row
+// and the stores are 8- or 16-byte vectors.  (One element per lane per step took this warp ~15 us
+// per 512-key item of 4 KV heads on GB300 -- most of the time the item streams.)
+template <int D, int NT, int WN, int STAGES, int HG = 1, bool BF16 = false>
+__device__ __forceinline__ void emit_slice_warp(const DecodeArgs& a, const float* scratch, int b, int g0, int slice,
+                                                bool single, int lane) {
+  using C = Cfg<D, NT, WN, STAGES>;
+  constexpr int KS = kWK / HG;
+  constexpr int PER = D / 32;                          // 4 columns (d 128) or 2 (d 64) per lane
+  if (!single && !idx_ok(slice, a.n_splits, a.status)) return;
+  for (int hh = 0; hh < HG; ++hh) {
+    for (int r = 0; r < a.rows; ++r) {
+      const int col = r / C::WROWS, lr = r - col * C::WROWS;
+      const int w0 = HG > 1 ? hh * KS : col * kWK;
+      if (!idx_ok((int64_t)(w0 + KS) * C::WSCRATCH - 1, (int64_t)C::CONSUMERS * C::WSCRATCH, a.status)) return;
+      float mk[KS];
+      float M = -CUDART_INF_F;
+#pragma unroll
+      for (int k = 0; k < KS; ++k) {
+        mk[k] = scratch[(w0 + k) * C::WSCRATCH + C::WROWS * C::OSTRIDE + lr];
+        M = fmaxf(M, mk[k]);
+      }
+      float L = 0.f, o[PER];
+#pragma unroll
+      for (int i = 0; i < PER; ++i) o[i] = 0.f;
+      if (M != -CUDART_INF_F) {
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+          const float* wsp = scratch + (w0 + k) * C::WSCRATCH;
+          const float w = ptx::ex2(mk[k] - M);
+          L += w * wsp[C::WROWS * C::OSTRIDE + C::WROWS + lr];
+#pragma unroll
+          for (int i = 0; i < PER; ++i) o[i] += w * wsp[lr * C::OSTRIDE + lane * PER + i];
+        }
+      }
+      const int64_t orow = out_row(a, b, g0 + hh, r);
+      if (!idx_ok(orow, a.R, a.status)) continue;
+      if (single) {
+        // a one-partition sequence: the final output
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        uint32_t pk[PER / 2];
+#pragma unroll
+        for (int i = 0; i < PER / 2; ++i) pk[i] = Elem<BF16>::pack(o[2 * i] * inv, o[2 * i + 1] * inv);
+        __half* dst = a.o + orow * D + lane * PER;
+        if constexpr (PER == 4) {
+          *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
+        } else {
+          *reinterpret_cast<uint32_t*>(dst) = pk[0];
+        }
+      } else {
+        const int64_t prow = (int64_t)slice * a.R + orow;
+        if (lane == 0) {
+          a.ws_m[prow] = M * kLn2;
+          a.ws_l[prow] = L;
+        }
+        float* dst = a.ws_o + prow * D + lane * PER;
+        if constexpr (PER == 4) {
+          *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+          *reinterpret_cast<float2*>(dst) = make_float2(o[0], o[1]);
+        }
+      }
+    }
+  }
+}
+
 // After this slice's partial is written: take an arrival ticket for the unit; true
 // on the CTA that arrives last (all other slices of the unit are then in memory).
 template <int CTHREADS>
@@ -1117,7 +1184,7 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       const ItemDesc d = edesc[buf];
       if (d.kind == 2) break;
       const float* sb = reinterpret_cast<const float*>(smem + C::PSCRATCH_OFF + buf * C::PSCRATCH_STRIDE);
-      emit_slice<D, NT, WN, STAGES, HG, BF16>(a, sb, d.b, d.g, d.p, d.n_parts == 1, lane, 32);
+      emit_slice_warp<D, NT, WN, STAGES, HG, BF16>(a, sb, d.b, d.g, d.p, d.n_parts == 1, lane);
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(sfree + buf));
     }
