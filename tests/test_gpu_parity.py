@@ -368,3 +368,27 @@ def test_causal_partial_with_empty_rows(gqa):
         assert ((m[keep] - rm[keep]).abs() <= 1e-5 * (1 + rm[keep].abs())).all()
         assert ((l[keep] - rl[keep]).abs() <= 2e-3 * rl[keep]).all()
         assert_close(op[keep] / l[keep][:, None], oracle.normalize(rl[keep], ro[keep]), f"causal partial {s0},{n}")
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_merge_kernel_path(gqa, path):
+    """The separate merge kernel after either decode kernel: parity on repeated calls with the
+    counters left at 0, and a withheld tile reported (the workspace then re-initialised)."""
+    x = gi.make_contiguous(gi.custom(3, 2, 3000, 16, 4, 128, 1101))
+    ref = ref_contig(x)
+    units = 3 * 4
+    nbytes = gqa.gqa_decode_workspace_size(3, 2, 3000, 16, 4, 128, 6)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        o = run_contig(gqa, x, n_splits=6, merge_mode=1, mma_path=path, workspace_tensor=ws)
+        assert_close(o, ref, f"merge kernel, path {path}")
+        assert gqa.gqa_workspace_check(ws) == gqa.GQA_OK
+        assert bool((ws[256:256 + 4 * units] == 0).all())          # counters back to 0
+    q, k, v = cuda(x["q"]), cuda(x["k"]), cuda(x["v"])
+    gqa.gqa_decode(q, k, v, 16, 4, x["scale"], n_splits=6, merge_mode=1, mma_path=path, workspace_tensor=ws,
+                   timeout_us=20000, test_stall_cta=5)
+    assert gqa.gqa_workspace_check(ws) == gqa.GQA_ERR_TIMEOUT
+    gqa.gqa_workspace_init(ws)
+    assert_close(run_contig(gqa, x, n_splits=6, merge_mode=1, mma_path=path, workspace_tensor=ws), ref,
+                 "after a timeout")
+    assert gqa.gqa_workspace_check(ws) == gqa.GQA_OK
