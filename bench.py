@@ -109,7 +109,7 @@ def measured_peak():
 # device-code files that define each timed kernel (its template instantiations, the shared
 # kernel helpers and the PTX wrappers); a traffic record is valid while these are unchanged
 KERNEL_SOURCES = {
-    "gqa_split_kernel": ["gqa_kernels.cuh", "gqa_instances.cuh", "ptx.cuh", "gqa_contig_*.cu"],
+    "gqa_split_kernel": ["gqa_kernels.cuh", "gqa_instances.cuh", "ptx.cuh", "gqa_contig_*.cu", "gqa_cluster_*.cu"],
     "gqa_paged_kernel": ["gqa_kernels.cuh", "gqa_instances.cuh", "ptx.cuh", "gqa_paged_*.cu"],
     "gqa_tc_kernel": ["gqa_kernels.cuh", "gqa_tc.cuh", "ptx.cuh", "gqa_tc_*.cu"],
 }
