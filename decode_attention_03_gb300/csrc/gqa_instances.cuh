@@ -80,16 +80,11 @@ struct Inst {
   }
   static cudaError_t launch(dim3 grid, cudaStream_t st, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a) {
-    if constexpr (!CLUSTER) {
-      gqa_split_kernel<D, NT, WN, STAGES, SUB, CAUSAL, BF16><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tk, tv, a);
-      return cudaGetLastError();
-    } else {
+    if constexpr (CLUSTER) {
       if (grid.y < 2 || grid.y > (unsigned)kMaxClusterSplits) return cudaErrorInvalidValue;
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute attr[1];
-      cluster_config(cfg, attr, grid, st);
-      return cudaLaunchKernelEx(&cfg, gqa_split_kernel<D, NT, WN, STAGES, SUB, CAUSAL, BF16, true>, tk, tv, a);
     }
+    return launch_dependent(gqa_split_kernel<D, NT, WN, STAGES, SUB, CAUSAL, BF16, CLUSTER>, grid, C::THREADS,
+                            C::SMEM_BYTES, st, CLUSTER ? dim3(1, grid.y, 1) : dim3(1, 1, 1), tk, tv, a);
   }
 };
 
@@ -109,8 +104,8 @@ struct PagedInst {
   }
   static cudaError_t launch(dim3 grid, cudaStream_t st, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a) {
-    gqa_paged_kernel<D, NT, WN, STAGES, HG, BF16, VLLM><<<grid, C::PTHREADS, C::PSMEM_BYTES, st>>>(tk, tv, a);
-    return cudaGetLastError();
+    return launch_dependent(gqa_paged_kernel<D, NT, WN, STAGES, HG, BF16, VLLM>, grid, C::PTHREADS, C::PSMEM_BYTES,
+                            st, dim3(1, 1, 1), tk, tv, a);
   }
 };
 

@@ -35,6 +35,7 @@
 //   overlaps the previous one's tail.
 #pragma once
 #include <cuda.h>
+#include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
@@ -896,6 +897,9 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     ptx::prefetch_tensormap(&tmV);
   }
   __syncthreads();
+  // launched as a programmatic dependent: the set-up above may overlap the previous kernel in the
+  // stream; nothing in global memory is read or written before that kernel has completed
+  ptx::grid_dependency_wait();
 
   // ---------------------------------------------------------------- producer warp
   if (warp == C::CONSUMERS) {
@@ -1131,6 +1135,9 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     pre[0] = 0;
     ptx::fence_mbar_init();
   }
+  // launched as a programmatic dependent: nothing in global memory is read or written before the
+  // previous kernel in the stream has completed
+  ptx::grid_dependency_wait();
   // lengths (clamped to what the table can hold) and partitions per sequence
   for (int i = threadIdx.x; i < N; i += blockDim.x) {
     int len = __ldg(a.seq_lens + i);
@@ -1447,8 +1454,31 @@ gqa_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   }
 }
 
-// Fold n partials of output row r: m, l at [s * rows + r], O at [(s * rows + r) * D].
-// One warp: lane j reads the (m, l) of partials j, j+32, ...; the weights exp(m - M)
-// are broadcast with shuffles and each lane accumulates its D/32 output columns over
-// all partials, the loads of different partials independent of each other.
+// Every decode kernel is launched with programmatic stream serialisation: its CTAs may begin (and
+// set up their barriers and tensor memory) while the previous kernel in the stream finishes, and
+// wait in griddepcontrol.wait before they touch global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, unsigned block, unsigned smem, cudaStream_t st,
+                             dim3 cluster, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster.x * cluster.y * cluster.z > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster.x;
+    attr[1].val.clusterDim.y = cluster.y;
+    attr[1].val.clusterDim.z = cluster.z;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 }  // namespace gqa

@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 gqa_paged_merge_kernel(const DecodeArgs a) {
   constexpr int PER = D / 32, RPB = kMergeThreads / (32 * W);
   __shared__ float sm[RPB][W * (D + 2)];
+  if (threadIdx.x == 0) ptx::grid_launch_dependents();   // the next decode step may set up meanwhile
   ptx::grid_dependency_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rr = warp / W, w = warp % W;
@@ -139,6 +140,7 @@ gqa_merge_kernel(const float* __restrict__ m, const float* __restrict__ l, const
                  int n_parts, int64_t rows, __half* o, float* m_out, float* l_out, float* o_out, uint32_t* status) {
   constexpr int PER = D / 32, RPB = kMergeThreads / (32 * W);
   __shared__ float sm[RPB][W * (D + 2)];
+  if (threadIdx.x == 0) ptx::grid_launch_dependents();   // the next decode step may set up meanwhile
   ptx::grid_dependency_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rr = warp / W, w = warp % W;

@@ -176,6 +176,9 @@ gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = (uint32_t)flags[2];
+  // launched as a programmatic dependent: the set-up above (barriers, tensor memory) may overlap the
+  // previous kernel in the stream; nothing in global memory is touched before it has completed
+  ptx::grid_dependency_wait();
 
   if (warp == C::TMA_WARP) {
     // ------------------------------------------------------------ TMA producer
@@ -532,8 +535,8 @@ struct TcInst {
   }
   static cudaError_t launch(dim3 grid, cudaStream_t st, const CUtensorMap& tk, const CUtensorMap& tv,
                             const DecodeArgs& a) {
-    gqa_tc_kernel<D, STAGES, CAUSAL, BF16><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tk, tv, a);
-    return cudaGetLastError();
+    return launch_dependent(gqa_tc_kernel<D, STAGES, CAUSAL, BF16>, grid, C::THREADS, C::SMEM_BYTES, st,
+                            dim3(1, 1, 1), tk, tv, a);
   }
 };
 
