@@ -74,6 +74,7 @@ _SIGS = {
     "gqa_decode_partial_ex": ([_p, _p, _p, _p, _p, _p, _i, _i, _i64, _i64, _i64, _i, _i, _i, _f, _p, _sz, _p,
                                _opt], _i),
     "gqa_merge": ([_p, _p, _p, _i, _i64, _i, _p, _p], _i),
+    "gqa_merge_ex": ([_p, _p, _p, _i, _i64, _i, _p, _p, _opt], _i),
     "gqa_merge_partial": ([_p, _p, _p, _i, _i64, _i, _p, _p, _p, _p], _i),
     "gqa_decode_paged": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p], _i),
     "gqa_decode_paged_ex": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p, _sz, _p, _opt],
@@ -299,14 +300,17 @@ def gqa_decode_partial(q, k, v, h_q: int, h_kv: int, s_begin: int, s_len: int, s
     return m, l, o_part
 
 
-def gqa_merge(m: torch.Tensor, l: torch.Tensor, o_part: torch.Tensor, *, out=None, stream=None) -> torch.Tensor:
-    """Merge partials m, l (n_parts, rows), o_part (n_parts, rows, D) into o (rows, D) f16."""
+def gqa_merge(m: torch.Tensor, l: torch.Tensor, o_part: torch.Tensor, *, out=None, stream=None,
+              dtype=torch.float16) -> torch.Tensor:
+    """Merge partials m, l (n_parts, rows), o_part (n_parts, rows, D) into o (rows, D), float16 or
+    bfloat16 (the dtype of ``out`` when given, else ``dtype``)."""
     _f32(m, "m"), _f32(l, "l"), _f32(o_part, "o_part")
     n_parts, rows, D = o_part.shape
-    out = torch.empty(rows, D, dtype=torch.float16, device=o_part.device) if out is None else out
-    _f16(out, "out")
-    _check(lib.gqa_merge(_ptr(m), _ptr(l), _ptr(o_part), n_parts, rows, D, _ptr(out), _stream(stream)),
-           "gqa_merge")
+    out = torch.empty(rows, D, dtype=dtype, device=o_part.device) if out is None else out
+    _h16(out, "out")
+    opt = _opts(bf16=out.dtype == torch.bfloat16)
+    _check(lib.gqa_merge_ex(_ptr(m), _ptr(l), _ptr(o_part), n_parts, rows, D, _ptr(out), _stream(stream),
+                            ctypes.byref(opt)), "gqa_merge")
     return out
 
 

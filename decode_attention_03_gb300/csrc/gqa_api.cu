@@ -807,14 +807,19 @@ gqa_status gqa_decode_partial(const uint16_t* q, const uint16_t* k, const uint16
                                workspace, ws_bytes, stream, nullptr);
 }
 
-gqa_status gqa_merge(const float* m, const float* l, const float* o_part, int n_parts, int64_t rows, int d_head,
-                     uint16_t* o, void* stream) {
+gqa_status gqa_merge_ex(const float* m, const float* l, const float* o_part, int n_parts, int64_t rows, int d_head,
+                        uint16_t* o, void* stream, const gqa_options* opt) {
   if (n_parts < 1 || rows < 0) return GQA_ERR_INVALID_ARG;
   if (d_index(d_head) < 0) return GQA_ERR_UNSUPPORTED;
   if (rows == 0) return GQA_OK;
   if (!aligned16(m) || !aligned16(l) || !aligned16(o_part) || !aligned16(o)) return GQA_ERR_INVALID_ARG;
   return merge_launch(m, l, o_part, n_parts, rows, d_head, reinterpret_cast<__half*>(o), nullptr, nullptr, nullptr,
-                      reinterpret_cast<cudaStream_t>(stream));
+                      reinterpret_cast<cudaStream_t>(stream), opt != nullptr && opt->bf16 ? 1 : 0);
+}
+
+gqa_status gqa_merge(const float* m, const float* l, const float* o_part, int n_parts, int64_t rows, int d_head,
+                     uint16_t* o, void* stream) {
+  return gqa_merge_ex(m, l, o_part, n_parts, rows, d_head, o, stream, nullptr);
 }
 
 gqa_status gqa_merge_partial(const float* m, const float* l, const float* o_part, int n_parts, int64_t rows,

@@ -93,11 +93,11 @@ def sharded_decode(q: torch.Tensor, k_shard: torch.Tensor, v_shard: torch.Tensor
     Every rank passes the same ``q`` and its own ``k_shard, v_shard (B, s_local, h_kv*D)``: the
     rank's contiguous slice of each sequence's keys, in rank order (``shard_range``), possibly
     empty.  Returns ``O (B, T_q, h_q*D)`` on every rank (``root=None``) or on rank ``root`` only
-    (``None`` elsewhere).  float16 inputs and output, fp32 partials."""
+    (``None`` elsewhere).  float16 or bfloat16 inputs and output (q's dtype), fp32 partials."""
     from . import _binding as b
 
-    if q.dtype != torch.float16:
-        raise ValueError("sharded_decode takes float16 inputs (gqa_merge writes float16)")
+    if q.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("sharded_decode takes float16 or bfloat16 inputs")
     B, T_q, qc = q.shape
     D = qc // h_q
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)

@@ -195,6 +195,11 @@ gqa_status gqa_decode_partial_ex(const uint16_t* q, const uint16_t* k, const uin
 gqa_status gqa_merge(const float* m, const float* l, const float* o_part, int n_parts,
                      int64_t rows, int d_head, uint16_t* o, void* stream);
 
+/* gqa_merge with options: gqa_options.bf16 writes o as bfloat16 instead of IEEE binary16 (the
+ * other fields are not used).  opt NULL = gqa_merge. */
+gqa_status gqa_merge_ex(const float* m, const float* l, const float* o_part, int n_parts,
+                        int64_t rows, int d_head, uint16_t* o, void* stream, const gqa_options* opt);
+
 /* As gqa_merge but keeps the merged partial (one hop of the page's chain reduce):
  * m_out, l_out (rows) and o_out (rows, d_head), fp32. */
 gqa_status gqa_merge_partial(const float* m, const float* l, const float* o_part, int n_parts,

@@ -116,3 +116,20 @@ def test_bf16_rejects_mixed_dtypes(gqa):
     k = dev(x["k"]).float().half()
     with pytest.raises(ValueError):
         gqa.gqa_decode(q, k, k, 8, 2)
+
+
+def test_bf16_public_merge(gqa):
+    """gqa_merge writing bfloat16: the fold of fp32 partials, rounded to bf16 (the binding picks
+    gqa_merge_ex with the bf16 option from the output's dtype)."""
+    x = contig(2, 1, 2000, 8, 2, 128, 3900)
+    cuts = [0, 700, 701, 2000]
+    parts = [oracle.decode_partial(val(x["q"]), val(x["k"]), val(x["v"]), 8, 2, 128, x["scale"], a, b - a)
+             for a, b in zip(cuts[:-1], cuts[1:])]
+    m = torch.stack([p[0].reshape(-1).float() for p in parts]).cuda()
+    l = torch.stack([p[1].reshape(-1).float() for p in parts]).cuda()
+    o = torch.stack([p[2].reshape(-1, 128).float() for p in parts]).cuda()
+    out = gqa.gqa_merge(m, l, o, dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert out.dtype == torch.bfloat16
+    ref = oracle.decode(val(x["q"]), val(x["k"]), val(x["v"]), 8, 2, 128, x["scale"])
+    assert_close(out, ref.reshape(-1, 128), "bf16 merge")

@@ -10,7 +10,6 @@ GPU test: ranks as processes on cuda:0, exchanging over gloo (nothing on the dev
 another rank), each running ``sharded_decode`` on its own uneven (sometimes empty) shard; every
 rank's output is checked against the oracle on the whole sequence.
 """
-import math
 import os
 import socket
 
@@ -100,20 +99,28 @@ def test_exchange_partials_gloo(world, root):
 
 
 # ---------------------------------------------------------------- on the GPU
-def _gpu_worker(rank, world, port, out, cuts, root, shape):
+def _dev(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:                       # bfloat16 bit patterns
+        return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(a).cuda()
+
+
+def _gpu_worker(rank, world, port, out, cuts, root, shape, elem="f16"):
     _init(rank, world, port)
     torch.cuda.set_device(0)
     from decode_attention_03_gb300 import build
     build.build()
     from decode_attention_03_gb300.sharded import sharded_decode
     B, T_q, S, hq, hkv, D, seed = shape
-    x = gi.make_contiguous(gi.custom(B, T_q, S, hq, hkv, D, seed))
+    x = gi.make_contiguous(gi.custom(B, T_q, S, hq, hkv, D, seed, elem=elem))
     a, b = cuts[rank], cuts[rank + 1]
-    q = torch.from_numpy(x["q"]).cuda()
-    k = torch.from_numpy(np.ascontiguousarray(x["k"][:, a:b])).cuda()
-    v = torch.from_numpy(np.ascontiguousarray(x["v"][:, a:b])).cuda()
+    q = _dev(x["q"])
+    k = _dev(x["k"][:, a:b])
+    v = _dev(x["v"][:, a:b])
     o = sharded_decode(q, k, v, hq, hkv, x["scale"], root=root)
     torch.cuda.synchronize()
+    assert o is None or o.dtype == q.dtype
     out[rank] = None if o is None else o.double().cpu().numpy()
     dist.barrier()
     dist.destroy_process_group()
@@ -141,3 +148,21 @@ def test_sharded_decode_matches_oracle(world, cuts, root):
         err = np.abs(got - ref)
         assert (err <= 2e-3 + 2e-3 * np.abs(ref)).all(), f"rank {r}: max err {err.max():.3e}"
         assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 5e-3
+
+
+@pytest.mark.gpu
+def test_sharded_decode_bf16():
+    """bfloat16 inputs: the partials stay fp32, gqa_merge writes bfloat16 (tolerance of the bf16 path)."""
+    import oracle
+    shape = (1, 2, 3000, 16, 4, 64, 5160)
+    cuts = [0, 1234, 3000]
+    res = _run_ranks(_gpu_worker, 2, cuts, None, shape, "bf16", timeout=600)
+    B, T_q, S, hq, hkv, D, seed = shape
+    x = gi.make_contiguous(gi.custom(B, T_q, S, hq, hkv, D, seed, elem="bf16"))
+    vals = {n: gi.values(x[n], "bf16") for n in ("q", "k", "v")}
+    ref = oracle.decode(vals["q"], vals["k"], vals["v"], hq, hkv, D, x["scale"]).numpy()
+    for r in range(2):
+        got = res[r].reshape(ref.shape)
+        err = np.abs(got - ref)
+        assert (err <= 2e-3 + 8e-3 * np.abs(ref)).all(), f"rank {r}: max err {err.max():.3e}"
+        assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 1e-2
