@@ -3,8 +3,8 @@
 Each case draws its shape and options from a fixed seed (the same cases on every run), across
 the whole supported space: batch, query tokens T_q, KV heads, group size G (G*T_q up to 128
 rows), d_head 64 / 128, key counts from 1 to a few thousand, the split count and merge mode,
-the kernel (mma.sync, tcgen05, automatic), the causal tail, float16 / bfloat16, partial key
-ranges, and for paged calls both cache layouts, block sizes 8-64, partitions of 64 keys up to
+the kernel (mma.sync, tcgen05, automatic), the split kernel's cluster variant (merge mode 3),
+the causal tail, float16 / bfloat16, partial key ranges, and for paged calls both cache layouts, block sizes 8-64, partitions of 64 keys up to
 single pass, head groups, empty sequences and NaN in the unused tail slots.  Every output
 element is checked: |o - o_ref| <= 2e-3 + 2e-3 |o_ref| and the relative L2 error <= 5e-3.
 
@@ -91,7 +91,35 @@ def _contig_cases(n, seed):
 CONTIG = _contig_cases(120, 4242)
 
 
-@pytest.mark.parametrize("c", CONTIG, ids=[f"c{i:02d}" for i in range(len(CONTIG))])
+def _cluster_cases(n, seed):
+    """The split kernel's cluster variant (merge_mode 3): up to 64 rows per KV head, split counts
+    up to 40 (capped at 16 by the call), the automatic or the mma.sync path."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    cases = []
+    while len(cases) < n:
+        D = int(rng.choice([64, 128]))
+        h_kv = int(rng.choice([1, 2, 4, 8]))
+        G = int(rng.choice([1, 2, 3, 4, 5, 8, 16]))
+        T = int(rng.choice([1, 1, 2, 3, 4]))
+        if G * T > 64:
+            continue
+        S = max(int(np.exp(rng.uniform(0, np.log(9000)))), 1)
+        partial = bool(rng.random() < 0.25)
+        s0 = int(rng.integers(0, S)) if partial else 0
+        sl = int(rng.integers(0, S - s0 + 1)) if partial else S
+        cases.append(dict(B=int(rng.choice([1, 2, 3])), T=T, S=S, h_q=G * h_kv, h_kv=h_kv, D=D,
+                          path=int(rng.choice([0, 1])), n_splits=int(rng.choice([0, 2, 3, 7, 16, 40])),
+                          merge_mode=3, causal=bool(T > 1 and rng.random() < 0.4),
+                          elem=str(rng.choice(["f16", "bf16"])), partial=partial, s0=s0, sl=sl,
+                          seed=int(rng.integers(30_000, 40_000))))
+    return cases
+
+
+CLUSTER = _cluster_cases(40, 4545)
+
+
+@pytest.mark.parametrize("c", CONTIG + CLUSTER,
+                         ids=[f"c{i:02d}" for i in range(len(CONTIG))] + [f"k{i:02d}" for i in range(len(CLUSTER))])
 def test_fuzz_contiguous(gqa, c):
     w = gi.custom(c["B"], c["T"], c["S"], c["h_q"], c["h_kv"], c["D"], c["seed"], elem=c["elem"],
                   spike_frac=0.02, spike_mult=6.0)
