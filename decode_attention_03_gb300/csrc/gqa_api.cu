@@ -335,9 +335,17 @@ gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_
   } else {
     p->n_splits = 1;
   }
-  // the workspace holds the partials of the heuristic's (or the forced) split count, whatever the
-  // merge: the size query serves every merge mode
-  p->lay = ws_layout(p->units, p->n_splits, p->R, D);
+  // the workspace holds the partials of the forced split count, or of the larger of the two kernels'
+  // heuristic counts (their occupancies differ): one size query serves every MMA path and merge mode
+  int ws_splits = p->n_splits;
+  if (forced_splits == 0 && need_device) {
+    int sms = 0, occ = 0;
+    if (rows <= 64 && device_info(p->di, row_class(p->rows), 0, 0, &sms, &occ) == GQA_OK)
+      ws_splits = std::max(ws_splits, heuristic_splits(p->units, p->tiles, sms, occ));
+    if (device_info(p->di, 0, 2, 0, &sms, &occ) == GQA_OK)
+      ws_splits = std::max(ws_splits, heuristic_splits(p->units, p->tiles, sms, occ));
+  }
+  p->lay = ws_layout(p->units, ws_splits, p->R, D);
   // merge_mode 3: the unit's splits form one thread-block cluster, at most kMaxClusterSplits CTAs
   p->cluster = false;
   if (merge_mode == 3) {

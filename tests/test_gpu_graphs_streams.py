@@ -135,3 +135,47 @@ def test_cached_workspace_on_a_side_stream(gqa):
         o = gqa.gqa_decode(q, k, v, 64, 8, x["scale"], stream=s)
         s.synchronize()
         assert_close(o, ref, "cached workspace, side stream")
+
+
+# ---------------------------------------------------------------- programmatic dependent launches
+@pytest.mark.parametrize("kw", [{}, {"n_splits": 64, "merge_mode": 1}, {"merge_mode": 3}, {"mma_path": 2}])
+def test_dependent_launch_reads_the_previous_kernels_output(gqa, kw):
+    """Every decode kernel may begin while the previous kernel in the stream finishes, and waits
+    (griddepcontrol.wait) before it reads global memory.  Chain the library's own kernels -- the merge
+    kernel and the decode kernels signal their dependents early -- so that each call's Q is the
+    output the previous kernel has just written: gqa_merge -> gqa_decode -> gqa_decode.  A read
+    before the wait would see the NaN the buffers were filled with, or stale values."""
+    B, T, S, hq, hkv, D = 1, 4, 3000, 32, 8, 64
+    x = gi.make_contiguous(gi.custom(B, T, S, hq, hkv, D, 4400))
+    k, v = cuda(x["k"]), cuda(x["v"])
+    rows = B * T * hq
+    parts = [oracle.decode_partial(x["q"], x["k"], x["v"], hq, hkv, D, x["scale"], a, b - a)
+             for a, b in [(0, 1000), (1000, 3000)]]
+    m = torch.stack([p[0].reshape(-1).float() for p in parts]).cuda()
+    l = torch.stack([p[1].reshape(-1).float() for p in parts]).cuda()
+    o = torch.stack([p[2].reshape(-1, D).float() for p in parts]).cuda()
+    q1 = torch.full((B, T, hq * D), float("nan"), dtype=torch.float16, device="cuda")
+    q2 = torch.full_like(q1, float("nan"))
+    q3 = torch.full_like(q1, float("nan"))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):   # set-up outside the chain: the stream's cached workspace, first use
+        gqa.gqa_decode(q1, k, v, hq, hkv, x["scale"], out=q3, stream=s, **kw)
+    torch.cuda.synchronize()
+    q3.fill_(float("nan"))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        # a long sleep first, so that the three calls are all queued before the first one runs:
+        # each dependent kernel can then launch while its predecessor is still at work
+        torch.cuda._sleep(20_000_000)
+        gqa.gqa_merge(m, l, o, out=q1.view(rows, D), stream=s)
+        gqa.gqa_decode(q1, k, v, hq, hkv, x["scale"], out=q2, stream=s, **kw)
+        gqa.gqa_decode(q2, k, v, hq, hkv, x["scale"], out=q3, stream=s, **kw)
+    torch.cuda.synchronize()
+    # each stage against the oracle applied to the previous stage's (device-computed) values
+    r1 = oracle.decode(x["q"], x["k"], x["v"], hq, hkv, D, x["scale"])
+    assert_close(q1, r1, "merge output")
+    a1 = q1.cpu().numpy()
+    r2 = oracle.decode(a1, x["k"], x["v"], hq, hkv, D, x["scale"])
+    assert_close(q2, r2, f"decode of the merge output {kw}")
+    r3 = oracle.decode(q2.cpu().numpy(), x["k"], x["v"], hq, hkv, D, x["scale"])
+    assert_close(q3, r3, f"decode of the decode output {kw}")

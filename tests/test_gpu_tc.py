@@ -196,3 +196,21 @@ def test_plan_query(gqa):
     n, path, launches = gqa.gqa_decode_plan(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head)
     assert path == 1 and launches == 1
     assert gqa.gqa_decode_plan(1, 1, 100, 8, 2, 64, n_splits=1) == (1, 1, 1)
+
+
+@pytest.mark.parametrize("rows", [(4, 4), (8, 2), (16, 4), (16, 1)])
+def test_workspace_query_serves_every_path(gqa, rows):
+    """gqa_decode_workspace_size (automatic split count) covers both MMA paths and every merge mode:
+    the two kernels' occupancies, and so their heuristic split counts, differ."""
+    G, T = rows
+    hq, hkv = G * 8, 8
+    x = gi.make_contiguous(gi.custom(1, T, 3000, hq, hkv, 128, 2300 + G * T))
+    nbytes = gqa.gqa_decode_workspace_size(1, T, 3000, hq, hkv, 128, 0)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    r = ref(x)
+    for path in (1, 2):
+        for mode in (0, 1, 2, 3):
+            if mode == 3 and path == 2:
+                continue
+            o = run(gqa, x, mma_path=path, merge_mode=mode, workspace_tensor=ws)
+            assert_close(o, r, f"rows {G * T}, path {path}, merge {mode}")
