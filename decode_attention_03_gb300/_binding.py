@@ -257,7 +257,9 @@ def gqa_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, h_q: int, h_kv
     bfloat16 (all the same; the output has that dtype too).
     ``causal``: query token t sees keys j <= S_kv - T_q + t only.
     ``mma_path``: 0 automatic, 1 the mma.sync split kernel (G*T_q <= 64), 2 the tcgen05 kernel
-    (G*T_q <= 128)."""
+    (G*T_q <= 128).
+    ``merge_mode``: 0 automatic, 1 separate merge kernel, 2 last-arriving CTA, 3 the splits of a
+    (sequence, KV head) as one thread-block cluster (at most 16) merging in distributed shared memory."""
     B, T_q, S, D = _shape_qkv(q, k, v, h_q, h_kv)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if out is None:

@@ -69,7 +69,9 @@ typedef enum {
 typedef struct {
   int n_splits;          /* contiguous calls: splits per (sequence, KV head); 0 = heuristic */
   int merge_mode;        /* how a unit's splits are folded: 0 = automatic (the last-arriving CTA of the
-                            unit in the same kernel, except above 32 splits or, for the tcgen05
+                            unit in the same kernel; on the mma.sync kernel a cluster (3) instead where
+                            the heuristic wants more than 16 splits over at most 16 x 8 tiles (short
+                            sweeps); the separate merge kernel above 32 splits or, for the tcgen05
                             kernel, when a unit's partials exceed 256 KB), 1 = separate merge kernel,
                             2 = last-arriving CTA, 3 = the unit's splits (at most 16; more are
                             capped) run as one thread-block cluster and fold their partials through
