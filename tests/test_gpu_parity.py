@@ -392,3 +392,31 @@ def test_merge_kernel_path(gqa, path):
     assert_close(run_contig(gqa, x, n_splits=6, merge_mode=1, mma_path=path, workspace_tensor=ws), ref,
                  "after a timeout")
     assert gqa.gqa_workspace_check(ws) == gqa.GQA_OK
+
+
+@pytest.mark.parametrize("bs,part", [(16, 512), (8, 64), (64, 1024)])
+def test_paged_matches_contiguous_on_gathered_kv(gqa, bs, part):
+    """Paged decode over a shuffled pool equals contiguous decode over the same keys gathered into
+    (sequences, keys, h_kv*d) -- two different kernels -- and both match the oracle."""
+    N, L, hq, hkv, D = 3, 3000, 32, 8, 128
+    nb = (L + bs - 1) // bs
+    num_blocks = N * nb + 5
+    perm = np.random.Generator(np.random.PCG64(bs + part)).permutation(num_blocks).astype(np.int32)
+    tab = perm[:N * nb].reshape(N, nb).copy()
+    q = gi.normal_f16(6100 + bs, 0, (N, 1, hq * D))
+    kp = gi.normal_f16(6100 + bs, 1, (num_blocks, bs, hkv * D))
+    vp = gi.normal_f16(6100 + bs, 2, (num_blocks, bs, hkv * D))
+    lens = np.full(N, L, dtype=np.int32)
+    j = np.arange(L)
+    kc = np.stack([kp[tab[b, j // bs], j % bs] for b in range(N)])       # (N, L, h_kv*D), gathered
+    vc = np.stack([vp[tab[b, j // bs], j % bs] for b in range(N)])
+    scale = 1 / math.sqrt(D)
+    op = gqa.gqa_decode_paged(cuda(q).reshape(N, -1), cuda(kp), cuda(vp), cuda(tab), cuda(lens), hq, hkv, scale,
+                              max_seq_len=L, partition_size=part)
+    oc = gqa.gqa_decode(cuda(q), cuda(kc), cuda(vc), hq, hkv, scale)
+    torch.cuda.synchronize()
+    ref = oracle.decode(q, kc, vc, hq, hkv, D, scale)
+    assert_close(op, ref.reshape(N, -1), f"paged bs={bs} part={part}")
+    assert_close(oc, ref, "contiguous on the gathered keys")
+    d = (op.double().cpu().reshape(-1) - oc.double().cpu().reshape(-1)).abs()
+    assert float(d.max()) <= 2e-3, f"paged vs contiguous: {float(d.max()):.3e}"
