@@ -36,27 +36,47 @@ constexpr int paged_stages_for() {
   return n < 2 ? 2 : (n > 8 ? 8 : n);
 }
 
-// Largest cluster of the split kernel's cluster variant: 16 CTAs (beyond the portable 8, allowed
-// per kernel with cudaFuncAttributeNonPortableClusterSizeAllowed).
-constexpr int kMaxClusterSplits = 16;
+
+// Dynamic shared memory of the split kernel over a ring of `tiles` 64-key tiles (Cfg's layout: the
+// ring or the merge scratch, whichever is larger, then the barriers and flags), and for the cluster
+// variant its receiving area after them.
+template <int D, int NT, int WN>
+constexpr int split_smem_bytes(int tiles, bool cluster) {
+  using C1 = Cfg<D, NT, WN, 1>;
+  const int pipe = tiles * C1::STAGE_BYTES;
+  const int data = pipe > C1::SCRATCH_BYTES ? pipe : C1::SCRATCH_BYTES;
+  const int ctrl = 2 * tiles * 8 + 16;
+  return 1024 + data + (cluster ? ((ctrl + 15) & ~15) + ClusterRecv<C1::WROWS * WN, D>::BYTES : ctrl);
+}
+
+// Ring stages of SUB tiles: the split kernel's choice, fewer for the cluster variant where its
+// receiving area would not fit beside them (64 query rows at d_head 128: 6 -> 5 stages)
+template <int D, int NT, int WN, int SUB, bool CLUSTER>
+constexpr int split_stages() {
+  int st = stages_for<D, NT, WN>() / SUB;
+  while (CLUSTER && st > 2 && split_smem_bytes<D, NT, WN>(st * SUB, true) > 227 * 1024) --st;
+  return st;
+}
 
 template <int D, int CLS, bool CAUSAL, bool BF16, bool CLUSTER = false>
 struct Inst {
   static constexpr int NT = cls_nt(CLS);
   static constexpr int WN = cls_wn(CLS);
   static constexpr int SUB = split_sub(D);
-  static constexpr int STAGES = stages_for<D, NT, WN>() / SUB;   // ring stages of SUB tiles
+  static constexpr int STAGES = split_stages<D, NT, WN, SUB, CLUSTER>();   // ring stages of SUB tiles
   using C = Cfg<D, NT, WN, STAGES * SUB>;
-  static_assert(C::SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static constexpr int SMEM = split_smem_bytes<D, NT, WN>(STAGES * SUB, CLUSTER);
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(CLUSTER || SMEM == C::SMEM_BYTES, "the size formula follows Cfg's layout");
 
   // resident CTAs per SM; for the cluster variant, the number of clusters of kMaxClusterSplits CTAs
   // the GPU can hold at once is the occupancy reported (0: that cluster size cannot be scheduled)
   static cudaError_t prepare(int* occupancy) {
     auto fn = gqa_split_kernel<D, NT, WN, STAGES, SUB, CAUSAL, BF16, CLUSTER>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     if constexpr (!CLUSTER) {
-      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, fn, C::THREADS, C::SMEM_BYTES);
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occupancy, fn, C::THREADS, SMEM);
     } else {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
@@ -69,7 +89,7 @@ struct Inst {
   static void cluster_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[1], dim3 grid, cudaStream_t st) {
     cfg.gridDim = grid;
     cfg.blockDim = dim3(C::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.dynamicSmemBytes = SMEM;
     cfg.stream = st;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
@@ -83,8 +103,8 @@ struct Inst {
     if constexpr (CLUSTER) {
       if (grid.y < 2 || grid.y > (unsigned)kMaxClusterSplits) return cudaErrorInvalidValue;
     }
-    return launch_dependent(gqa_split_kernel<D, NT, WN, STAGES, SUB, CAUSAL, BF16, CLUSTER>, grid, C::THREADS,
-                            C::SMEM_BYTES, st, CLUSTER ? dim3(1, grid.y, 1) : dim3(1, 1, 1), tk, tv, a);
+    return launch_dependent(gqa_split_kernel<D, NT, WN, STAGES, SUB, CAUSAL, BF16, CLUSTER>, grid, C::THREADS, SMEM,
+                            st, CLUSTER ? dim3(1, grid.y, 1) : dim3(1, 1, 1), tk, tv, a);
   }
 };
 

@@ -743,85 +743,159 @@ __device__ __forceinline__ void merge_unit(const DecodeArgs& a, int b, int g, in
 // =====================================================================================
 // merge inside a thread-block cluster: the splits of one unit are the CTAs of one cluster
 // =====================================================================================
-// Layout of a CTA's partial in its own shared memory (the cluster variant of the split
-// kernel): m, l [RMAX] (log2 domain) and O [RMAX][D], fp32, at byte offset `off`.
+// Largest cluster of the split kernel's cluster variant: 16 CTAs (beyond the portable 8, allowed
+// per kernel with cudaFuncAttributeNonPortableClusterSizeAllowed).
+constexpr int kMaxClusterSplits = 16;
+static_assert(kMaxClusterSplits <= 32, "the cluster fold checks the CTAs' flags one per lane of a warp");
+
+// The receiving area of a CTA of the cluster variant, in shared memory of its own (apart from the
+// ring, which siblings may still be filling when they push): the unit's items -- (row, 4 columns)
+// pairs -- are dealt out to the n CTAs in contiguous runs of at most ipo = ceil(items / n), and
+// every CTA pushes its partial of each item to the item's owner: float4 O [n][ipo] and
+// float2 (m, l) [n][ipo] (m in the log2 domain), source-major, plus the sources' completion flags.
 template <int RMAX, int D>
-struct ClusterPartial {
-  static constexpr int M = 0;
-  static constexpr int L = RMAX * 4;
-  static constexpr int O = 2 * RMAX * 4;   // 16-byte aligned (RMAX is a multiple of 8)
-  static constexpr int BYTES = O + RMAX * D * 4;
+struct ClusterRecv {
+  static constexpr int ITEMS = RMAX * (D / 4);
+  static constexpr int SLOTS = ITEMS + kMaxClusterSplits;   // n * ipo <= items + n - 1
+  static constexpr int O = 0;
+  static constexpr int ML = SLOTS * 16;
+  static constexpr int VALID = ML + SLOTS * 8;
+  static constexpr int BYTES = VALID + kMaxClusterSplits * 4;
 };
 
-// This CTA's combined partial: every query row of the unit, its key-slice warps folded.
+// Items [first, end) of the unit's n_items that CTA `rank` of n owns, and the owner of an item:
+// ceil(rank * n_items / n) <= item < ceil((rank + 1) * n_items / n)  <=>  owner = floor(item * n / n_items).
+// 32-bit arithmetic: n_items <= 64 rows x 32 column groups, n <= kMaxClusterSplits (the 64-bit
+// divisions took a quarter of a microsecond of the fold).
+__device__ __forceinline__ int cluster_first_item(int rank, int n, int n_items) {
+  return (rank * n_items + n - 1) / n;
+}
+
+// This CTA's partial of every item of the unit, its key-slice warps folded, pushed into the
+// owners' receiving areas through distributed shared memory (the stores are complete, for the
+// owners, once the cluster barrier that follows has been passed).  `recv`: the receiving area's
+// shared-memory address, the same offset in every CTA.
 template <int D, int NT, int WN, int STAGES>
-__device__ __forceinline__ void emit_cta_partial(const DecodeArgs& a, const float* scratch, uint8_t* cp, int tid,
-                                                 int nthreads) {
+__device__ __forceinline__ void push_cta_partial(const DecodeArgs& a, const float* scratch, uint32_t recv, int n,
+                                                 int rank, int tid, int nthreads) {
   using C = Cfg<D, NT, WN, STAGES>;
-  using P = ClusterPartial<C::WROWS * WN, D>;
-  float* cm = reinterpret_cast<float*>(cp + P::M);
-  float* cl = reinterpret_cast<float*>(cp + P::L);
-  float* co = reinterpret_cast<float*>(cp + P::O);
-  for (int idx = tid; idx < a.rows * D; idx += nthreads) {
-    const int r = idx / D, d = idx - r * D;
+  using RV = ClusterRecv<C::WROWS * WN, D>;
+  constexpr int DQ = D / 4;
+  const int n_items = a.rows * DQ;
+  const int ipo = (n_items + n - 1) / n;
+  for (int idx = tid; idx < n_items; idx += nthreads) {
+    const int r = idx / DQ, c4 = idx - r * DQ;
     const int col = r / C::WROWS, lr = r - col * C::WROWS;
-    float M, L, O;
-    combine_warps<D, NT, WN, STAGES, kWK>(scratch, col * kWK, lr, d, M, L, O, a.status);
-    if (!idx_ok(r, C::WROWS * WN, a.status)) continue;   // rows of the partial's layout
-    co[r * D + d] = O;
-    if (d == 0) {
-      cm[r] = M;
-      cl[r] = L;
+    const int w0 = col * kWK;
+    if (!idx_ok((int64_t)(w0 + kWK) * C::WSCRATCH - 1, (int64_t)C::CONSUMERS * C::WSCRATCH, a.status) ||
+        !idx_ok(lr, C::WROWS, a.status))
+      continue;
+    // the kWK key-slice warps of row r, columns 4 c4 .. 4 c4 + 3
+    float mk[kWK];
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int k = 0; k < kWK; ++k) {
+      mk[k] = scratch[(w0 + k) * C::WSCRATCH + C::WROWS * C::OSTRIDE + lr];
+      M = fmaxf(M, mk[k]);
     }
+    float L = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -CUDART_INF_F) {
+#pragma unroll
+      for (int k = 0; k < kWK; ++k) {
+        const float* wsp = scratch + (w0 + k) * C::WSCRATCH;
+        const float w = ptx::ex2(mk[k] - M);
+        L += w * wsp[C::WROWS * C::OSTRIDE + C::WROWS + lr];
+        const float4 o = *reinterpret_cast<const float4*>(wsp + lr * C::OSTRIDE + c4 * 4);
+        O.x += w * o.x;
+        O.y += w * o.y;
+        O.z += w * o.z;
+        O.w += w * o.w;
+      }
+    }
+    const int owner = idx * n / n_items;
+    const int j = idx - cluster_first_item(owner, n, n_items);
+    const int slot = rank * ipo + j;
+    if (!idx_ok(slot, RV::SLOTS, a.status) || !idx_ok(owner, n, a.status)) continue;
+    const uint32_t dst = ptx::mapa(recv, (uint32_t)owner);
+    ptx::st_cluster_v4(dst + RV::O + slot * 16, O);
+    ptx::st_cluster_v2(dst + RV::ML + slot * 8, M, L);
   }
 }
 
-// Fold the n CTAs' partials of unit (b, g) (page: _merge_running over the splits in order, then
-// O / l) for this CTA's share of the unit's outputs -- items (row, 4 columns) [lo, hi) of
-// rows * D/4 -- reading every partial through distributed shared memory, and write the output
-// (or the merged partial).  `cp` is the shared-memory address of this CTA's partial (the same
-// offset in every CTA); `valid` its flag word.  Nothing is written unless every CTA of the
-// cluster completed its slice (a wait that gave up leaves the output alone).
+// One online-softmax merge step of two partials (M in the log2 domain): the page's
+// _merge_running, both sides rescaled to the larger max; empty sides (M = -inf) contribute nothing.
+__device__ __forceinline__ void merge_into(float& M, float& L, float4& O, float m2, float l2, const float4& o2) {
+  const float m_new = fmaxf(M, m2);
+  const float ref = m_new == -CUDART_INF_F ? 0.f : m_new;   // both sides empty so far
+  const float so = ptx::ex2(M - ref), sn = ptx::ex2(m2 - ref);
+  L = L * so + l2 * sn;
+  O.x = O.x * so + o2.x * sn;
+  O.y = O.y * so + o2.y * sn;
+  O.z = O.z * so + o2.z * sn;
+  O.w = O.w * so + o2.w * sn;
+  M = m_new;
+}
+
+// After the cluster barrier: fold, for this CTA's items, the n sources' partials it received (the
+// page's _merge_running, then O / l) from its own shared memory, and write the output (or the
+// merged partial).  An item's sources are spread over a group of `lpi` lanes (a power of two, up to
+// 16, as many as the CTA's threads allow): lane k of the group folds sources k, k + lpi, ... in
+// order, then the group combines its lanes in a fixed butterfly of shuffles -- a fixed order, so
+// results are reproducible; one thread walking all 16 sources took ~1 us for the tiny workload.
+// Nothing is written unless every CTA completed its slice (a wait that gave up leaves the output
+// alone).
 template <int RMAX, int D, int NTH, bool BF16>
-__device__ __forceinline__ void cluster_merge(const DecodeArgs& a, int b, int g, uint32_t cp, uint32_t valid, int n,
+__device__ __forceinline__ void fold_received(const DecodeArgs& a, int b, int g, const uint8_t* recv, int n,
                                               int rank) {
-  using P = ClusterPartial<RMAX, D>;
+  using RV = ClusterRecv<RMAX, D>;
   constexpr int DQ = D / 4;
-  constexpr int UNR = 8;
-  bool all_valid = true;
-  for (int s = 0; s < n; ++s) all_valid &= ptx::ld_cluster_s32(ptx::mapa(valid, (uint32_t)s)) != 0;
-  if (!all_valid) return;
+  const int lane = threadIdx.x & 31;
+  const int flag = lane < n ? reinterpret_cast<const volatile int*>(recv + RV::VALID)[lane] : 1;
+  if (!__all_sync(0xffffffffu, flag != 0)) return;
   const int n_items = a.rows * DQ;
-  const int lo = (int)((int64_t)n_items * rank / n), hi = (int)((int64_t)n_items * (rank + 1) / n);
-  for (int item = lo + (int)threadIdx.x; item < hi; item += NTH) {
-    const int r = item / DQ, c4 = item - r * DQ;
-    if (!idx_ok(r, RMAX, a.status) || !idx_ok(out_row(a, b, g, r), a.R, a.status)) continue;
+  const int ipo = (n_items + n - 1) / n;
+  const int lo = cluster_first_item(rank, n, n_items), hi = cluster_first_item(rank + 1, n, n_items);
+  int lg = 0;   // lanes per item: 1 << lg
+  while (lg < 4 && (1 << lg) < n && (hi - lo) << (lg + 1) <= NTH) ++lg;
+  const int lpi = 1 << lg;
+  const int sub = (int)threadIdx.x & (lpi - 1);
+  const float4* ro = reinterpret_cast<const float4*>(recv + RV::O);
+  const float2* rml = reinterpret_cast<const float2*>(recv + RV::ML);
+  // every thread runs the same number of rounds, so that whole warps meet at the shuffles
+  for (int base = lo; base < hi; base += NTH >> lg) {
+    const int item = base + ((int)threadIdx.x >> lg);
+    const int j = item - lo;
+    const bool mine = item < hi && idx_ok((int64_t)(n - 1) * ipo + j, RV::SLOTS, a.status);
     float M = -CUDART_INF_F, L = 0.f;
     float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < n; s0 += UNR) {
-      float ms[UNR], ls[UNR];
-      float4 os[UNR];
-#pragma unroll
-      for (int u = 0; u < UNR; ++u) {   // every load of the chunk issued before any fold
-        const bool have = s0 + u < n;
-        const uint32_t base = ptx::mapa(cp, (uint32_t)(have ? s0 + u : 0));
-        ms[u] = have ? ptx::ld_cluster_f32(base + P::M + r * 4) : -CUDART_INF_F;
-        ls[u] = have ? ptx::ld_cluster_f32(base + P::L + r * 4) : 0.f;
-        os[u] = have ? ptx::ld_cluster_v4(base + P::O + (r * D + c4 * 4) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (mine)
+      for (int s = sub; s < n; s += lpi) {
+        const float2 ml = rml[s * ipo + j];
+        merge_into(M, L, O, ml.x, ml.y, ro[s * ipo + j]);
       }
-#pragma unroll
-      for (int u = 0; u < UNR; ++u) {
-        const float m_new = fmaxf(M, ms[u]);
-        const float ref = m_new == -CUDART_INF_F ? 0.f : m_new;   // both sides empty so far
-        const float so = ptx::ex2(M - ref), sn = ptx::ex2(ms[u] - ref);
-        L = L * so + ls[u] * sn;
-        O.x = O.x * so + os[u].x * sn;
-        O.y = O.y * so + os[u].y * sn;
-        O.z = O.z * so + os[u].z * sn;
-        O.w = O.w * so + os[u].w * sn;
-        M = m_new;
-      }
+    for (int off = lpi >> 1; off > 0; off >>= 1) {   // the group's butterfly
+      const float m2 = __shfl_xor_sync(0xffffffffu, M, off), l2 = __shfl_xor_sync(0xffffffffu, L, off);
+      float4 o2;
+      o2.x = __shfl_xor_sync(0xffffffffu, O.x, off);
+      o2.y = __shfl_xor_sync(0xffffffffu, O.y, off);
+      o2.z = __shfl_xor_sync(0xffffffffu, O.z, off);
+      o2.w = __shfl_xor_sync(0xffffffffu, O.w, off);
+      // both lanes of a pair fold (lower lane's partial, upper lane's) in that order: the same
+      // result on both, selected rather than branched on so the pair does not diverge
+      const bool upper = (threadIdx.x & off) != 0;
+      float M1 = upper ? m2 : M, L1 = upper ? l2 : L;
+      float4 O1 = upper ? o2 : O;
+      const float M2 = upper ? M : m2, L2 = upper ? L : l2;
+      const float4 O2 = upper ? O : o2;
+      merge_into(M1, L1, O1, M2, L2, O2);
+      M = M1;
+      L = L1;
+      O = O1;
     }
+    if (!mine || sub != 0) continue;
+    const int r = item / DQ, c4 = item - r * DQ;
+    if (!idx_ok(r, RMAX, a.status) || !idx_ok(out_row(a, b, g, r), a.R, a.status)) continue;
     const int64_t orow = out_row(a, b, g, r);
     if (a.o != nullptr) {
       const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -858,9 +932,8 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   constexpr int KVB = SUB * C::KV_BYTES;     // K (or V) bytes of one stage
   constexpr int STB = 2 * KVB;               // one stage
   constexpr int SROWS = SUB * kTile;         // keys (TMA box rows) per stage
-  using CP = ClusterPartial<C::WROWS * WN, D>;
-  constexpr int CP_OFF = (C::SCRATCH_BYTES + 15) & ~15;   // this CTA's partial (CLUSTER), after the scratch
-  static_assert(!CLUSTER || CP_OFF + CP::BYTES <= C::DATA_BYTES, "cluster partial fits the drained ring");
+  // CLUSTER: the receiving area, after the barriers and flags (split_smem_bytes counts it)
+  constexpr int RECV_OFF = C::DATA_BYTES + ((C::CTRL_BYTES + 15) & ~15);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::DATA_BYTES);
@@ -944,9 +1017,8 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         }
       }
     }
-    if constexpr (CLUSTER) {   // the producer's threads take part in both cluster barriers too
+    if constexpr (CLUSTER) {   // the producer's threads take part in the cluster barrier too
       __syncwarp();
-      ptx::cluster_sync();
       ptx::cluster_sync();
     }
     return;
@@ -987,20 +1059,23 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   if (threadIdx.x == 0) ptx::grid_launch_dependents();   // a separate merge kernel may start launching
   const bool aborted = ptx::named_bar_or(1, C::CTHREADS, flags[0] != 0);
   if constexpr (CLUSTER) {
-    // this CTA's partial into its own shared memory, then the cluster folds all of them; a CTA
-    // whose wait gave up still takes part in both barriers, flagging its partial incomplete
+    // push this CTA's partial of every item to the item's owner (distributed shared memory) and
+    // its completion flag to every CTA; one cluster barrier; then each CTA folds the items it owns
+    // from its own shared memory and leaves -- nothing reads another CTA's shared memory.  A CTA
+    // whose wait gave up pushes no partial and flags it incomplete.
+    using RV = ClusterRecv<C::WROWS * WN, D>;
+    const uint32_t recv = ptx::smem_u32(smem + RECV_OFF);
+    const int n = a.n_splits;
     if (!aborted) {
       float* scratch = reinterpret_cast<float*>(smem);
       stash_warp<D, NT, WN, STAGES>(st, scratch, warp, lane, a.status);
       ptx::named_bar_sync(1, C::CTHREADS);
-      emit_cta_partial<D, NT, WN, STAGES>(a, scratch, smem + CP_OFF, threadIdx.x, C::CTHREADS);
-      if (threadIdx.x == 0) flags[2] = 1;
+      push_cta_partial<D, NT, WN, STAGES>(a, scratch, recv, n, split, threadIdx.x, C::CTHREADS);
     }
-    ptx::cluster_sync();   // every CTA's partial (and flag) visible to the cluster
-    cluster_merge<C::WROWS * WN, D, C::CTHREADS, BF16>(a, b, g_kv, ptx::smem_u32(smem + CP_OFF),
-                                                       ptx::smem_u32(const_cast<int*>(flags + 2)), a.n_splits,
-                                                       split);
-    ptx::cluster_sync();   // no CTA leaves while the cluster may still read its partial
+    if (threadIdx.x < n)   // this CTA's flag into CTA threadIdx.x's receiving area
+      ptx::st_cluster_s32(ptx::mapa(recv + RV::VALID + split * 4, threadIdx.x), aborted ? 0 : 1);
+    ptx::cluster_sync();   // every push (and flag) complete and visible to its owner
+    fold_received<C::WROWS * WN, D, C::CTHREADS, BF16>(a, b, g_kv, smem + RECV_OFF, n, split);
     return;
   }
   if (aborted) return;

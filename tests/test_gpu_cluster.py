@@ -45,6 +45,7 @@ def test_cluster_caps_at_sixteen(gqa):
     (1, 2, 3001, 16, 2, 64),      # 16 rows (two n-tiles)
     (1, 4, 2999, 32, 4, 128),     # 32 rows (two warp columns)
     (1, 8, 1500, 64, 8, 64),      # 64 rows (four warp columns)
+    (1, 8, 2500, 64, 8, 128),     # 64 rows at d_head 128 (the cluster variant's shorter ring)
     (3, 1, 65, 8, 2, 64),         # two tiles, ragged
     (1, 1, 1, 8, 1, 128),         # one key
 ])
