@@ -100,8 +100,8 @@ def test_cluster_is_deterministic(gqa):
 
 
 def test_cluster_timeout_is_reported_not_hung(gqa):
-    """One CTA of a cluster withholds a tile: its waits give up, it still joins both cluster
-    barriers, the cluster writes nothing for that unit, the status word says timeout, and the
+    """One CTA of a cluster withholds a tile: its waits give up, it still pushes its completion
+    flag and joins the cluster barrier, the cluster writes nothing for that unit, the status word says timeout, and the
     next call succeeds."""
     x = gi.make_contiguous(gi.custom(1, 1, 8192, 8, 2, 128, 7800))
     q, k, v = cuda(x["q"]), cuda(x["k"]), cuda(x["v"])
