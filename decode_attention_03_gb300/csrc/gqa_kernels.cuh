@@ -921,8 +921,9 @@ __device__ __forceinline__ void fold_received(const DecodeArgs& a, int b, int g,
 __host__ __device__ constexpr int split_sub(int D) { return D == 64 ? 2 : 1; }
 
 // CLUSTER: launched with cluster dimensions (1, n_splits, 1) -- the splits of a unit are the CTAs
-// of one cluster, which fold their partials through distributed shared memory in place of the
-// workspace and the arrival ticket (every thread of the CTA stays until the cluster has read them).
+// of one cluster, which exchange their partials through distributed shared memory in place of the
+// workspace and the arrival ticket (every thread of every CTA takes part in both phases of the
+// cluster barrier: one before the first remote store, one after the last).
 template <int D, int NT, int WN, int STAGES, int SUB, bool CAUSAL, bool BF16, bool CLUSTER = false>
 __global__ void __launch_bounds__(Cfg<D, NT, WN, STAGES * SUB>::THREADS)
 gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -970,6 +971,9 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     ptx::prefetch_tensormap(&tmV);
   }
   __syncthreads();
+  // CLUSTER: first phase of the cluster barrier, waited for before the first access to another
+  // CTA's shared memory (which must be running by then); every CTA arrives here, long before
+  if constexpr (CLUSTER) ptx::cluster_arrive_relaxed();
   // launched as a programmatic dependent: the set-up above may overlap the previous kernel in the
   // stream; nothing in global memory is read or written before that kernel has completed
   ptx::grid_dependency_wait();
@@ -1017,8 +1021,9 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         }
       }
     }
-    if constexpr (CLUSTER) {   // the producer's threads take part in the cluster barrier too
+    if constexpr (CLUSTER) {   // the producer's threads take part in both cluster barrier phases too
       __syncwarp();
+      ptx::cluster_wait();
       ptx::cluster_sync();
     }
     return;
@@ -1066,6 +1071,7 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     using RV = ClusterRecv<C::WROWS * WN, D>;
     const uint32_t recv = ptx::smem_u32(smem + RECV_OFF);
     const int n = a.n_splits;
+    ptx::cluster_wait();   // every CTA of the cluster is running: its shared memory may be written
     if (!aborted) {
       float* scratch = reinterpret_cast<float*>(smem);
       stash_warp<D, NT, WN, STAGES>(st, scratch, warp, lane, a.status);
