@@ -22,16 +22,27 @@ constexpr size_t kHeaderBytes = 256;        // status word (+ reserved)
 constexpr int kMinTilesPerSplit = 1;        // a split streams at least one 64-key tile
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;
 constexpr int kMaxDevices = 64;
-// Automatic merge choice of the tcgen05 kernel: the last CTA of a unit folds the splits
-// itself only while the unit's partials stay below this size; above it one CTA streaming
-// them is latency-bound (128 rows x 19 splits = 1.26 MB took 42 us in-kernel on GB300
-// against a few us for the separate merge kernel spread over the whole GPU).
-constexpr int64_t kInKernelMergeBytes = 256 * 1024;
 constexpr int kTcMinRows = 16;              // automatic MMA path: tcgen05 from this many rows per KV head
-// Automatic merge: more splits than this go to the separate merge kernel (the last CTA folding
-// them serialises the fold: tiny workload, 64 splits, 16.7 us in-kernel vs 11.9 us with the merge
-// kernel; 16 splits in-kernel 12.7 us)
-constexpr int kInKernelMaxSplits = 32;
+// Automatic merge: the mma.sync split kernel folds 2 to kMaxClusterSplits splits in one cluster
+// (distributed shared memory, one launch), more in the merge kernel, launched as a programmatic
+// dependent; the tcgen05 kernel's splits always go to the merge kernel.  The last CTA of a unit
+// folding the splits itself (merge_mode 2) is taken only on request: one CTA streaming a unit's
+// partials is latency-bound (tcgen05, 128 rows x 19 splits = 1.26 MB: 42 us in-kernel against a
+// few us for the merge kernel spread over the GPU; tiny workload, 64 splits: 16.7 vs 11.9 us),
+// and with the merge kernel overlapping the decode kernel's tail it lost on small partials too.
+// Measured on GB300 (us per step; last-CTA fold / cluster / merge kernel), inputs larger than L2,
+// d_head 128 unless noted.  mma.sync kernel:
+// 8 x 32768 keys, 4 rows, 3 splits 153.5 / 151.3 / 151.6; 8 rows 154.9 / 151.9 / 153.3; 16 rows
+// 162.3 / 156.1 / 177.3; 32 rows 179.6 / 176.1 / 179.0; d_head 64, 16 rows 92.2 / 88.3 / 91.2, 64
+// rows 211.2 / 186.2 / 210.1; 4 x 65536 keys (6 splits) 153.6 / 151.8 / 152.3; 16 x 16384 (2)
+// 158.5 / 154.9 / 159.6; 2 x 131072 (12) 154.6 / 152.9 / 151.7; one sequence of 2^18 keys (24
+// splits) 155.8 / - / 152.5, of 2^20 keys 586.9 / - / 582.5.  Where the cluster's receiving area
+// costs a ring stage (64 rows at d_head 128: 510.9 / 518.9 / 509.5) or a resident CTA per SM,
+// the merge kernel serves instead.  tcgen05 kernel (last-CTA fold / merge kernel): 8 x 32768 keys,
+// 16 rows, 2 splits 160.7 / 159.7; 32 rows 162.7 / 160.8; 2^18 keys, 16 rows, 19 splits 158.9 /
+// 155.2; 2 x 131072 keys, 16 rows, 9 splits 158.1 / 155.6; d_head 64, 8 x 32768, 16 rows 124.6 /
+// 120.9; d_head 64, 2^18 keys, 32 rows, 19 splits 101.2 / 103.5 (the one shape where the fold
+// in-kernel was faster).
 // Automatic merge, short sweeps: where the heuristic asks for more splits than a cluster holds and
 // every CTA of a 16-CTA cluster gets at most this many 64-key tiles, the unit's splits run as one
 // cluster folding through distributed shared memory (one launch, no partials in global memory).
@@ -72,6 +83,8 @@ bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 struct DevState {
   bool ready = false;
   int sms = 0;
+  int smem_sm = 0;             // shared memory per SM and reserved per CTA (bytes)
+  int smem_reserved = 0;
   int occ[2][4][12][2] = {};   // [d index][row class][kernel: see kernel_slot][bf16] resident CTAs
                                // per SM (cluster variant: clusters of kMaxClusterSplits the GPU holds),
                                // 0 = not prepared
@@ -140,6 +153,21 @@ int kernel_slot(int kind) {
   return (kind < 200 ? 2 : 7) + hg_slot;   // paged: 2-4, vLLM layout: 7-9
 }
 
+// The split kernel's shared-memory layouts per (d index, row class): the plain kernel's and the
+// cluster variant's dynamic shared memory, and whether the variant keeps the plain ring depth
+struct SplitLayout {
+  int smem_plain, smem_cluster;
+  bool same_ring;
+};
+template <int D, int CLS>
+constexpr SplitLayout split_layout() {
+  return {Inst<D, CLS, false, false, false>::SMEM, Inst<D, CLS, false, false, true>::SMEM,
+          Inst<D, CLS, false, false, false>::STAGES == Inst<D, CLS, false, false, true>::STAGES};
+}
+constexpr SplitLayout kSplitLayout[2][4] = {
+    {split_layout<64, 0>(), split_layout<64, 1>(), split_layout<64, 2>(), split_layout<64, 3>()},
+    {split_layout<128, 0>(), split_layout<128, 1>(), split_layout<128, 2>(), split_layout<128, 3>()}};
+
 // SM count and resident CTAs per SM of one kernel configuration on the current device
 gqa_status device_info(int di, int cls, int kind, int bf16, int* sms, int* occ) {
   int dev = 0;
@@ -147,7 +175,10 @@ gqa_status device_info(int di, int cls, int kind, int bf16, int* sms, int* occ) 
   std::lock_guard<std::mutex> lock(g_mu);
   DevState& st = g_dev[dev];
   if (!st.ready) {
-    if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return GQA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&st.smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&st.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+      return GQA_ERR_CUDA;
     if (g_encode == nullptr) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -170,6 +201,16 @@ gqa_status device_info(int di, int cls, int kind, int bf16, int* sms, int* occ) 
   *sms = st.sms;
   *occ = o;
   return GQA_OK;
+}
+
+// CTAs per SM that `smem` bytes of dynamic shared memory allow on the current device (0 before
+// device_info has read its attributes)
+int smem_residency(int smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  const DevState& st = g_dev[dev];
+  return st.ready ? st.smem_sm / (smem + st.smem_reserved) : 0;
 }
 
 // 3-D map over a (rows, cols) f16 / bf16 matrix seen as (64-column planes, rows, 64 columns):
@@ -352,12 +393,24 @@ gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_
     if (p->tc) return GQA_ERR_UNSUPPORTED;
     if (p->n_splits > kMaxClusterSplits) p->n_splits = kMaxClusterSplits;
     p->cluster = p->n_splits > 1;
-  } else if (merge_mode == 0 && !p->tc && forced_splits == 0 && need_device && p->n_splits > kMaxClusterSplits &&
-             p->tiles <= (int64_t)kMaxClusterSplits * kClusterMaxTilesPerSplit) {
+  } else if (merge_mode == 0 && !p->tc && need_device && p->n_splits > 1) {
+    // automatic, mma.sync kernel: 2 to kMaxClusterSplits splits fold in one cluster where the
+    // variant keeps the plain kernel's ring depth and does not add a wave of CTAs (its resident CTAs
+    // per SM are the plain kernel's, for which the split count was chosen, or the grid fits in one
+    // wave at its own); a short sweep asking for more splits runs as one cluster of
+    // kMaxClusterSplits; anything else goes to the merge kernel (merge_in_kernel)
+    const SplitLayout& L = kSplitLayout[p->di][p->cls];
+    const bool short_sweep = forced_splits == 0 && p->n_splits > kMaxClusterSplits &&
+                             p->tiles <= (int64_t)kMaxClusterSplits * kClusterMaxTilesPerSplit;
+    const bool holds = p->n_splits <= kMaxClusterSplits && L.same_ring;
     int sms = 0, clusters = 0;   // only where a cluster of kMaxClusterSplits can be scheduled
-    if (device_info(p->di, p->cls, 4, 0, &sms, &clusters) == GQA_OK && clusters > 0) {
-      p->n_splits = kMaxClusterSplits;
-      p->cluster = true;
+    if ((short_sweep || holds) && device_info(p->di, p->cls, 4, 0, &sms, &clusters) == GQA_OK && clusters > 0) {
+      const int res = smem_residency(L.smem_cluster);
+      const bool one_wave = p->units * p->n_splits <= (int64_t)sms * res;
+      if (short_sweep || (res > 0 && (res >= smem_residency(L.smem_plain) || one_wave))) {
+        if (short_sweep) p->n_splits = kMaxClusterSplits;
+        p->cluster = true;
+      }
     }
   }
   return GQA_OK;
@@ -419,15 +472,10 @@ cudaError_t paged_merge_launch_w(const DecodeArgs& a, cudaStream_t st) {
   return launch_pdl(gqa_paged_merge_kernel<D, BF16, W>, (unsigned)((a.R + rpb - 1) / rpb), kMergeThreads, st, a);
 }
 
-// merge_mode 0 (automatic): in-kernel up to kInKernelMaxSplits splits (and, for the tcgen05 kernel,
-// while a unit's partials are at most kInKernelMergeBytes); 1 separate kernel; 2 in-kernel
-bool merge_in_kernel(const ContigPlan& p, int D, int merge_mode) {
-  if (p.cluster) return true;
-  if (merge_mode == 1) return false;
-  if (merge_mode == 2) return true;
-  if (p.n_splits > kInKernelMaxSplits) return false;
-  return !p.tc || (int64_t)p.n_splits * p.rows * (D + 2) * 4 <= kInKernelMergeBytes;
-}
+// Whether the splits fold inside the decode launch (a cluster, or the unit's last CTA) rather than
+// in the merge kernel: the cluster where plan_contig chose it (merge_mode 3, or automatic), the
+// last CTA for merge_mode 2; otherwise (automatic, or merge_mode 1) the merge kernel.
+bool merge_in_kernel(const ContigPlan& p, int merge_mode) { return p.cluster || merge_mode == 2; }
 
 gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* m_out,
                        float* l_out, float* op_out, int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_len,
@@ -494,7 +542,7 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
   a.s_begin = s_begin;
   a.s_len = s_len;
   a.n_splits = p.n_splits;
-  a.merge_in_kernel = p.cluster || merge_in_kernel(p, D, opt.merge_mode) ? 1 : 0;
+  a.merge_in_kernel = merge_in_kernel(p, opt.merge_mode) ? 1 : 0;
   a.causal = opt.causal ? 1 : 0;
   a.scale_log2 = scale * kLog2e;
   a.timeout_ns = opt.timeout_us ? (uint64_t)opt.timeout_us * 1000ull : kDefaultTimeoutNs;
@@ -708,7 +756,7 @@ gqa_status gqa_decode_plan(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, 
     if (s != GQA_OK) return s;
     if (n_splits) *n_splits = p.n_splits;
     if (mma_path) *mma_path = p.tc ? 2 : 1;
-    if (launches) *launches = (p.n_splits > 1 && !merge_in_kernel(p, d_head, o.merge_mode)) ? 2 : 1;
+    if (launches) *launches = (p.n_splits > 1 && !merge_in_kernel(p, o.merge_mode)) ? 2 : 1;
     return GQA_OK;
   } catch (...) {
     return GQA_ERR_CUDA;

@@ -68,16 +68,19 @@ typedef enum {
 /* Optional knobs for tests and benchmarks (NULL = defaults everywhere). */
 typedef struct {
   int n_splits;          /* contiguous calls: splits per (sequence, KV head); 0 = heuristic */
-  int merge_mode;        /* how a unit's splits are folded: 0 = automatic (the last-arriving CTA of the
-                            unit in the same kernel; on the mma.sync kernel a cluster (3) instead where
-                            the heuristic wants more than 16 splits over at most 16 x 8 tiles (short
-                            sweeps); the separate merge kernel above 32 splits or, for the tcgen05
-                            kernel, when a unit's partials exceed 256 KB), 1 = separate merge kernel,
-                            2 = last-arriving CTA, 3 = the unit's splits (at most 16; more are
-                            capped) run as one thread-block cluster and fold their partials through
-                            distributed shared memory, no workspace partials and one launch
-                            (mma.sync kernel only: the automatic mma_path takes it for up to 64
-                            rows; GQA_ERR_UNSUPPORTED on the tcgen05 kernel) */
+  int merge_mode;        /* how a unit's splits are folded.  0 = automatic: on the mma.sync kernel
+                            a cluster (3) for 2 to 16 splits where the cluster variant keeps the
+                            plain kernel's ring depth (not at d_head 128 with more than 32 rows)
+                            and adds no wave of CTAs, and one cluster of 16 where the heuristic
+                            wants more than 16 splits over at most 16 x 8 tiles (short sweeps);
+                            otherwise, and always after the tcgen05 kernel, the separate merge
+                            kernel.  1 = separate merge kernel.  2 = the last-arriving CTA of the
+                            unit folds the splits in the same kernel (only on request).  3 = the
+                            unit's splits (at most 16; more are capped) run as one thread-block
+                            cluster and fold their partials through distributed shared memory, no
+                            workspace partials and one launch (mma.sync kernel only: the automatic
+                            mma_path takes it for up to 64 rows; GQA_ERR_UNSUPPORTED on the tcgen05
+                            kernel) */
   uint32_t timeout_us;   /* limit of every device wait; 0 = 1,000,000 us */
   int test_stall_cta;    /* test hook, -1 = off.  Contiguous calls: linear id (x + X*(y + Y*z)) of
                             one CTA whose producer never loads its second tile; paged calls: the

@@ -139,5 +139,19 @@ def test_automatic_choice_takes_the_cluster_for_short_sweeps(gqa):
     # a longer sweep keeps the heuristic's splits (and its bandwidth)
     n, path, launches = gqa.gqa_decode_plan(1, 1, 65536, 8, 2, 64)
     assert n > 16 and launches == 2
-    # many units: the in-kernel last-CTA merge, no cluster
-    assert gqa.gqa_decode_plan(8, 1, 32768, 32, 8, 128)[2] == 1
+    # many units, 3 splits each: one cluster per unit (one launch)
+    assert gqa.gqa_decode_plan(8, 1, 32768, 32, 8, 128) == (3, 1, 1)
+
+
+def test_automatic_choice_between_cluster_and_merge_kernel(gqa):
+    """merge_mode 0 on the mma.sync kernel: 2 to 16 splits fold in a cluster (one launch), more in the
+    merge kernel (two); at d_head 128 with 64 rows, where the cluster variant's receiving area costs a
+    ring stage, the merge kernel too.  Each choice matches the oracle."""
+    for n, launches in [(2, 1), (5, 1), (16, 1), (17, 2), (24, 2)]:
+        assert gqa.gqa_decode_plan(2, 1, 20000, 32, 8, 128, n_splits=n) == (n, 1, launches)
+    assert gqa.gqa_decode_plan(1, 1, 20000, 32, 8, 64, n_splits=7) == (7, 1, 1)
+    assert gqa.gqa_decode_plan(1, 16, 20000, 32, 8, 128, n_splits=3, mma_path=1) == (3, 1, 2)   # 64 rows
+    assert gqa.gqa_decode_plan(1, 16, 20000, 32, 8, 64, n_splits=3, mma_path=1) == (3, 1, 1)
+    for (T, D, n) in [(1, 128, 5), (1, 128, 24), (16, 128, 3), (16, 64, 3), (2, 64, 11)]:
+        y = gi.make_contiguous(gi.custom(2, T, 3000, 32, 8, D, 7900 + T + D + n))
+        assert_close(run_contig(gqa, y, n_splits=n, mma_path=1), ref_contig(y), f"automatic T={T} D={D} n={n}")

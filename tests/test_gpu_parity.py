@@ -131,8 +131,9 @@ def test_workload_paged(gqa, hg):
 
 # ---------------------------------------------------------------- splits, shapes, edges
 @pytest.mark.parametrize("n_splits", [1, 2, 7, 37, 79])
-@pytest.mark.parametrize("merge_mode", [0, 1])
+@pytest.mark.parametrize("merge_mode", [0, 1, 2])
 def test_split_sweep(gqa, n_splits, merge_mode):
+    # automatic (a cluster up to 16 splits, else the merge kernel), the merge kernel, the last CTA's fold
     x = gi.make_contiguous(gi.custom(2, 1, 5000, 8, 2, 128, 101))
     ref = ref_contig(x)
     assert_close(run_contig(gqa, x, n_splits=n_splits, merge_mode=merge_mode), ref,
@@ -159,6 +160,9 @@ def test_row_classes(gqa, hq, hkv, T, D, path):
     ref = ref_contig(x)
     assert_close(run_contig(gqa, x, mma_path=path), ref, f"hq={hq} hkv={hkv} T={T} D={D} path={path}")
     assert_close(run_contig(gqa, x, n_splits=3, mma_path=path), ref, f"hq={hq} hkv={hkv} T={T} D={D} 3 splits")
+    if path == 1:   # the last CTA's fold, which the automatic choice leaves to explicit requests
+        assert_close(run_contig(gqa, x, n_splits=3, merge_mode=2, mma_path=1), ref,
+                     f"hq={hq} hkv={hkv} T={T} D={D} 3 splits, last-CTA fold")
 
 
 def test_constant_scores_and_shift(gqa):
@@ -296,16 +300,17 @@ def test_paged_bad_block_is_reported(gqa):
 
 def test_timeout_is_reported_not_hung(gqa):
     """A CTA whose producer withholds a tile: its bounded waits give up after ~20 ms and the
-    status word says so; the context stays usable."""
+    status word says so; the context stays usable (the last-CTA fold; the cluster variant and the
+    merge kernel have their own such tests)."""
     x = gi.make_contiguous(gi.custom(1, 1, 8192, 8, 2, 128, 1001))
     q, k, v = cuda(x["q"]), cuda(x["k"]), cuda(x["v"])
     nbytes = gqa.gqa_decode_workspace_size(1, 1, 8192, 8, 2, 128, 4)
     ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
-    gqa.gqa_decode(q, k, v, 8, 2, x["scale"], n_splits=4, workspace_tensor=ws, timeout_us=20000,
+    gqa.gqa_decode(q, k, v, 8, 2, x["scale"], n_splits=4, merge_mode=2, workspace_tensor=ws, timeout_us=20000,
                    test_stall_cta=1)
     assert gqa.gqa_workspace_check(ws) == gqa.GQA_ERR_TIMEOUT
     gqa.gqa_workspace_init(ws)
-    o = gqa.gqa_decode(q, k, v, 8, 2, x["scale"], n_splits=4, workspace_tensor=ws)
+    o = gqa.gqa_decode(q, k, v, 8, 2, x["scale"], n_splits=4, merge_mode=2, workspace_tensor=ws)
     assert gqa.gqa_workspace_check(ws) == gqa.GQA_OK
     assert_close(o, ref_contig(x), "after a timeout")
 

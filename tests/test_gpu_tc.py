@@ -72,6 +72,8 @@ SHAPES = [
     (1, 16, 64, 64, 8, 128, 0, 0),
     (1, 16, 65, 64, 8, 128, 1, 0),
     (2, 8, 9000, 128, 8, 64, 5, 0),
+    (3, 5, 2000, 16, 1, 128, 3, 2),
+    (2, 8, 9000, 128, 8, 64, 5, 2),
 ]
 
 
@@ -160,17 +162,20 @@ def test_tc_bf16(gqa, causal):
     assert_close(o, ref(x, causal=causal, elem="bf16"), f"tc bf16 causal={causal}", rel_tol=8e-3, rel_l2=1e-2)
 
 
-def test_tc_timeout_is_reported_not_hung(gqa):
+@pytest.mark.parametrize("merge_mode", [0, 2])
+def test_tc_timeout_is_reported_not_hung(gqa, merge_mode):
     """A CTA whose producer withholds a tile: every wait of the tcgen05 kernel gives up after
-    ~20 ms, the tensor memory is released, the status word says so and the context stays usable."""
+    ~20 ms, the tensor memory is released, the status word says so and the context stays usable
+    (splits folded by the merge kernel, or by the unit's last CTA)."""
     x = gi.make_contiguous(gi.custom(1, 16, 8192, 64, 8, 128, 2500))
     q, k, v = dev(x["q"]), dev(x["k"]), dev(x["v"])
     nbytes = gqa.gqa_decode_workspace_size(1, 16, 8192, 64, 8, 128, 4)
     ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
-    gqa.gqa_decode(q, k, v, 64, 8, x["scale"], n_splits=4, workspace_tensor=ws, timeout_us=20000, test_stall_cta=9)
+    gqa.gqa_decode(q, k, v, 64, 8, x["scale"], n_splits=4, merge_mode=merge_mode, workspace_tensor=ws,
+                   timeout_us=20000, test_stall_cta=9)
     assert gqa.gqa_workspace_check(ws) == gqa.GQA_ERR_TIMEOUT
     gqa.gqa_workspace_init(ws)
-    o = gqa.gqa_decode(q, k, v, 64, 8, x["scale"], n_splits=4, workspace_tensor=ws)
+    o = gqa.gqa_decode(q, k, v, 64, 8, x["scale"], n_splits=4, merge_mode=merge_mode, workspace_tensor=ws)
     assert gqa.gqa_workspace_check(ws) == gqa.GQA_OK
     assert_close(o, ref(x), "after a timeout")
 
@@ -186,13 +191,14 @@ def test_plan_query(gqa):
     """gqa_decode_plan reports the kernel path, the split count and the launches of a call."""
     w = gi.WORKLOADS["verify16"]
     n, path, launches = gqa.gqa_decode_plan(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head)
-    assert path == 2 and n > 1 and launches == 2          # 128 rows: tcgen05, partials too big to fold in-kernel
+    assert path == 2 and n > 1 and launches == 2          # tcgen05: the splits fold in the merge kernel
     assert gqa.gqa_decode_plan(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head, merge_mode=2)[2] == 1
     w = gi.WORKLOADS["ragged"]                          # 32 rows: tcgen05 automatically
     n, path, launches = gqa.gqa_decode_plan(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head)
     assert path == 2
-    assert gqa.gqa_decode_plan(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head, mma_path=1) == (n, 1, 1)
-    w = gi.WORKLOADS["llama8b"]                         # 4 rows: mma.sync, in-kernel merge
+    # the same split count on the mma.sync kernel, more than a cluster holds: the merge kernel
+    assert n > 16 and gqa.gqa_decode_plan(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head, mma_path=1) == (n, 1, 2)
+    w = gi.WORKLOADS["llama8b"]                         # 4 rows: mma.sync, 3 splits folded in a cluster
     n, path, launches = gqa.gqa_decode_plan(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head)
     assert path == 1 and launches == 1
     assert gqa.gqa_decode_plan(1, 1, 100, 8, 2, 64, n_splits=1) == (1, 1, 1)
