@@ -83,8 +83,9 @@ bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 struct DevState {
   bool ready = false;
   int sms = 0;
-  int smem_sm = 0;             // shared memory per SM and reserved per CTA (bytes)
-  int smem_reserved = 0;
+  int clusters[2][4][kMaxClusterSplits + 1] = {};   // [d index][row class][n]: clusters of n CTAs of the
+                                                   // split kernel's cluster variant held at once
+                                                   // (0 = not asked, -1 = none)
   int occ[2][4][12][2] = {};   // [d index][row class][kernel: see kernel_slot][bf16] resident CTAs
                                // per SM (cluster variant: clusters of kMaxClusterSplits the GPU holds),
                                // 0 = not prepared
@@ -153,20 +154,16 @@ int kernel_slot(int kind) {
   return (kind < 200 ? 2 : 7) + hg_slot;   // paged: 2-4, vLLM layout: 7-9
 }
 
-// The split kernel's shared-memory layouts per (d index, row class): the plain kernel's and the
-// cluster variant's dynamic shared memory, and whether the variant keeps the plain ring depth
-struct SplitLayout {
-  int smem_plain, smem_cluster;
-  bool same_ring;
-};
+// Whether the split kernel's cluster variant keeps the plain kernel's ring depth (its receiving area
+// fits beside the ring), per (d index, row class)
 template <int D, int CLS>
-constexpr SplitLayout split_layout() {
-  return {Inst<D, CLS, false, false, false>::SMEM, Inst<D, CLS, false, false, true>::SMEM,
-          Inst<D, CLS, false, false, false>::STAGES == Inst<D, CLS, false, false, true>::STAGES};
+constexpr bool cluster_same_ring() {
+  return Inst<D, CLS, false, false, false>::STAGES == Inst<D, CLS, false, false, true>::STAGES;
 }
-constexpr SplitLayout kSplitLayout[2][4] = {
-    {split_layout<64, 0>(), split_layout<64, 1>(), split_layout<64, 2>(), split_layout<64, 3>()},
-    {split_layout<128, 0>(), split_layout<128, 1>(), split_layout<128, 2>(), split_layout<128, 3>()}};
+constexpr bool kClusterSameRing[2][4] = {
+    {cluster_same_ring<64, 0>(), cluster_same_ring<64, 1>(), cluster_same_ring<64, 2>(), cluster_same_ring<64, 3>()},
+    {cluster_same_ring<128, 0>(), cluster_same_ring<128, 1>(), cluster_same_ring<128, 2>(),
+     cluster_same_ring<128, 3>()}};
 
 // SM count and resident CTAs per SM of one kernel configuration on the current device
 gqa_status device_info(int di, int cls, int kind, int bf16, int* sms, int* occ) {
@@ -175,10 +172,7 @@ gqa_status device_info(int di, int cls, int kind, int bf16, int* sms, int* occ) 
   std::lock_guard<std::mutex> lock(g_mu);
   DevState& st = g_dev[dev];
   if (!st.ready) {
-    if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&st.smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&st.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
-      return GQA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return GQA_ERR_CUDA;
     if (g_encode == nullptr) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -203,14 +197,27 @@ gqa_status device_info(int di, int cls, int kind, int bf16, int* sms, int* occ) 
   return GQA_OK;
 }
 
-// CTAs per SM that `smem` bytes of dynamic shared memory allow on the current device (0 before
-// device_info has read its attributes)
-int smem_residency(int smem) {
+typedef cudaError_t (*ClustersFn)(int, int, int, int*);
+const ClustersFn kClusters[2][2] = {{cluster_d64_clusters, cluster_d64_bf16_clusters},
+                                    {cluster_d128_clusters, cluster_d128_bf16_clusters}};
+
+// Clusters of n CTAs of the split kernel's cluster variant (d index di, row class cls) the current
+// device holds at once -- a cluster's CTAs are placed together, within one GPC, so this can be
+// fewer than the resident CTAs divided by n; 0 when none fits or the query failed
+int cluster_capacity(int di, int cls, int n) {
+  if (n < 2 || n > kMaxClusterSplits) return 0;
+  int sms = 0, c16 = 0;
+  if (device_info(di, cls, 4, 0, &sms, &c16) != GQA_OK) return 0;   // prepares the variant's attributes
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   std::lock_guard<std::mutex> lock(g_mu);
-  const DevState& st = g_dev[dev];
-  return st.ready ? st.smem_sm / (smem + st.smem_reserved) : 0;
+  int& c = g_dev[dev].clusters[di][cls][n];
+  if (c == 0) {
+    int v = 0;
+    if (kClusters[di][0](cls, 0, n, &v) != cudaSuccess) v = 0;
+    c = v > 0 ? v : -1;
+  }
+  return c > 0 ? c : 0;
 }
 
 // 3-D map over a (rows, cols) f16 / bf16 matrix seen as (64-column planes, rows, 64 columns):
@@ -395,20 +402,18 @@ gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_
     p->cluster = p->n_splits > 1;
   } else if (merge_mode == 0 && !p->tc && need_device && p->n_splits > 1) {
     // automatic, mma.sync kernel: 2 to kMaxClusterSplits splits fold in one cluster where the
-    // variant keeps the plain kernel's ring depth and does not add a wave of CTAs (its resident CTAs
-    // per SM are the plain kernel's, for which the split count was chosen, or the grid fits in one
-    // wave at its own); a short sweep asking for more splits runs as one cluster of
-    // kMaxClusterSplits; anything else goes to the merge kernel (merge_in_kernel)
-    const SplitLayout& L = kSplitLayout[p->di][p->cls];
+    // variant keeps the plain kernel's ring depth and every unit's cluster is resident at once
+    // (one wave; a cluster variant with one CTA per SM holding clusters of 9, 16 units took 996 us
+    // where the plain kernel takes 589, its clusters in two waves); a short sweep asking for more
+    // splits runs as one cluster of kMaxClusterSplits; anything else goes to the merge kernel
+    // (merge_in_kernel)
     const bool short_sweep = forced_splits == 0 && p->n_splits > kMaxClusterSplits &&
                              p->tiles <= (int64_t)kMaxClusterSplits * kClusterMaxTilesPerSplit;
-    const bool holds = p->n_splits <= kMaxClusterSplits && L.same_ring;
-    int sms = 0, clusters = 0;   // only where a cluster of kMaxClusterSplits can be scheduled
-    if ((short_sweep || holds) && device_info(p->di, p->cls, 4, 0, &sms, &clusters) == GQA_OK && clusters > 0) {
-      const int res = smem_residency(L.smem_cluster);
-      const bool one_wave = p->units * p->n_splits <= (int64_t)sms * res;
-      if (short_sweep || (res > 0 && (res >= smem_residency(L.smem_plain) || one_wave))) {
-        if (short_sweep) p->n_splits = kMaxClusterSplits;
+    const bool holds = p->n_splits <= kMaxClusterSplits && kClusterSameRing[p->di][p->cls];
+    if (short_sweep || holds) {
+      const int n = short_sweep ? kMaxClusterSplits : p->n_splits;
+      if (p->units <= (int64_t)cluster_capacity(p->di, p->cls, n)) {
+        p->n_splits = n;
         p->cluster = true;
       }
     }

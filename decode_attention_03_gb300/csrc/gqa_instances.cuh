@@ -86,6 +86,20 @@ struct Inst {
       return cudaOccupancyMaxActiveClusters(occupancy, fn, &cfg);
     }
   }
+  // cluster variant: how many clusters of n CTAs (the n splits of a unit) the GPU holds at once,
+  // after prepare() has set the kernel's attributes
+  static cudaError_t max_clusters(int n, int* count) {
+    if constexpr (!CLUSTER) {
+      return cudaErrorInvalidValue;
+    } else {
+      if (n < 2 || n > kMaxClusterSplits) return cudaErrorInvalidValue;
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      cluster_config(cfg, attr, dim3(1, (unsigned)n, 1), nullptr);
+      return cudaOccupancyMaxActiveClusters(count, gqa_split_kernel<D, NT, WN, STAGES, SUB, CAUSAL, BF16, CLUSTER>,
+                                            &cfg);
+    }
+  }
   static void cluster_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[1], dim3 grid, cudaStream_t st) {
     cfg.gridDim = grid;
     cfg.blockDim = dim3(C::THREADS, 1, 1);
@@ -149,6 +163,9 @@ struct PagedInst {
   cudaError_t NAME##_prepare(int cls, int variant, int* occupancy) {                             \
     GQA_CONTIG_CASES(D, BF, CL, prepare(occupancy))                                              \
   }                                                                                              \
+  cudaError_t NAME##_clusters(int cls, int variant, int n, int* count) {                         \
+    GQA_CONTIG_CASES(D, BF, CL, max_clusters(n, count))                                          \
+  }                                                                                              \
   cudaError_t NAME##_launch(int cls, int variant, dim3 grid, cudaStream_t st, const CUtensorMap& tk, \
                             const CUtensorMap& tv, const DecodeArgs& a) {                        \
     GQA_CONTIG_CASES(D, BF, CL, launch(grid, st, tk, tv, a))                                     \
@@ -184,6 +201,11 @@ GQA_DECLARE_UNIT(cluster_d64)
 GQA_DECLARE_UNIT(cluster_d128)
 GQA_DECLARE_UNIT(cluster_d64_bf16)
 GQA_DECLARE_UNIT(cluster_d128_bf16)
+// the cluster units also answer how many clusters of n CTAs the GPU holds at once
+cudaError_t cluster_d64_clusters(int cls, int variant, int n, int* count);
+cudaError_t cluster_d128_clusters(int cls, int variant, int n, int* count);
+cudaError_t cluster_d64_bf16_clusters(int cls, int variant, int n, int* count);
+cudaError_t cluster_d128_bf16_clusters(int cls, int variant, int n, int* count);
 GQA_DECLARE_UNIT(paged_d64_bf16)
 GQA_DECLARE_UNIT(paged_d128_bf16)
 GQA_DECLARE_UNIT(paged_vllm_d64)

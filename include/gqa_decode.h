@@ -71,8 +71,10 @@ typedef struct {
   int merge_mode;        /* how a unit's splits are folded.  0 = automatic: on the mma.sync kernel
                             a cluster (3) for 2 to 16 splits where the cluster variant keeps the
                             plain kernel's ring depth (not at d_head 128 with more than 32 rows)
-                            and adds no wave of CTAs, and one cluster of 16 where the heuristic
-                            wants more than 16 splits over at most 16 x 8 tiles (short sweeps);
+                            and the GPU holds every unit's cluster at once (one wave; the
+                            runtime's count of co-resident clusters of that size), and one
+                            cluster of 16 where the heuristic wants more than 16 splits over at
+                            most 16 x 8 tiles (short sweeps);
                             otherwise, and always after the tcgen05 kernel, the separate merge
                             kernel.  1 = separate merge kernel.  2 = the last-arriving CTA of the
                             unit folds the splits in the same kernel (only on request).  3 = the

@@ -147,11 +147,15 @@ def test_automatic_choice_between_cluster_and_merge_kernel(gqa):
     """merge_mode 0 on the mma.sync kernel: 2 to 16 splits fold in a cluster (one launch), more in the
     merge kernel (two); at d_head 128 with 64 rows, where the cluster variant's receiving area costs a
     ring stage, the merge kernel too.  Each choice matches the oracle."""
-    for n, launches in [(2, 1), (5, 1), (16, 1), (17, 2), (24, 2)]:
-        assert gqa.gqa_decode_plan(2, 1, 20000, 32, 8, 128, n_splits=n) == (n, 1, launches)
+    for n, launches in [(2, 1), (5, 1), (16, 1), (17, 2), (24, 2)]:   # 2 units: their clusters fit at once
+        assert gqa.gqa_decode_plan(1, 1, 20000, 8, 2, 128, n_splits=n) == (n, 1, launches)
     assert gqa.gqa_decode_plan(1, 1, 20000, 32, 8, 64, n_splits=7) == (7, 1, 1)
     assert gqa.gqa_decode_plan(1, 16, 20000, 32, 8, 128, n_splits=3, mma_path=1) == (3, 1, 2)   # 64 rows
     assert gqa.gqa_decode_plan(1, 16, 20000, 32, 8, 64, n_splits=3, mma_path=1) == (3, 1, 1)
+    # only while every unit's cluster is resident at once: at d_head 64 with 64 rows the variant
+    # holds one CTA per SM, so 64 units of 2-CTA clusters fit in one wave and 160 do not
+    assert gqa.gqa_decode_plan(8, 16, 4096, 32, 8, 64, n_splits=2, mma_path=1) == (2, 1, 1)
+    assert gqa.gqa_decode_plan(20, 16, 4096, 32, 8, 64, n_splits=2, mma_path=1) == (2, 1, 2)
     for (T, D, n) in [(1, 128, 5), (1, 128, 24), (16, 128, 3), (16, 64, 3), (2, 64, 11)]:
         y = gi.make_contiguous(gi.custom(2, T, 3000, 32, 8, D, 7900 + T + D + n))
         assert_close(run_contig(gqa, y, n_splits=n, mma_path=1), ref_contig(y), f"automatic T={T} D={D} n={n}")
