@@ -203,10 +203,10 @@ def gqa_paged_plan(num_seqs, h_q, h_kv, d_head, max_seq_len, partition_size=0, *
     return part.value, hg.value, launches.value
 
 
-def gqa_decode_plan(batch, T_q, S_kv, h_q, h_kv, d_head, *, n_splits=0, merge_mode=0, mma_path=0):
+def gqa_decode_plan(batch, T_q, S_kv, h_q, h_kv, d_head, *, n_splits=0, merge_mode=0, mma_path=0, causal=False):
     """(n_splits, mma_path, launches) of a gqa_decode call with these shapes and options on the current
     device: mma_path 1 = mma.sync split kernel, 2 = tcgen05 kernel; launches 2 with the merge kernel."""
-    opt = _opts(n_splits, merge_mode, mma_path=mma_path)
+    opt = _opts(n_splits, merge_mode, causal=causal, mma_path=mma_path)
     n, path, launches = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
     st = lib.gqa_decode_plan(batch, T_q, S_kv, h_q, h_kv, d_head, ctypes.byref(opt), ctypes.byref(n),
                              ctypes.byref(path), ctypes.byref(launches))

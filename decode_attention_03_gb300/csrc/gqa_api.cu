@@ -53,6 +53,10 @@ constexpr int kTcMinRows = 16;              // automatic MMA path: tcgen05 from 
 // L2: there the heuristic's 95 splits stream faster).  Clusters of 12 / 8 / 4 at 4096 keys: 11.6 /
 // 12.2 / 14.6.  Longer sweeps keep the splits, and the bandwidth, of the heuristic.
 constexpr int kClusterMaxTilesPerSplit = 8;
+// The deep-ring variant of the split kernel (kDeepRingBytes, one CTA per SM) needs at least this many
+// 64-key tiles per split (measured: 54 tiles per split 1.6 % faster than the heuristic's grid, 27
+// tiles 12 % slower)
+constexpr int64_t kDeepMinTilesPerSplit = 48;
 // Paged partitions chosen automatically (partition_size 0).  Page "muh_kernel_map.py" picks v1 --
 // one pass over each whole sequence, no merge pass -- for seq_len <= 8192 and v2 with 512-token
 // partitions above.  On GB300 the persistent kernel with 512-token partitions (and the merge pass
@@ -86,7 +90,7 @@ struct DevState {
   int clusters[2][4][kMaxClusterSplits + 1] = {};   // [d index][row class][n]: clusters of n CTAs of the
                                                    // split kernel's cluster variant held at once
                                                    // (0 = not asked, -1 = none)
-  int occ[2][4][12][2] = {};   // [d index][row class][kernel: see kernel_slot][bf16] resident CTAs
+  int occ[2][4][13][2] = {};   // [d index][row class][kernel: see kernel_slot][bf16] resident CTAs
                                // per SM (cluster variant: clusters of kMaxClusterSplits the GPU holds),
                                // 0 = not prepared
 };
@@ -100,9 +104,10 @@ EncodeTiledFn g_encode = nullptr;
 
 // Kernel selector `kind`: 0 contiguous, 1 contiguous with the causal tail, 2 / 3 the same two
 // on the tcgen05 kernel (row class 0 stands for its single configuration), 4 / 5 the same two as
-// the cluster variant of the split kernel (a unit's splits merged in one cluster), and for the paged
-// kernel 100 + its head group (101, 102, 104) over the row-layout pool, 200 + its head group over
-// the vLLM cache layout.
+// the cluster variant of the split kernel (a unit's splits merged in one cluster), 6 the split
+// kernel's deep-ring variant (no causal tail, row class 0, d_head 128), and for the paged kernel
+// 100 + its head group (101, 102, 104) over the row-layout pool, 200 + its head group over the
+// vLLM cache layout.
 typedef cudaError_t (*PrepareFn)(int, int, int*);
 typedef cudaError_t (*LaunchFn)(int, int, dim3, cudaStream_t, const CUtensorMap&, const CUtensorMap&,
                                 const DecodeArgs&);
@@ -133,6 +138,7 @@ const TcLaunchFn kTcLaunch[2] = {tc_d64_launch, tc_d128_launch};
 
 cudaError_t prepare_unit(int di, int cls, int kind, int bf16, int* occ) {
   if (kind == 2 || kind == 3) return kTcPrepare[di](kind - 2, bf16, occ);
+  if (kind == 6) return kPrepare[0][di][bf16](0, 2, occ);
   if (kind == 4 || kind == 5) return kClusterPrepare[di][bf16](cls, kind - 4, occ);
   const int family = kind / 100;   // 0 contiguous, 1 paged, 2 paged over the vLLM layout
   return kPrepare[family][di][bf16](cls, kind - 100 * family, occ);
@@ -141,6 +147,7 @@ cudaError_t prepare_unit(int di, int cls, int kind, int bf16, int* occ) {
 cudaError_t launch_unit(int di, int cls, int kind, int bf16, dim3 grid, cudaStream_t st, const CUtensorMap& tk,
                         const CUtensorMap& tv, const DecodeArgs& a) {
   if (kind == 2 || kind == 3) return kTcLaunch[di](kind - 2, bf16, grid, st, tk, tv, a);
+  if (kind == 6) return kLaunch[0][di][bf16](0, 2, grid, st, tk, tv, a);
   if (kind == 4 || kind == 5) return kClusterLaunch[di][bf16](cls, kind - 4, grid, st, tk, tv, a);
   const int family = kind / 100;   // 0 contiguous, 1 paged, 2 paged over the vLLM layout
   return kLaunch[family][di][bf16](cls, kind - 100 * family, grid, st, tk, tv, a);
@@ -149,7 +156,7 @@ cudaError_t launch_unit(int di, int cls, int kind, int bf16, dim3 grid, cudaStre
 int kernel_slot(int kind) {
   if (kind < 2) return kind;
   if (kind < 4) return kind + 3;     // tcgen05: 5, 6
-  if (kind < 100) return kind + 6;   // cluster variant: 10, 11
+  if (kind < 100) return kind + 6;   // cluster variant: 10, 11; deep ring: 12
   const int hg_slot = (kind % 100) == 1 ? 0 : ((kind % 100) == 2 ? 1 : 2);
   return (kind < 200 ? 2 : 7) + hg_slot;   // paged: 2-4, vLLM layout: 7-9
 }
@@ -337,6 +344,7 @@ struct ContigPlan {
   int di, cls, rows, n_splits;
   bool tc;                     // the tcgen05 kernel (else the mma.sync split kernel)
   bool cluster;                // the split kernel's cluster variant (merge_mode 3)
+  bool deep;                   // the split kernel's deep-ring variant (kind 6)
   int64_t units, tiles, R;
   Layout lay;
 };
@@ -344,7 +352,8 @@ struct ContigPlan {
 // validation shared by the size query and the calls
 // mma_path: 0 auto (tcgen05 above 64 query rows per KV head), 1 mma.sync, 2 tcgen05
 gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_len, int h_q, int h_kv, int D,
-                       int forced_splits, bool need_device, ContigPlan* p, int mma_path = 0, int merge_mode = 0) {
+                       int forced_splits, bool need_device, ContigPlan* p, int mma_path = 0, int merge_mode = 0,
+                       bool causal = false) {
   if (B < 0 || T_q < 1 || h_q < 1 || h_kv < 1 || S_kv < 0 || s_begin < 0 || s_len < 0) return GQA_ERR_INVALID_ARG;
   if (s_begin + s_len > S_kv) return GQA_ERR_INVALID_ARG;
   if (h_q % h_kv != 0 || forced_splits < 0) return GQA_ERR_INVALID_ARG;
@@ -415,6 +424,22 @@ gqa_status plan_contig(int B, int T_q, int64_t S_kv, int64_t s_begin, int64_t s_
       if (p->units <= (int64_t)cluster_capacity(p->di, p->cls, n)) {
         p->n_splits = n;
         p->cluster = true;
+      }
+    }
+  }
+  // automatic, mma.sync kernel without the causal tail, up to 8 rows at d_head 128: where the units
+  // divide the SMs into more splits than a cluster holds, each long enough, one CTA per SM with the
+  // deep ring (kDeepRingBytes) instead of the heuristic's splits at two CTAs on some SMs
+  p->deep = false;
+  if (merge_mode == 0 && forced_splits == 0 && need_device && !p->tc && !p->cluster && !causal && D == 128 &&
+      p->cls == 0 && p->units > 0) {
+    int sms = 0, occ = 0;
+    if (device_info(p->di, 0, 6, 0, &sms, &occ) == GQA_OK && occ == 1 && sms % p->units == 0) {
+      const int64_t n = sms / p->units;
+      // (the workspace above holds the partials of ws_splits splits)
+      if (n > kMaxClusterSplits && n <= ws_splits && p->tiles >= n * kDeepMinTilesPerSplit) {
+        p->n_splits = (int)n;
+        p->deep = true;
       }
     }
   }
@@ -506,11 +531,12 @@ gqa_status decode_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
   } else if (!aligned16(o)) {
     return GQA_ERR_INVALID_ARG;
   }
-  s = plan_contig(B, T_q, S_kv, s_begin, s_len, h_q, h_kv, D, opt.n_splits, true, &p, opt.mma_path, opt.merge_mode);
+  s = plan_contig(B, T_q, S_kv, s_begin, s_len, h_q, h_kv, D, opt.n_splits, true, &p, opt.mma_path, opt.merge_mode,
+                  opt.causal != 0);
   if (s != GQA_OK) return s;
   if (ws_bytes < p.lay.total) return GQA_ERR_WORKSPACE;
   int sms = 0, occ = 0;
-  const int kind = (p.tc ? 2 : (p.cluster ? 4 : 0)) + (opt.causal ? 1 : 0);
+  const int kind = p.deep ? 6 : (p.tc ? 2 : (p.cluster ? 4 : 0)) + (opt.causal ? 1 : 0);
   const int bf16 = opt.bf16 ? 1 : 0;
   s = device_info(p.di, p.cls, kind, bf16, &sms, &occ);
   if (s != GQA_OK) return s;
@@ -757,7 +783,7 @@ gqa_status gqa_decode_plan(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, 
     if (S_kv < 1 || batch < 1 || o.merge_mode < 0 || o.merge_mode > 3) return GQA_ERR_INVALID_ARG;
     ContigPlan p;
     gqa_status s = plan_contig(batch, T_q, S_kv, 0, S_kv, h_q, h_kv, d_head, o.n_splits, true, &p, o.mma_path,
-                               o.merge_mode);
+                               o.merge_mode, o.causal != 0);
     if (s != GQA_OK) return s;
     if (n_splits) *n_splits = p.n_splits;
     if (mma_path) *mma_path = p.tc ? 2 : 1;

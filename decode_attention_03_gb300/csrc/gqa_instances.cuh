@@ -58,12 +58,23 @@ constexpr int split_stages() {
   return st;
 }
 
-template <int D, int CLS, bool CAUSAL, bool BF16, bool CLUSTER = false>
+// The deep-ring variant of the split kernel: a ring of kDeepRingBytes (4 stages of 32 KB at d_head
+// 128), one CTA per SM, for grids that give every SM exactly one CTA.  Measured on GB300 (us per
+// step; the heuristic's splits at two CTAs per SM on some SMs / one per SM with the deep ring),
+// d_head 128, 4 rows per KV head: 8 KV heads, 2^20 keys 582.5 / 576.7-578.5 (19 splits; 3 and 5
+// stages there 604.0 / 610.0); 2^17 keys 80.0 / 79.1; 2^16 keys 43.7 / 43.0; 2^15 keys 24.2 /
+// 27.1 (27 tiles per split: too short); one KV head, 2^20 keys 87.1 / 86.0; two KV heads 154.0 /
+// 154.3.
+constexpr int kDeepRingBytes = 128 * 1024;
+
+template <int D, int CLS, bool CAUSAL, bool BF16, bool CLUSTER = false, bool DEEP = false>
 struct Inst {
+  static_assert(!DEEP || (!CLUSTER && !CAUSAL), "the deep ring is a variant of the plain kernel");
   static constexpr int NT = cls_nt(CLS);
   static constexpr int WN = cls_wn(CLS);
   static constexpr int SUB = split_sub(D);
-  static constexpr int STAGES = split_stages<D, NT, WN, SUB, CLUSTER>();   // ring stages of SUB tiles
+  static constexpr int STAGES = DEEP ? kDeepRingBytes / (SUB * Cfg<D, NT, WN, 1>::STAGE_BYTES)
+                                     : split_stages<D, NT, WN, SUB, CLUSTER>();   // ring stages of SUB tiles
   using C = Cfg<D, NT, WN, STAGES * SUB>;
   static constexpr int SMEM = split_smem_bytes<D, NT, WN>(STAGES * SUB, CLUSTER);
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -144,14 +155,29 @@ struct PagedInst {
 };
 
 // One unit (translation unit) per (kernel kind, d_head, element type).  Contiguous units:
-// cls in [0, 4), variant = causal (0 / 1).  Paged units (row-layout pool or vLLM cache
-// layout): cls in [0, 4), variant = head group in {1, 2, 4} (2 and 4 only for cls 0 and 1).
+// cls in [0, 4), variant = causal (0 / 1), or 2 = the deep-ring variant (plain units, d_head 128,
+// cls 0).  Paged units (row-layout pool or vLLM cache layout): cls in [0, 4), variant = head
+// group in {1, 2, 4} (2 and 4 only for cls 0 and 1).
 #define GQA_DECLARE_UNIT(NAME)                                                                   \
   cudaError_t NAME##_prepare(int cls, int variant, int* occupancy);                              \
   cudaError_t NAME##_launch(int cls, int variant, dim3 grid, cudaStream_t st, const CUtensorMap& tk, \
                             const CUtensorMap& tv, const DecodeArgs& a);
 
+// variant 2 of a contiguous unit: the deep-ring variant, row class 0 of the plain units at d_head
+// 128 (elsewhere: invalid)
+template <int D, bool BF, bool CL>
+struct DeepCase {
+  static cudaError_t prepare(int*) { return cudaErrorInvalidValue; }
+  static cudaError_t max_clusters(int, int*) { return cudaErrorInvalidValue; }
+  static cudaError_t launch(dim3, cudaStream_t, const CUtensorMap&, const CUtensorMap&, const DecodeArgs&) {
+    return cudaErrorInvalidValue;
+  }
+};
+template <bool BF>
+struct DeepCase<128, BF, false> : Inst<128, 0, false, BF, false, true> {};
+
 #define GQA_CONTIG_CASES(D, BF, CL, CALL)                                                        \
+  if (variant == 2) return cls == 0 ? DeepCase<D, BF, CL>::CALL : cudaErrorInvalidValue;         \
   if (cls == 0) return variant ? Inst<D, 0, true, BF, CL>::CALL : Inst<D, 0, false, BF, CL>::CALL; \
   if (cls == 1) return variant ? Inst<D, 1, true, BF, CL>::CALL : Inst<D, 1, false, BF, CL>::CALL; \
   if (cls == 2) return variant ? Inst<D, 2, true, BF, CL>::CALL : Inst<D, 2, false, BF, CL>::CALL; \

@@ -3,9 +3,9 @@ computed global- and shared-memory offset of the kernels is range-checked on the
 failure would set GQA_ERR_BOUNDS in the status word instead of making the access.
 
 Run over the small ragged shapes -- key counts around the tile and block edges, every kernel
-(mma.sync split kernel with each merge, its cluster variant, the tcgen05 kernel, the paged kernel
-over both cache layouts, the merge kernels) -- each call must leave the status word clean and
-match the CPU float64 oracle at the parity tolerance.  Calls go through the C ABI of the checked
+(mma.sync split kernel with each merge, its cluster and deep-ring variants, the tcgen05 kernel,
+the paged kernel over both cache layouts, the merge kernels) -- each call must leave the status
+word clean and match the CPU float64 oracle at the parity tolerance.  Calls go through the C ABI of the checked
 library.
 """
 from __future__ import annotations
@@ -74,6 +74,19 @@ def test_checked_contiguous(chk, S, D):
     for opt in ({}, {"n_splits": 3, "merge_mode": 1}, {"n_splits": 5, "merge_mode": 2},
                 {"n_splits": 7, "merge_mode": 3}):
         assert_close(_decode(b, lib, x, **opt), ref, f"checked S={S} D={D} {opt}")
+
+
+def test_checked_deep_ring(chk):
+    """The split kernel's deep-ring variant (one CTA per SM), which the plan takes for 8 units where the
+    SMs divide into more than 16 splits of at least 48 tiles."""
+    b, lib = chk
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms % 8 or sms // 8 <= 16:
+        pytest.skip("no deep-ring grid for 8 units on this GPU")
+    S = (sms // 8) * 48 * 64 + 37
+    x = gi.make_contiguous(gi.custom(1, 1, S, 32, 8, 128, 9500))
+    ref = oracle.decode(x["q"], x["k"], x["v"], 32, 8, 128, x["scale"])
+    assert_close(_decode(b, lib, x), ref, "checked deep ring")
 
 
 @pytest.mark.parametrize("S", [1, 65, 513, 4097])
