@@ -176,6 +176,17 @@ gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = (uint32_t)flags[2];
+  // the first ring's worth of K and V boxes into L2 while the previous kernel in the stream may
+  // still run (a hint: the loads after the dependency wait read whatever it wrote)
+  if (warp == C::TMA_WARP && lane == 0) {
+    for (int it = 0; it < n_tiles && it < STAGES; ++it) {
+      const int64_t y = (int64_t)b * a.S_kv + key_begin + (int64_t)it * kTcKeys;
+      if (y < (int64_t)a.B * a.S_kv && g_kv < a.h_kv) {
+        ptx::tma_prefetch_3d(&tmK, 0, (int)y, g_kv * C::HALVES);
+        ptx::tma_prefetch_3d(&tmV, 0, (int)y, g_kv * C::HALVES);
+      }
+    }
+  }
   // launched as a programmatic dependent: the set-up above (barriers, tensor memory) may overlap the
   // previous kernel in the stream; nothing in global memory is touched before it has completed
   ptx::grid_dependency_wait();

@@ -120,6 +120,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
 }
 
 // 3-D tiled tensor load (x innermost); same completion mechanism
+// L2 prefetch of the box that tma_load_3d with the same coordinates loads: no shared memory, no
+// barrier, a hint.  The load still reads the lines (from L2 if they arrived), so a prefetch issued
+// before the grid dependency resolves cannot return stale data: L2 is where every write lands.
+__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+               ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int x, int y, int z,
                                             uint64_t policy) {
   asm volatile(
