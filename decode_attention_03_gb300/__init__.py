@@ -1,8 +1,10 @@
 """GB300-native (sm_103a) GQA split-KV decode attention.
 
 The compute lives in ``libgqa_decode.so`` (C ABI, ``include/gqa_decode.h``):
-hand-written CUDA kernels for the split-KV partial pass with its in-kernel
-online-softmax merge, the paged (block-table) variant and the standalone merge.
+hand-written CUDA kernels for the split-KV partial pass (mma.sync with TMA, and
+tcgen05 with tensor memory), the online-softmax merge of its splits (inside a
+thread-block cluster, or a merge kernel), the paged (block-table) variant and the
+standalone merge.
 This package is the thin Python binding (``_binding``), loaded on first use of
 any of its names; it raises if the library has not been built -- there is no
 fallback path.  ``build`` compiles the library in-tree.
