@@ -43,7 +43,8 @@ def assert_close(got, ref, where):
 
 @pytest.mark.parametrize("shape,kw", [((1, 16, 6000, 64, 8, 128), {}),                  # tcgen05 + merge kernel
                                       ((2, 1, 4096, 8, 2, 64), {"n_splits": 64}),       # one-tile splits + merge
-                                      ((2, 1, 9000, 32, 8, 128), {})])                  # in-kernel merge
+                                      ((2, 1, 9000, 32, 8, 128), {}),                   # cluster
+                                      ((2, 1, 9000, 32, 8, 128), {"merge_mode": 2})])   # last-CTA fold
 def test_graph_replay_contiguous(gqa, shape, kw):
     B, T, S, hq, hkv, D = shape
     x = gi.make_contiguous(gi.custom(B, T, S, hq, hkv, D, 4000 + S))
@@ -138,7 +139,8 @@ def test_cached_workspace_on_a_side_stream(gqa):
 
 
 # ---------------------------------------------------------------- programmatic dependent launches
-@pytest.mark.parametrize("kw", [{}, {"n_splits": 64, "merge_mode": 1}, {"merge_mode": 3}, {"mma_path": 2}])
+@pytest.mark.parametrize("kw", [{}, {"n_splits": 64, "merge_mode": 1}, {"merge_mode": 3}, {"mma_path": 2},
+                                {"mma_path": 1}, {"mma_path": 1, "n_splits": 5, "merge_mode": 2}])
 def test_dependent_launch_reads_the_previous_kernels_output(gqa, kw):
     """Every decode kernel may begin while the previous kernel in the stream finishes, and waits
     (griddepcontrol.wait) before it reads global memory.  Chain the library's own kernels -- the merge
@@ -179,3 +181,41 @@ def test_dependent_launch_reads_the_previous_kernels_output(gqa, kw):
     assert_close(q2, r2, f"decode of the merge output {kw}")
     r3 = oracle.decode(q2.cpu().numpy(), x["k"], x["v"], hq, hkv, D, x["scale"])
     assert_close(q3, r3, f"decode of the decode output {kw}")
+
+
+@pytest.mark.parametrize("shape", ["deep", (1, 4, 20000, 64, 8, 128), (8, 1, 4096, 32, 8, 128)])
+def test_keys_written_by_the_previous_kernel(gqa, shape):
+    """The split and tcgen05 kernels prefetch their first K/V boxes into L2 before their dependency
+    wait, while the previous kernel may still run.  Here that kernel (gqa_merge, which signals its
+    dependents at its start) writes the very K buffer the decode reads, over NaN: the decode must
+    see the written keys.  Shapes: the deep-ring split kernel, the tcgen05 kernel, the cluster."""
+    if shape == "deep":
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        if sms % 8 or sms // 8 <= 16:
+            pytest.skip("no deep-ring grid for 8 units on this GPU")
+        shape = (1, 1, (sms // 8) * 48 * 64 + 37, 32, 8, 128)
+    B, T, S, hq, hkv, D = shape
+    x = gi.make_contiguous(gi.custom(B, T, S, hq, hkv, D, 4500 + S))
+    ref = oracle.decode(x["q"], x["k"], x["v"], hq, hkv, D, x["scale"])
+    q, k, v = cuda(x["q"]), cuda(x["k"]), cuda(x["v"])
+    R = B * S * hkv
+    # one partial per row with m = 0, l = 1: the merge writes O = the keys (f16 -> f32 -> f16 exact)
+    m = torch.zeros(1, R, device="cuda")
+    l = torch.ones(1, R, device="cuda")
+    op = k.float().reshape(1, R, D)
+    kbuf = torch.empty_like(k)
+    out = torch.empty_like(q)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):   # set-up outside the chain: the stream's cached workspace, first use
+        gqa.gqa_decode(q, k, v, hq, hkv, x["scale"], out=out, stream=s)
+    torch.cuda.synchronize()
+    for it in range(3):
+        with torch.cuda.stream(s):
+            kbuf.fill_(float("nan"))
+            out.fill_(float("nan"))
+            torch.cuda._sleep(5_000_000)   # queue both calls before the merge runs
+            gqa.gqa_merge(m, l, op, out=kbuf.view(R, D), stream=s)
+            gqa.gqa_decode(q, kbuf, v, hq, hkv, x["scale"], out=out, stream=s)
+        torch.cuda.synchronize()
+        assert torch.equal(kbuf, k), "merge output"
+        assert_close(out, ref, f"decode of keys written just before it, {shape}, pass {it}")
