@@ -444,6 +444,132 @@ __device__ __forceinline__ void consume_tile(WarpState<D, NT>& st, uint32_t kbas
   }
 }
 
+// Two 16-key slices of one stage at once (row layout): the warp's slices ks[0] and ks[1] of a
+// stage of two 64-key tiles (d_head 64), with the same arithmetic as consume_tile on both -- the
+// two slices' S products in flight together, one running-max update, rescale and l update for the
+// 32 keys, then both P.V products -- so that the two slices' dependent chains overlap instead of
+// running back to back.  Slice 1 holds keys (valid[1] > 0) only when slice 0 is whole.
+template <int D, int NT, int BOXP, bool CAUSAL = false, bool BF16 = false>
+__device__ __forceinline__ void consume_tile2(WarpState<D, NT>& st, uint32_t kbase, uint32_t vbase,
+                                              const int (&valid)[2], const int (&key0)[2], const int (&ks)[2],
+                                              int lane, float scale_log2, int rb, const Win& ring) {
+  constexpr int KD = WarpState<D, NT>::KD;
+  const int gq = lane >> 2;
+  const int k_c0 = lane >> 4;
+  const int v_c0 = (lane >> 3) & 1;
+  const int plane = rb * 128;
+  int k_row[2], v_row[2], k_off[2], v_off[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    k_row[u] = ks[u] * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    v_row[u] = ks[u] * 16 + (lane & 7) + ((lane >> 4) & 1) * 8;
+    k_off[u] = row_offset<BOXP>(k_row[u], rb);
+    v_off[u] = row_offset<BOXP>(v_row[u], rb);
+  }
+
+  // ---- S^T = K Q^T for both slices: 2 x 16 keys x 8*NT query rows, fp32
+  float sc[2][NT][4];
+#pragma unroll
+  for (int u = 0; u < 2; ++u)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) sc[u][nt][0] = sc[u][nt][1] = sc[u][nt][2] = sc[u][nt][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < KD; ++kk) {
+    uint32_t af[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      ptx::ldmatrix_x4(af[u], smem_clamp(chunk_addr(kbase, k_off[u], k_row[u], kk * 2 + k_c0, plane), 16, ring.lo,
+                                         ring.hi, ring.status));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      Elem<BF16>::mma(sc[0][nt], af[0], st.qf[nt][kk]);
+      Elem<BF16>::mma(sc[1][nt], af[1], st.qf[nt][kk]);
+    }
+  }
+  // ---- scale (log2 domain) and mask each slice; sc[u][nt][c]: key gq (c<2) or gq+8 of slice u,
+  //      query row 2*tq4 + (c&1) of n-tile nt
+#pragma unroll
+  for (int u = 0; u < 2; ++u)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      if constexpr (CAUSAL) {
+        const int last0 = min(valid[u] - 1, st.lim[nt][0] - key0[u]);
+        const int last1 = min(valid[u] - 1, st.lim[nt][1] - key0[u]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int key = gq + ((c >> 1) << 3);
+          sc[u][nt][c] = key <= ((c & 1) ? last1 : last0) ? sc[u][nt][c] * scale_log2 : -CUDART_INF_F;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int key = gq + ((c >> 1) << 3);
+          sc[u][nt][c] = key < valid[u] ? sc[u][nt][c] * scale_log2 : -CUDART_INF_F;
+        }
+      }
+    }
+  // ---- online softmax over the 32 keys
+  float alpha[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float mx = fmaxf(fmaxf(sc[0][nt][j], sc[0][nt][j + 2]), fmaxf(sc[1][nt][j], sc[1][nt][j + 2]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(st.m_run[nt][j], mx);
+      const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
+      alpha[nt][j] = ptx::ex2(st.m_run[nt][j] - m_use);
+      st.m_run[nt][j] = m_new;
+      const float p00 = ptx::ex2(sc[0][nt][j] - m_use), p01 = ptx::ex2(sc[0][nt][j + 2] - m_use);
+      const float p10 = ptx::ex2(sc[1][nt][j] - m_use), p11 = ptx::ex2(sc[1][nt][j + 2] - m_use);
+      st.l_run[nt][j] = st.l_run[nt][j] * alpha[nt][j] + ((p00 + p01) + (p10 + p11));
+      sc[0][nt][j] = p00;
+      sc[0][nt][j + 2] = p01;
+      sc[1][nt][j] = p10;
+      sc[1][nt][j + 2] = p11;
+    }
+  // ---- rescale O^T when a running max of the warp moved (as consume_tile)
+  bool moved = false;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) moved |= (alpha[nt][0] != 1.f) | (alpha[nt][1] != 1.f);
+  if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+    for (int i = 0; i < KD; ++i)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        st.acc[i][nt][0] *= alpha[nt][0];
+        st.acc[i][nt][1] *= alpha[nt][1];
+        st.acc[i][nt][2] *= alpha[nt][0];
+        st.acc[i][nt][3] *= alpha[nt][1];
+      }
+  }
+  // ---- P^T of both slices as B operands
+  uint32_t pf[2][NT][2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      pf[u][nt][0] = ptx::movmatrix_trans(Elem<BF16>::pack(sc[u][nt][0], sc[u][nt][1]));
+      pf[u][nt][1] = ptx::movmatrix_trans(Elem<BF16>::pack(sc[u][nt][2], sc[u][nt][3]));
+    }
+  // ---- O^T += V^T P^T, slice 0 then slice 1 into each accumulator
+#pragma unroll
+  for (int i = 0; i < KD; ++i) {
+    uint32_t af[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      ptx::ldmatrix_x4_trans(af[u], smem_clamp(chunk_addr(vbase, v_off[u], v_row[u], i * 2 + v_c0, plane), 16,
+                                               ring.lo, ring.hi, ring.status));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      Elem<BF16>::mma(st.acc[i][nt], af[0], pf[0][nt]);
+      Elem<BF16>::mma(st.acc[i][nt], af[1], pf[1][nt]);
+    }
+  }
+}
+
 // =====================================================================================
 // end of a slice: merge the key-slice warps, emit, merge the unit's slices
 // =====================================================================================
@@ -1063,15 +1189,34 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     }
     const uint32_t kbase = ptx::smem_u32(smem + s * STB);
     const uint32_t vbase = kbase + KVB;
+    if constexpr (SUB == 2) {
+      // both of the warp's slices of the stage (tiles 0 and 1) in one step where both hold keys
+      const int kr[2] = {ks, kWK + ks};
+      int key0[2], valid[2];
 #pragma unroll
-    for (int sub = 0; sub < SUB; ++sub) {
-      const int kr = sub * kWK + ks;                      // 16-key slice of the stage's box rows
-      const int64_t key0 = key_begin + (int64_t)it * SROWS + kr * 16;
-      const int valid = (int)max((int64_t)0, min((int64_t)16, key_end - key0));
-      if (valid < 16) zero_masked_v<C::HALVES, C::HALVES>(smem + s * STB + KVB, kr, valid, lane, SROWS, ring);
-      if (valid > 0)
-        consume_tile<D, NT, C::HALVES, CAUSAL, BF16>(st, kbase, vbase, valid, (int)key0, kr, lane, a.scale_log2,
-                                                     SROWS, ring);
+      for (int u = 0; u < 2; ++u) {
+        const int64_t k0 = key_begin + (int64_t)it * SROWS + kr[u] * 16;
+        key0[u] = (int)k0;
+        valid[u] = (int)max((int64_t)0, min((int64_t)16, key_end - k0));
+        if (valid[u] < 16) zero_masked_v<C::HALVES, C::HALVES>(smem + s * STB + KVB, kr[u], valid[u], lane, SROWS, ring);
+      }
+      if (valid[1] > 0)
+        consume_tile2<D, NT, C::HALVES, CAUSAL, BF16>(st, kbase, vbase, valid, key0, kr, lane, a.scale_log2, SROWS,
+                                                      ring);
+      else if (valid[0] > 0)
+        consume_tile<D, NT, C::HALVES, CAUSAL, BF16>(st, kbase, vbase, valid[0], key0[0], kr[0], lane,
+                                                     a.scale_log2, SROWS, ring);
+    } else {
+#pragma unroll
+      for (int sub = 0; sub < SUB; ++sub) {
+        const int kr = sub * kWK + ks;                      // 16-key slice of the stage's box rows
+        const int64_t key0 = key_begin + (int64_t)it * SROWS + kr * 16;
+        const int valid = (int)max((int64_t)0, min((int64_t)16, key_end - key0));
+        if (valid < 16) zero_masked_v<C::HALVES, C::HALVES>(smem + s * STB + KVB, kr, valid, lane, SROWS, ring);
+        if (valid > 0)
+          consume_tile<D, NT, C::HALVES, CAUSAL, BF16>(st, kbase, vbase, valid, (int)key0, kr, lane, a.scale_log2,
+                                                       SROWS, ring);
+      }
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(empty + s));
