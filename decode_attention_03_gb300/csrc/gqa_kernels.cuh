@@ -1189,8 +1189,11 @@ gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     }
     const uint32_t kbase = ptx::smem_u32(smem + s * STB);
     const uint32_t vbase = kbase + KVB;
-    if constexpr (SUB == 2) {
+    if constexpr (SUB == 2 && WN == 1) {
       // both of the warp's slices of the stage (tiles 0 and 1) in one step where both hold keys
+      // (measured on GB300 for one warp column, up to 16 rows: the tiny workload's L2-resident step
+      // 4.35 -> 4.10 us, 16 rows at 2^18 keys 90.3 -> 82.7 us; with two or four warp columns it
+      // made each CTA slower, 32 rows at 19 splits 105.6 -> 144.2 us)
       const int kr[2] = {ks, kWK + ks};
       int key0[2], valid[2];
 #pragma unroll
