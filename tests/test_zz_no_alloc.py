@@ -44,7 +44,8 @@ def _rel_l2(a, b):
     return float((a - b).norm() / b.norm())
 
 
-@pytest.mark.parametrize("shape", [(2, 1, 5000, 32, 8, 128), (1, 4, 131071, 64, 8, 128), (1, 1, 4096, 8, 2, 64)])
+@pytest.mark.parametrize("shape", [(2, 1, 5000, 32, 8, 128), (1, 4, 131071, 64, 8, 128), (1, 1, 4096, 8, 2, 64),
+                                   (1, 1, 19 * 48 * 64 + 37, 32, 8, 128)])   # 152 SMs: the deep ring + merge kernel
 def test_noalloc_matches_regular_entry_point_twice(lib, shape):
     B, T_q, S, hq, hkv, D = shape
     x = gi.make_contiguous(gi.custom(B, T_q, S, hq, hkv, D, 1234 + S))
