@@ -67,7 +67,11 @@ typedef enum {
 
 /* Optional knobs for tests and benchmarks (NULL = defaults everywhere). */
 typedef struct {
-  int n_splits;          /* contiguous calls: splits per (sequence, KV head); 0 = heuristic */
+  int n_splits;          /* contiguous calls: splits per (sequence, KV head); 0 = automatic: about
+                            1.25 CTAs per SM, or, where the (sequence, KV head) units divide the
+                            SM count into more than 16 splits of at least 48 64-key tiles (d_head
+                            128, up to 8 rows, no causal tail), one CTA per SM running a deeper
+                            ring; a forced count keeps the plain kernel */
   int merge_mode;        /* how a unit's splits are folded.  0 = automatic: on the mma.sync kernel
                             a cluster (3) for 2 to 16 splits where the cluster variant keeps the
                             plain kernel's ring depth (not at d_head 128 with more than 32 rows)
@@ -117,8 +121,9 @@ int gqa_version(void);
  * compiled with GQA_BOUNDS_CHECK=1; slower, for tests and debugging), 0 for the regular one. */
 int gqa_build_flags(void);
 
-/* Splits per (sequence, KV head) the heuristic picks on the current device for a contiguous
- * call sweeping S_kv keys; <= 0 on invalid arguments or when no device is usable. */
+/* Splits per (sequence, KV head) the automatic plan picks on the current device for a contiguous
+ * call with default options sweeping S_kv keys (gqa_options.n_splits); <= 0 on invalid arguments
+ * or when no device is usable. */
 int gqa_decode_num_splits(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head);
 
 /* What a gqa_decode_ex call with these shapes and options (NULL = defaults) launches on the current
