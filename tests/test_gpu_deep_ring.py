@@ -106,3 +106,30 @@ def test_deep_ring_timeout_is_reported_not_hung(gqa):
     o = gqa.gqa_decode(q, k, v, 32, 8, x["scale"], workspace_tensor=ws)
     assert gqa.gqa_workspace_check(ws) == gqa.GQA_OK
     assert_close(o, ref_contig(x), "deep ring after a timeout")
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_deep_ring_random_shapes(gqa, seed):
+    """Seeded random shapes the deep ring serves: (sequences, KV heads) giving 1, 2, 4 or 8 units,
+    G * T_q up to 8 rows, f16 or bf16, a ragged number of keys of at least 48 tiles per split."""
+    rng = np.random.default_rng(7300 + seed)
+    B, hkv = [(1, 1), (2, 1), (1, 2), (1, 4), (2, 2), (4, 2), (8, 1), (2, 4)][rng.integers(8)]
+    n = _deep_splits(B * hkv)
+    if n is None:
+        pytest.skip("no deep-ring grid for these units on this GPU")
+    G, T = [(1, 1), (2, 1), (4, 1), (8, 1), (2, 2), (4, 2), (1, 8)][rng.integers(7)]
+    S = n * 64 * int(rng.integers(48, 56)) + int(rng.integers(0, 64))
+    elem = "bf16" if rng.integers(2) else "f16"
+    x = gi.make_contiguous(gi.custom(B, T, S, G * hkv, hkv, 128, 7400 + seed, elem=elem))
+    assert gqa.gqa_decode_plan(B, T, S, G * hkv, hkv, 128)[0] == n
+    where = f"deep ring B={B} h_kv={hkv} G={G} T={T} S={S} {elem}"
+    if elem == "f16":
+        assert_close(run_contig(gqa, x), ref_contig(x), where)
+    else:
+        vals = {c: gi.values(x[c], "bf16") for c in ("q", "k", "v")}
+        ref = oracle.decode(vals["q"], vals["k"], vals["v"], G * hkv, hkv, 128, x["scale"])
+        q, k, v = (torch.from_numpy(np.ascontiguousarray(x[c]).view(np.int16)).cuda().view(torch.bfloat16)
+                   for c in ("q", "k", "v"))
+        o = gqa.gqa_decode(q, k, v, G * hkv, hkv, x["scale"])
+        torch.cuda.synchronize()
+        assert_close_bf16(o, ref, where)
