@@ -404,6 +404,7 @@ def main():
     d = to_device(x, dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     big = bytes_step > 2 * l2
+    variant = {}     # which kernel variant and fold a contiguous step runs (gqa_decode_plan_ex)
     stream = torch.cuda.Stream(dev)
     out = torch.empty(w.batch * w.T_q * w.h_q * w.d_head, dtype=torch.bfloat16 if w.elem == "bf16" else torch.float16,
                       device=dev)
@@ -415,9 +416,10 @@ def main():
         contig_launches += 1                              # the merge of the ranks' partials
     elif w.kind == "contiguous":
         nbytes = pkg.gqa_decode_workspace_size(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head, args.n_splits)
-        n_splits, mma_path, contig_launches = pkg.gqa_decode_plan(
-            w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head, n_splits=args.n_splits, merge_mode=args.merge_mode,
-            mma_path=args.mma_path)
+        plan = pkg.gqa_decode_plan(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head, n_splits=args.n_splits,
+                                   merge_mode=args.merge_mode, mma_path=args.mma_path, detail=True)
+        n_splits, mma_path, contig_launches = plan["n_splits"], plan["mma_path"], plan["launches"]
+        variant = {"kernel_variant": plan["kernel"], "fold": plan["fold"]}
     else:
         nbytes = pkg.gqa_paged_workspace_size(w.batch, w.h_q, w.h_kv, w.d_head, x["max_seq_len"], w.partition_size)
         n_splits, mma_path, contig_launches = None, 0, 0
@@ -539,7 +541,8 @@ def main():
             "warmup": warm, "ms_per_step": round(ms_step, 6), "us_per_step": round(ms_step * 1e3, 3),
             "higher_is_better": True, "scaling": "strong" if shard is not None else "weak", "vs_baseline": None,
             "dtype": w.elem, "data": "synthetic",
-            "config": dict(config_of(w, x, n_splits, shard_world=world if shard is not None else None), accum="f32",
+            "config": dict(config_of(w, x, n_splits, shard_world=world if shard is not None else None), **variant,
+                           accum="f32",
                            l2=("inputs larger than L2, no flush" if flush is None
                                else f"L2 flushed ({2 * l2 >> 20} MiB write) before every timed step, outside events")),
             "roofline": {"bound": "hbm", "achieved": round(per_launch_gbs, 2), "peak": peak, "unit": "GB/s",

@@ -62,6 +62,7 @@ _SIGS = {
     "gqa_build_flags": ([], _i),
     "gqa_decode_num_splits": ([_i, _i, _i64, _i, _i, _i], _i),
     "gqa_decode_plan": ([_i, _i, _i64, _i, _i, _i, _opt, _p, _p, _p], _i),
+    "gqa_decode_plan_ex": ([_i, _i, _i64, _i, _i, _i, _opt, _p, _p, _p, _p, _p], _i),
     "gqa_paged_plan": ([_i, _i, _i, _i, _i, _i, _i, _i, _opt, _p, _p, _p], _i),
     "gqa_decode_workspace_size": ([_i, _i, _i64, _i, _i, _i, _i], _sz),
     "gqa_workspace_size": ([_i, _i, _i64, _i, _i, _i], _sz),
@@ -203,14 +204,23 @@ def gqa_paged_plan(num_seqs, h_q, h_kv, d_head, max_seq_len, partition_size=0, *
     return part.value, hg.value, launches.value
 
 
-def gqa_decode_plan(batch, T_q, S_kv, h_q, h_kv, d_head, *, n_splits=0, merge_mode=0, mma_path=0, causal=False):
+KERNELS = {0: "split", 1: "split-cluster", 2: "split-deep-ring", 3: "tcgen05"}   # GQA_KERNEL_*
+FOLDS = {0: "none", 1: "cluster", 2: "merge-kernel", 3: "last-cta"}                # GQA_FOLD_*
+
+
+def gqa_decode_plan(batch, T_q, S_kv, h_q, h_kv, d_head, *, n_splits=0, merge_mode=0, mma_path=0, causal=False,
+                    detail=False):
     """(n_splits, mma_path, launches) of a gqa_decode call with these shapes and options on the current
-    device: mma_path 1 = mma.sync split kernel, 2 = tcgen05 kernel; launches 2 with the merge kernel."""
+    device: mma_path 1 = mma.sync split kernel, 2 = tcgen05 kernel; launches 2 with the merge kernel.
+    ``detail``: a dict with those and the kernel variant and fold (names from KERNELS and FOLDS)."""
     opt = _opts(n_splits, merge_mode, causal=causal, mma_path=mma_path)
-    n, path, launches = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
-    st = lib.gqa_decode_plan(batch, T_q, S_kv, h_q, h_kv, d_head, ctypes.byref(opt), ctypes.byref(n),
-                             ctypes.byref(path), ctypes.byref(launches))
-    _check(st, "gqa_decode_plan")
+    n, path, launches, kernel, fold = (ctypes.c_int(0) for _ in range(5))
+    st = lib.gqa_decode_plan_ex(batch, T_q, S_kv, h_q, h_kv, d_head, ctypes.byref(opt), ctypes.byref(n),
+                                ctypes.byref(path), ctypes.byref(launches), ctypes.byref(kernel), ctypes.byref(fold))
+    _check(st, "gqa_decode_plan_ex")
+    if detail:
+        return {"n_splits": n.value, "mma_path": path.value, "launches": launches.value,
+                "kernel": KERNELS[kernel.value], "fold": FOLDS[fold.value]}
     return n.value, path.value, launches.value
 
 

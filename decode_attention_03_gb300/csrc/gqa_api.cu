@@ -776,8 +776,9 @@ int gqa_decode_num_splits(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, i
   }
 }
 
-gqa_status gqa_decode_plan(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head, const gqa_options* opt,
-                           int* n_splits, int* mma_path, int* launches) {
+gqa_status gqa_decode_plan_ex(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head,
+                              const gqa_options* opt, int* n_splits, int* mma_path, int* launches, int* kernel,
+                              int* fold) {
   try {
     const gqa_options o = opt ? *opt : defaults();
     if (S_kv < 1 || batch < 1 || o.merge_mode < 0 || o.merge_mode > 3) return GQA_ERR_INVALID_ARG;
@@ -785,13 +786,26 @@ gqa_status gqa_decode_plan(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, 
     gqa_status s = plan_contig(batch, T_q, S_kv, 0, S_kv, h_q, h_kv, d_head, o.n_splits, true, &p, o.mma_path,
                                o.merge_mode, o.causal != 0);
     if (s != GQA_OK) return s;
+    const bool in_kernel = merge_in_kernel(p, o.merge_mode);
     if (n_splits) *n_splits = p.n_splits;
     if (mma_path) *mma_path = p.tc ? 2 : 1;
-    if (launches) *launches = (p.n_splits > 1 && !merge_in_kernel(p, o.merge_mode)) ? 2 : 1;
+    if (launches) *launches = (p.n_splits > 1 && !in_kernel) ? 2 : 1;
+    if (kernel)
+      *kernel = p.tc ? GQA_KERNEL_TCGEN05
+                     : (p.cluster ? GQA_KERNEL_SPLIT_CLUSTER : (p.deep ? GQA_KERNEL_SPLIT_DEEP : GQA_KERNEL_SPLIT));
+    if (fold)
+      *fold = p.n_splits <= 1 ? GQA_FOLD_NONE
+                              : (p.cluster ? GQA_FOLD_CLUSTER : (in_kernel ? GQA_FOLD_LAST_CTA : GQA_FOLD_MERGE_KERNEL));
     return GQA_OK;
   } catch (...) {
     return GQA_ERR_CUDA;
   }
+}
+
+gqa_status gqa_decode_plan(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head, const gqa_options* opt,
+                           int* n_splits, int* mma_path, int* launches) {
+  return gqa_decode_plan_ex(batch, T_q, S_kv, h_q, h_kv, d_head, opt, n_splits, mma_path, launches, nullptr,
+                            nullptr);
 }
 
 size_t gqa_decode_workspace_size(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head, int n_splits) {

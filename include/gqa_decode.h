@@ -132,6 +132,23 @@ int gqa_decode_num_splits(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, i
 gqa_status gqa_decode_plan(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head, const gqa_options* opt,
                            int* n_splits, int* mma_path, int* launches);
 
+/* Decode kernel of a contiguous call (gqa_decode_plan_ex). */
+#define GQA_KERNEL_SPLIT 0         /* mma.sync split kernel, about 1.25 CTAs per SM */
+#define GQA_KERNEL_SPLIT_CLUSTER 1 /* its cluster variant: a unit's splits are the CTAs of one cluster */
+#define GQA_KERNEL_SPLIT_DEEP 2    /* its deep-ring variant: one CTA per SM, a deeper TMA ring */
+#define GQA_KERNEL_TCGEN05 3       /* tcgen05 kernel, accumulators in tensor memory */
+/* How the splits of a unit are folded (gqa_decode_plan_ex). */
+#define GQA_FOLD_NONE 0            /* one split: the kernel normalises and writes the output */
+#define GQA_FOLD_CLUSTER 1         /* in the cluster, through distributed shared memory */
+#define GQA_FOLD_MERGE_KERNEL 2    /* by the merge kernel, launched as a programmatic dependent */
+#define GQA_FOLD_LAST_CTA 3        /* by the unit's last-arriving CTA (merge_mode 2) */
+
+/* gqa_decode_plan, and which kernel runs (GQA_KERNEL_*) and how its splits are folded (GQA_FOLD_*).
+ * No counterpart on the pages: a query of this library's own plan.  Output pointers may be NULL. */
+gqa_status gqa_decode_plan_ex(int batch, int T_q, int64_t S_kv, int h_q, int h_kv, int d_head,
+                              const gqa_options* opt, int* n_splits, int* mma_path, int* launches, int* kernel,
+                              int* fold);
+
 /* Workspace bytes for gqa_decode / gqa_decode_partial on the current device, sweeping S_kv
  * keys (for a partial call pass s_len).  n_splits = 0 sizes for the heuristic; a positive
  * value sizes for that forced split count.  Returns 0 on invalid arguments.  The workspace

@@ -78,6 +78,14 @@ def test_validation_codes_without_gpu(binding):
     assert dec(T=0) == binding.GQA_ERR_INVALID_ARG
     assert dec(q=None) == binding.GQA_ERR_INVALID_ARG                # null pointer
     assert dec(q=ctypes.c_void_p(p.value + 2)) == binding.GQA_ERR_INVALID_ARG   # misaligned
+    # the plan query validates before it asks the device
+    outs = [ctypes.c_int(-7) for _ in range(5)]
+    assert lib.gqa_decode_plan_ex(1, 1, 0, 8, 2, 64, None, *(ctypes.byref(o) for o in outs)) == \
+        binding.GQA_ERR_INVALID_ARG
+    bad = binding._opts(merge_mode=4)
+    assert lib.gqa_decode_plan_ex(1, 1, 16, 8, 2, 64, ctypes.byref(bad), *(ctypes.byref(o) for o in outs)) == \
+        binding.GQA_ERR_INVALID_ARG
+    assert all(o.value == -7 for o in outs)                          # nothing written on an error
     assert dec(B=0) == binding.GQA_OK                                # empty batch: no-op
     assert dec(B=2, S=(1 << 30)) == binding.GQA_ERR_INVALID_ARG      # batch*S_kv >= 2^31
     assert lib.gqa_decode(p, p, p, p, 1, 1, 16, 8, 2, 64, float("nan"), p, 4096, st) == binding.GQA_ERR_INVALID_ARG

@@ -133,3 +133,19 @@ def test_deep_ring_random_shapes(gqa, seed):
         o = gqa.gqa_decode(q, k, v, G * hkv, hkv, x["scale"])
         torch.cuda.synchronize()
         assert_close_bf16(o, ref, where)
+
+
+def test_plan_names_the_kernel_and_fold_of_each_workload(gqa):
+    """gqa_decode_plan_ex: the kernel variant and fold the automatic plan picks for the workloads."""
+    def plan(name, **kw):
+        w = gi.WORKLOADS[name]
+        return gqa.gqa_decode_plan(w.batch, w.T_q, w.S_kv, w.h_q, w.h_kv, w.d_head, detail=True, **kw)
+    assert plan("tiny")["kernel"] == "split-cluster" and plan("tiny")["fold"] == "cluster"
+    assert plan("llama8b")["kernel"] == "split-cluster" and plan("llama8b")["fold"] == "cluster"
+    for name in ("ragged", "verify16"):
+        assert plan(name)["kernel"] == "tcgen05" and plan(name)["fold"] == "merge-kernel"
+    long = plan("long")
+    assert long["fold"] == "merge-kernel"
+    assert long["kernel"] == ("split-deep-ring" if _deep_splits(8) else "split")
+    assert plan("long", merge_mode=2)["fold"] == "last-cta" and plan("long", merge_mode=2)["kernel"] == "split"
+    assert plan("long", n_splits=1)["fold"] == "none"
