@@ -340,13 +340,11 @@ gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ C
         ptx::tc_fence_after();
         float x[kTcKeys];   // raw scores q.k of this row against the tile's keys
         {
-          uint32_t u[32];
-          ptx::tmem_ld32(tmem_s, u);
+          static_assert(kTcKeys == 64, "one 64-column load per tile");
+          uint32_t u[64];
+          ptx::tmem_ld64(tmem_s, u);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(u[j]);
-          ptx::tmem_ld32(tmem_s + 32, u);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) x[32 + j] = __uint_as_float(u[j]);
+          for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(u[j]);
         }
         ptx::tc_fence_before();
         __syncwarp();
