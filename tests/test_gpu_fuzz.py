@@ -88,7 +88,7 @@ def _contig_cases(n, seed):
     return cases
 
 
-CONTIG = _contig_cases(120, 4242)
+CONTIG = _contig_cases(300, 4242)
 
 
 def _cluster_cases(n, seed):
@@ -115,7 +115,7 @@ def _cluster_cases(n, seed):
     return cases
 
 
-CLUSTER = _cluster_cases(40, 4545)
+CLUSTER = _cluster_cases(100, 4545)
 
 
 @pytest.mark.parametrize("c", CONTIG + CLUSTER,
@@ -186,7 +186,7 @@ def _paged_cases(n, seed):
     return cases
 
 
-PAGED = _paged_cases(80, 4343)
+PAGED = _paged_cases(150, 4343)
 
 
 @pytest.mark.parametrize("c", PAGED, ids=[f"p{i:02d}" for i in range(len(PAGED))])
